@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for the CSA decode step.
+
+This module only draws random numbers and lays them out in the caller-owned
+pools the library reads.  It holds none of the method's arithmetic: no score,
+no selection, no softmax, no rotary math.  Both the CUDA path and the CPU
+oracle are fed from here, so the two always see identical stored values.
+
+Shapes follow the decode workloads of the hw-native-sys/pypto-lib pages
+("Perf: skip redundant CSA scoring and fuse gather unpack": TP4 CSA at 16x256;
+"Perf: fuse HCA merge, inverse RoPE, and packing": B=16, S=8) extended to long
+ragged contexts.  No dataset or trained weight is involved.
+
+Pool layout (the storage contract of the library):
+  * compressed pool ``cmp_kv`` and indexer-key pool ``idx_k``: request b owns
+    floor(L_b / ratio) consecutive rows starting at ``cmp_off[b]`` /
+    ``idx_off[b]``;
+  * heavy-compression pool ``hca_kv``: floor(L_b / hca_ratio) rows;
+  * raw (sliding-window) pool ``raw_kv``: an SWA cache keeps only the last
+    ``raw_keep`` raw tokens of each request, so row r of request b lives at
+    ``raw_off[b] + r`` for r in [L_b - raw_keep, L_b) and is absent otherwise
+    (``raw_off[b]`` may therefore be negative).
+  ``gap_rows`` rows filled with NaN separate requests in every pool, so a read
+  of a row a query may not use poisons its output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class CsaConfig:
+    """Static shape of one CSA attention layer."""
+    H: int = 64            # attention heads
+    D: int = 576           # KV row width: V value dims + R rope dims
+    V: int = 512           # value / output dims
+    Hi: int = 64           # indexer heads
+    Di: int = 128          # indexer dim
+    ratio: int = 4         # CSA compression ratio
+    topk: int = 512        # K
+    win: int = 128         # sliding window WIN
+    hca_ratio: int = 0     # heavy-compression ratio (0 = no third stream)
+    dtype: str = "bf16"    # "bf16" or "f32"
+    rope_base: float = 10000.0
+    scale: float | None = None  # softmax scale; None -> 1/sqrt(D)
+
+    @property
+    def R(self) -> int:
+        return self.D - self.V
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+    @property
+    def torch_dtype(self):
+        return torch.bfloat16 if self.dtype == "bf16" else torch.float32
+
+    @property
+    def esize(self) -> int:
+        return 2 if self.dtype == "bf16" else 4
+
+
+@dataclass(frozen=True)
+class Dists:
+    """Standard deviations of the normal draws (w is U(0, w_hi))."""
+    q: float = 1.0
+    q_idx: float = 1.0
+    k_idx: float = 1.0
+    raw: float = 1.0
+    cmp: float = 0.5
+    hca: float = 0.5
+    w_hi: float = 1.0
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    cfg: CsaConfig
+    B: int
+    S: int
+    L: int | None = None            # fixed context length, or
+    L_range: tuple | None = None    # (lo, hi) inclusive, uniform per request
+    seed: int = 1000
+    dists: Dists = field(default_factory=Dists)
+    description: str = ""
+
+
+TINY_CFG = CsaConfig(H=4, D=80, V=64, Hi=2, Di=32, ratio=4, topk=8, win=8, dtype="f32")
+BF16_CFG = CsaConfig()
+
+WORKLOADS = {
+    "tiny_f32": Workload(
+        "tiny_f32", TINY_CFG, B=1, S=1, L=64, seed=1000,
+        dists=Dists(cmp=1.0, hca=1.0),
+        description="B=1 S=1 L=64 (16 compressed rows > K=8), WIN=8, H=4, D=80 (V=64 + rope 16), "
+                    "indexer 2x32, fp32, all N(0,1), w~U(0,1)"),
+    "bypass_b16_l256": Workload(
+        "bypass_b16_l256", BF16_CFG, B=16, S=1, L=256, seed=1001,
+        description="B=16 S=1 L=256: 64 compressed rows <= K=512 so scoring is skipped; WIN=128, "
+                    "H=64, D=576, bf16; activations N(0,1), compressed rows N(0,0.5^2)"),
+    "topk_b16_l8192": Workload(
+        "topk_b16_l8192", BF16_CFG, B=16, S=1, L=8192, seed=1002,
+        description="B=16 S=1 L=8192: 2048 compressed rows, K=512, WIN=128, H=64, D=576, bf16; "
+                    "q_idx, k_idx N(0,1) so the Top-K boundary is dense with near-ties"),
+    "long_ragged_b64": Workload(
+        "long_ragged_b64", BF16_CFG, B=64, S=1, L_range=(1024, 65536), seed=1003,
+        description="B=64 S=1, L_b ~ U{1024..65536}: 256..16384 compressed rows per request, "
+                    "K=512, WIN=128, H=64, D=576, indexer 64x128, bf16"),
+    "multitoken_hca_b16_s8": Workload(
+        "multitoken_hca_b16_s8", replace(BF16_CFG, hca_ratio=128), B=16, S=8, L=32768, seed=1004,
+        description="B=16 S=8 L=32768 with per-query causal visibility; CSA (ratio 4, K=512, "
+                    "WIN=128) plus all ratio-128 rows as a third stream; H=64, D=576, bf16"),
+}
+
+
+def context_lengths(wl: Workload, gen: torch.Generator) -> torch.Tensor:
+    if wl.L is not None:
+        return torch.full((wl.B,), wl.L, dtype=torch.int32)
+    lo, hi = wl.L_range
+    return torch.randint(lo, hi + 1, (wl.B,), generator=gen, dtype=torch.int64).to(torch.int32)
+
+
+def _normal(gen, shape, std, dtype):
+    t = torch.randn(*shape, generator=gen, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)
+
+
+def _pool(gen, counts, width, std, dtype, gap_rows, first=None):
+    """Concatenates per-request row blocks; returns (pool [rows, width], off int64 [B])."""
+    B = len(counts)
+    total = sum(counts) + gap_rows * (B + 1)
+    pool = torch.full((max(total, 1), width), float("nan"), dtype=dtype) if gap_rows else \
+        torch.empty((max(total, 1), width), dtype=dtype)
+    off = torch.zeros(B, dtype=torch.int64)
+    cur = gap_rows
+    for b, n in enumerate(counts):
+        if n:
+            pool[cur:cur + n] = _normal(gen, (n, width), std, dtype)
+        off[b] = cur - (first[b] if first is not None else 0)
+        cur += n + gap_rows
+    return pool, off
+
+
+def make_batch(wl: Workload, lens=None, seed: int | None = None, gap_rows: int = 0,
+               raw_keep: int | None = None, dists: Dists | None = None) -> dict:
+    """Host (CPU) tensors for one batch of `wl`.
+
+    lens: optional explicit per-request context lengths (overrides the
+    workload's).  raw_keep: trailing raw tokens stored per request (default:
+    WIN + S, enough for every window of the step).
+    """
+    cfg = wl.cfg
+    d = dists or wl.dists
+    gen = torch.Generator().manual_seed(wl.seed if seed is None else seed)
+    dt = cfg.torch_dtype
+    if lens is None:
+        ctx = context_lengths(wl, gen)
+    else:
+        ctx = torch.as_tensor(list(lens), dtype=torch.int32)
+    B, S = int(ctx.numel()), wl.S
+    assert int(ctx.min()) >= S, "every request must hold its S new tokens"
+    keep = raw_keep if raw_keep is not None else cfg.win + S
+    q = _normal(gen, (B, S, cfg.H, cfg.D), d.q, dt)
+    q_idx = _normal(gen, (B, S, cfg.Hi, cfg.Di), d.q_idx, dt)
+    w = (torch.rand(B, S, cfg.Hi, generator=gen, dtype=torch.float32) * d.w_hi).contiguous()
+    Ls = [int(x) for x in ctx]
+    first = [max(0, L - keep) for L in Ls]
+    raw_kv, raw_off = _pool(gen, [L - f for L, f in zip(Ls, first)], cfg.D, d.raw, dt, gap_rows, first)
+    ncmp = [L // cfg.ratio for L in Ls]
+    cmp_kv, cmp_off = _pool(gen, ncmp, cfg.D, d.cmp, dt, gap_rows)
+    idx_k, idx_off = _pool(gen, ncmp, cfg.Di, d.k_idx, dt, gap_rows)
+    batch = dict(B=B, S=S, ctx_len=ctx, q=q, q_idx=q_idx, w=w,
+                 raw_kv=raw_kv, raw_off=raw_off, raw_stride=cfg.D, raw_first=first,
+                 cmp_kv=cmp_kv, cmp_off=cmp_off, cmp_stride=cfg.D,
+                 idx_k=idx_k, idx_off=idx_off, idx_stride=cfg.Di,
+                 hca_kv=None, hca_off=None, hca_stride=0)
+    if cfg.hca_ratio:
+        nh = [L // cfg.hca_ratio for L in Ls]
+        hca_kv, hca_off = _pool(gen, nh, cfg.D, d.hca, dt, gap_rows)
+        batch.update(hca_kv=hca_kv, hca_off=hca_off, hca_stride=cfg.D)
+    return batch
+
+
+TENSOR_KEYS = ("ctx_len", "q", "q_idx", "w", "raw_kv", "raw_off", "cmp_kv", "cmp_off",
+               "idx_k", "idx_off", "hca_kv", "hca_off")
+
+
+def to_device(batch: dict, device) -> dict:
+    out = dict(batch)
+    for k in TENSOR_KEYS:
+        if batch.get(k) is not None:
+            out[k] = batch[k].to(device).contiguous()
+    return out
