@@ -1,0 +1,411 @@
+"""Benchmark of the CSA decode step on GB300.
+
+One step = the whole hot path (plan, indexer score, Top-K, gather + split
+softmax attention + LSE merge + inverse RoPE) over one batch of the long
+ragged workload (B=64, S=1, L_b ~ U{1024..65536}, H=64, D=576, K=512,
+WIN=128, bf16) through the C ABI.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Inputs are resident in HBM.  Every step reads a different one of several
+device copies of the batch, so each step's reads (about 190 MB) come from
+HBM, not from a warm L2.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="long_ragged_b64")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--copies", type=int, default=3, help="device copies of the inputs, rotated per step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        hbm = d.get("hbm_gbs")
+        if hbm:
+            return float(hbm), "measured", d
+    except Exception:
+        pass
+    return FALLBACK_HBM_GBS, "fallback", {}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what the step must move; the score scratch is not counted)
+
+def step_bytes(cfg, lens, S, topk_idx=None):
+    """Per-step algorithmic bytes and per-kernel shares for one batch.
+
+    Per query: q (H*D*e), output (H*V*e); per request, counted once: the
+    window rows and selected compressed rows it reads (union over its
+    queries), the indexer keys it scores and q_idx/w of scored queries, and
+    the heavy-compression rows.  topk_idx [B*S, K] (numpy) gives the selected
+    rows; without it every query is assumed to read min(vis, K) rows.
+    """
+    e = cfg.esize
+    tot_q = tot_rows = idx_b = 0
+    for b, L in enumerate(lens):
+        win_rows, sel, hca_rows, krows = set(), set(), 0, 0
+        for s in range(S):
+            pos = L - S + s
+            vis = (pos + 1) // cfg.ratio
+            nwin = min(cfg.win, pos + 1)
+            win_rows.update(range(pos - nwin + 1, pos + 1))
+            if topk_idx is not None:
+                row = topk_idx[b * S + s]
+                sel.update(int(x) for x in row[row >= 0])
+            else:
+                sel.update(range(min(vis, cfg.topk)))
+            if vis > cfg.topk:
+                krows = max(krows, vis)
+                idx_b += cfg.Hi * cfg.Di * e + 4 * cfg.Hi
+            if cfg.hca_ratio:
+                hca_rows = max(hca_rows, (pos + 1) // cfg.hca_ratio)
+        idx_b += krows * cfg.Di * e
+        tot_rows += len(win_rows) + len(sel) + hca_rows
+        tot_q += S
+    attn_b = tot_q * (cfg.H * cfg.D * e + cfg.H * cfg.V * e) + tot_rows * cfg.D * e
+    return {"total": attn_b + idx_b, "indexer": idx_b, "attention": attn_b}
+
+
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+def cpu_baseline(wl, hb, budget_s=6.0, nq=16):
+    """The oracle as it stands, on the host cores, over a bounded sample of queries."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    cores = os.cpu_count() or 1
+    T = hb["B"] * hb["S"]
+    qids = np.arange(min(nq, T), dtype=np.int32)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode(wl.cfg, hb, qids=qids, nthreads=cores)
+        done += qids.size
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": done / el, "unit": "queries/s", "cores": min(cores, qids.size), "kind": "oracle",
+            "sample": f"{qids.size} queries of {wl.name} (first {qids.size} requests, their full "
+                      f"context), repeated {done // qids.size}x, fp64 C oracle, {el:.1f} s wall"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from compressed_sparse_attention_indexer_gb300.workloads import WORKLOADS, make_batch
+    import numpy as np
+    import oracle
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    hb = make_batch(wl)
+    cores = os.cpu_count() or 1
+    T = hb["B"] * hb["S"]
+    nq = min(T, max(cores, 8))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        oracle.decode(wl.cfg, hb, qids=rng.choice(T, nq, replace=False).astype(np.int32), nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode(wl.cfg, hb, qids=rng.choice(T, nq, replace=False).astype(np.int32), nthreads=cores)
+    el = time.perf_counter() - t0
+    value = nq * args.steps / el
+    line = {"impl": "reference", "metric": "csa_decode_queries_per_s", "value": value,
+            "unit": "queries/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "B": hb["B"], "S": hb["S"],
+                       "description": wl.description},
+            "cpu_baseline": {"value": value, "unit": "queries/s", "cores": min(cores, nq), "kind": "oracle",
+                             "sample": f"{nq} random queries of {wl.name} per step (full context each)"},
+            "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def src_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str, workload: str):
+    """ncu-measured DRAM bytes per launch, if recorded for the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
+    try:
+        d = json.load(open(p))
+    except Exception:
+        return None
+    if d.get("source_sha") != src_sha(d.get("sources", [])):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+KERNEL_SOURCES = {
+    "indexer": ["compressed_sparse_attention_indexer_gb300/csrc/indexer.cu"],
+    "attention": ["compressed_sparse_attention_indexer_gb300/csrc/attention.cu"],
+    "topk": ["compressed_sparse_attention_indexer_gb300/csrc/topk.cu"],
+    "plan": ["compressed_sparse_attention_indexer_gb300/csrc/plan.cu"],
+}
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from compressed_sparse_attention_indexer_gb300 import build as csa_build
+    from compressed_sparse_attention_indexer_gb300 import csa
+    from compressed_sparse_attention_indexer_gb300.workloads import WORKLOADS, make_batch, to_device
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    csa_build.build()
+    wl = WORKLOADS[args.workload]
+    cfg = wl.cfg
+    # weak scaling: every rank decodes its own batch (different seed per rank)
+    hb = make_batch(wl, seed=wl.seed + 7919 * rank)
+    B, S = hb["B"], hb["S"]
+    T = B * S
+    lens = [int(x) for x in hb["ctx_len"]]
+    max_ctx = 65536 if args.workload == "long_ragged_b64" else max(lens)
+    copies = [to_device(hb, dev)]
+    for _ in range(args.copies - 1):
+        copies.append({k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in copies[0].items()})
+    lens_host = hb["ctx_len"].clone()
+    structs = [csa.make_batch_struct(c, lens_host) for c in copies]
+    dec = csa.Decoder(cfg, B, S, max_ctx)
+    out = torch.empty(B, S, cfg.H, cfg.V, dtype=cfg.torch_dtype, device=dev)
+    idx = torch.empty(B, S, cfg.topk, dtype=torch.int32, device=dev)
+    cnt = torch.empty(B, S, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        dec.decode_step(structs[i % len(structs)], out, None, idx, cnt, stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize()
+    st = dec.status()
+    if st != csa.CSA_OK:
+        raise RuntimeError(f"device status {st}: {csa.last_error()}")
+    launches_per_step = dec.last_launch_count()
+    sel = idx.cpu().numpy().reshape(T, cfg.topk)
+    bytes_ = step_bytes(cfg, lens, S, sel)
+
+    # ---- timed region: K steps
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+
+    # ---- per-kernel times (events around each launch, same stream), separate pass
+    dec.profile(True)
+    for i in range(args.steps):
+        step(i)
+    torch.cuda.synchronize()
+    prof = dec.profile_read()
+    dec.profile(False)
+    per_kernel_ms = {k: (v[0] / v[1] if v[1] else 0.0) for k, v in prof.items()}
+    dom = max(("indexer", "attention", "topk"), key=lambda k: prof[k][0])
+    peak, peak_kind, peaks = measured_peaks()
+    alg = bytes_[dom] if dom in bytes_ else None
+    if alg is not None:
+        achieved = alg / (per_kernel_ms[dom] * 1e-3) / 1e9
+    else:
+        achieved = None
+    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": (achieved / peak) if achieved else None, "peak_source": peak_kind,
+            "algorithmic_bytes_per_launch": alg,
+            "traffic": load_traffic(dom, args.workload),
+            "per_kernel_us": {k: round(v * 1e3, 3) for k, v in per_kernel_ms.items()},
+            "time_share": {k: round(v[0] / max(sum(x[0] for x in prof.values()), 1e-9), 4)
+                           for k, v in prof.items()},
+            "step_achieved_gbs": bytes_["total"] / (ms * 1e-3) / 1e9}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        keys = ("q", "q_idx", "w", "ctx_len", "raw_off", "cmp_off", "idx_off")
+        host = {k: hb[k].pin_memory() for k in keys}
+        out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+        d2h = out_host.numel() * out_host.element_size()
+        for i in range(3):
+            c = copies[i % len(copies)]
+            for k in keys:
+                c[k].copy_(host[k], non_blocking=True)
+            step(i)
+            out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            c = copies[i % len(copies)]
+            for k in keys:
+                c[k].copy_(host[k], non_blocking=True)
+            step(i)
+            out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": T * ws / (ems * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": ems,
+               "note": "per-step activations (q, q_idx, w, lengths, pool offsets) copied H2D from "
+                       "pinned memory and the output D2H each step; KV/indexer caches stay resident"}
+
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, hb)
+    foot = sum(v.numel() * v.element_size() for v in copies[0].values() if isinstance(v, torch.Tensor))
+    line = {
+        "metric": "csa_decode_queries_per_s", "value": T * ws / (ms * 1e-3), "unit": "queries/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic (seeded normal / uniform draws, shapes of the workload)",
+        "config": {"workload": wl.name, "B": B, "S": S, "H": cfg.H, "D": cfg.D, "K": cfg.topk,
+                   "WIN": cfg.win, "L_range": list(wl.L_range) if wl.L_range else wl.L,
+                   "sum_L": int(sum(lens)), "parallelism": f"replicas{ws}",
+                   "l2": f"inputs rotate over {len(copies)} device copies ({foot / 1e9:.2f} GB each); "
+                         f"each step reads ~{bytes_['total'] / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB",
+                   "algorithmic_bytes_per_step": bytes_["total"]},
+        "achieved_hbm_gbs": bytes_["total"] / (ms * 1e-3) / 1e9,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

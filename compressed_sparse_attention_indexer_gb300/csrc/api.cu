@@ -1,0 +1,402 @@
+// The C ABI (include/csa.h): argument validation, workspace ownership and the
+// launch sequence of each entry point.  No computation happens on the host.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "csa_internal.cuh"
+
+struct csa_handle {
+  csa_config cfg;
+  csa::DevCfg dc;
+  csa::Workspace ws;
+  void* ws_base;
+  size_t ws_bytes;
+  int device;
+  int num_sms;
+  int last_launches;
+  // per-stage timing (csa_profile_enable): event pairs recorded around each
+  // launch on its stream, resolved by csa_profile_read
+  bool prof = false;
+  struct Mark { int stage; cudaEvent_t a, b; };
+  std::vector<Mark> marks;
+  std::vector<cudaEvent_t> spare;
+};
+
+namespace {
+enum Stage { kStagePlan = 0, kStageIndexer = 1, kStageTopk = 2, kStageAttention = 3, kStages = 4 };
+
+cudaEvent_t take_event(csa_handle* h) {
+  if (!h->spare.empty()) {
+    cudaEvent_t e = h->spare.back();
+    h->spare.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Runs one launch helper, bracketed by events when profiling is on.
+template <typename F>
+int staged(csa_handle* h, int stage, cudaStream_t st, F&& launch) {
+  if (!h->prof) return launch();
+  cudaEvent_t a = take_event(h), b = take_event(h);
+  cudaEventRecord(a, st);
+  const int r = launch();
+  cudaEventRecord(b, st);
+  if (r > 0) h->marks.push_back({stage, a, b});
+  else { h->spare.push_back(a); h->spare.push_back(b); }
+  return r;
+}
+}  // namespace
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(CSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxVisCap = 40960;  // keys of one query held in shared memory by the Top-K kernel
+
+int validate_cfg(const csa_config* c) {
+  if (!c) return fail(CSA_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->heads < 1 || c->row_dim < 1 || c->v_dim < 1 || c->v_dim > c->row_dim)
+    return fail(CSA_ERR_INVALID_ARG, "need heads >= 1 and 1 <= v_dim <= row_dim");
+  if ((c->row_dim - c->v_dim) % 2 != 0)
+    return fail(CSA_ERR_INVALID_ARG, "rope dims row_dim - v_dim must be even");
+  if (c->idx_heads < 1 || c->idx_dim < 1) return fail(CSA_ERR_INVALID_ARG, "bad indexer shape");
+  if (c->ratio < 1 || c->topk < 1 || c->win < 1 || c->hca_ratio < 0)
+    return fail(CSA_ERR_INVALID_ARG, "need ratio, topk, win >= 1 and hca_ratio >= 0");
+  if (c->dtype != CSA_DTYPE_F32 && c->dtype != CSA_DTYPE_BF16)
+    return fail(CSA_ERR_UNSUPPORTED, "dtype must be CSA_DTYPE_F32 or CSA_DTYPE_BF16");
+  if (c->max_batch < 1 || c->max_queries_per_req < 1 || c->max_context < 1)
+    return fail(CSA_ERR_INVALID_ARG, "workspace maxima must be >= 1");
+  if (c->max_context / c->ratio > kMaxVisCap)
+    return fail(CSA_ERR_UNSUPPORTED, "max_context / ratio = %d exceeds %d",
+                c->max_context / c->ratio, kMaxVisCap);
+  if (c->topk > kMaxVisCap) return fail(CSA_ERR_UNSUPPORTED, "topk above %d", kMaxVisCap);
+  if (!(c->rope_base > 0.f)) return fail(CSA_ERR_INVALID_ARG, "rope_base must be > 0");
+  if ((int64_t)c->max_batch * c->max_queries_per_req > (1 << 24))
+    return fail(CSA_ERR_UNSUPPORTED, "max_batch * max_queries_per_req too large");
+  // shapes outside the tensor-core set run on the SIMT path, which holds V/32
+  // accumulators per lane
+  if (c->v_dim > 512) return fail(CSA_ERR_UNSUPPORTED, "v_dim above 512");
+  return CSA_OK;
+}
+
+int validate_batch_cfg(const csa_config& c, const csa_batch* b) {
+  if (!b) return fail(CSA_ERR_INVALID_ARG, "batch is NULL");
+  if (b->B < 0 || b->S < 1) return fail(CSA_ERR_INVALID_ARG, "need B >= 0 and S >= 1");
+  if (b->B > c.max_batch || b->S > c.max_queries_per_req)
+    return fail(CSA_ERR_WORKSPACE, "B=%d S=%d above create-time maxima %d, %d", b->B, b->S,
+                c.max_batch, c.max_queries_per_req);
+  if (b->B == 0) return CSA_OK;
+  const int es = c.dtype == CSA_DTYPE_BF16 ? 2 : 4;
+  struct P { const void* p; const char* n; } ptrs[] = {
+      {b->ctx_len, "ctx_len"}, {b->q, "q"}, {b->q_idx, "q_idx"}, {b->w, "w"},
+      {b->raw_kv, "raw_kv"}, {b->raw_off, "raw_off"}, {b->cmp_kv, "cmp_kv"},
+      {b->cmp_off, "cmp_off"}, {b->idx_k, "idx_k"}, {b->idx_off, "idx_off"}};
+  for (const P& x : ptrs)
+    if (!x.p) return fail(CSA_ERR_INVALID_ARG, "%s is NULL", x.n);
+  for (const P& x : ptrs)
+    if (!aligned16(x.p)) return fail(CSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", x.n);
+  struct Pool { int64_t stride, rows; int width; const char* n; } pools[] = {
+      {b->raw_stride, b->raw_rows, c.row_dim, "raw"},
+      {b->cmp_stride, b->cmp_rows, c.row_dim, "cmp"},
+      {b->idx_stride, b->idx_rows, c.idx_dim, "idx"},
+      {b->hca_stride, b->hca_rows, c.row_dim, "hca"}};
+  for (int i = 0; i < 4; ++i) {
+    const Pool& x = pools[i];
+    if (i == 3 && c.hca_ratio == 0) continue;
+    if (x.stride < x.width) return fail(CSA_ERR_INVALID_ARG, "%s_stride below the row width", x.n);
+    if ((x.stride * es) % 16 != 0)
+      return fail(CSA_ERR_INVALID_ARG, "%s_stride * element size is not a multiple of 16", x.n);
+    if (x.rows < 0) return fail(CSA_ERR_INVALID_ARG, "%s_rows < 0", x.n);
+  }
+  if (c.hca_ratio > 0) {
+    if (!b->hca_kv || !b->hca_off) return fail(CSA_ERR_INVALID_ARG, "hca_kv/hca_off NULL with hca_ratio > 0");
+    if (!aligned16(b->hca_kv) || !aligned16(b->hca_off))
+      return fail(CSA_ERR_INVALID_ARG, "hca_kv/hca_off not 16-byte aligned");
+  }
+  if (b->ctx_len_host) {
+    for (int i = 0; i < b->B; ++i) {
+      const int L = b->ctx_len_host[i];
+      if (L < b->S || L > c.max_context)
+        return fail(CSA_ERR_WORKSPACE, "ctx_len[%d] = %d outside [S, max_context] = [%d, %d]", i, L,
+                    b->S, c.max_context);
+    }
+  }
+  return CSA_OK;
+}
+
+int validate_batch(const csa_handle* h, const csa_batch* b) {
+  if (!h) return fail(CSA_ERR_INVALID_ARG, "handle is NULL");
+  return validate_batch_cfg(h->cfg, b);
+}
+
+csa::DevBatch dev_batch(const csa_batch* b) {
+  csa::DevBatch d;
+  d.B = b->B; d.S = b->S; d.ctx_len = b->ctx_len;
+  d.q = b->q; d.q_idx = b->q_idx; d.w = b->w;
+  d.raw = b->raw_kv; d.raw_off = b->raw_off; d.raw_stride = b->raw_stride; d.raw_rows = b->raw_rows;
+  d.cmp = b->cmp_kv; d.cmp_off = b->cmp_off; d.cmp_stride = b->cmp_stride; d.cmp_rows = b->cmp_rows;
+  d.idx = b->idx_k; d.idx_off = b->idx_off; d.idx_stride = b->idx_stride; d.idx_rows = b->idx_rows;
+  d.hca = b->hca_kv; d.hca_off = b->hca_off; d.hca_stride = b->hca_stride; d.hca_rows = b->hca_rows;
+  return d;
+}
+
+// Indexer work items (128-row chunks) when the host knows the lengths; -1 otherwise.
+int host_items(const csa_handle* h, const csa_batch* b, int score_all) {
+  if (!b->ctx_len_host) return -1;
+  const csa_config& c = h->cfg;
+  int64_t items = 0;
+  for (int i = 0; i < b->B; ++i) {
+    const int L = b->ctx_len_host[i];
+    int rows = 0;
+    for (int s = 0; s < b->S; ++s) {
+      const int vis = (L - b->S + s + 1) / c.ratio;
+      if (vis > c.topk || (score_all && vis > 0)) rows = vis > rows ? vis : rows;
+    }
+    items += (rows + csa::kIdxChunk - 1) / csa::kIdxChunk;
+  }
+  return (int)items;
+}
+
+struct Launches {
+  int n = 0;
+  bool ok = true;
+  void add(int r) {
+    if (r < 0) ok = false; else n += r;
+  }
+};
+
+int finish(csa_handle* h, const Launches& L) {
+  h->last_launches = L.n;
+  if (!L.ok) {
+    cudaError_t e = cudaGetLastError();
+    return cuda_fail(e, "kernel launch");
+  }
+  return CSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t csa_abi_version(void) { return CSA_ABI_VERSION; }
+
+const char* csa_last_error(void) { return g_err.c_str(); }
+
+int32_t csa_last_launch_count(const csa_handle* h) { return h ? h->last_launches : -1; }
+
+int csa_decode_create(const csa_config* cfg, csa_handle** out) {
+  if (!out) return fail(CSA_ERR_INVALID_ARG, "out is NULL");
+  int rc = validate_cfg(cfg);
+  if (rc) return rc;
+  csa_handle* h = new csa_handle();
+  h->cfg = *cfg;
+  csa::DevCfg& d = h->dc;
+  d.H = cfg->heads; d.D = cfg->row_dim; d.V = cfg->v_dim; d.R = cfg->row_dim - cfg->v_dim;
+  d.Hi = cfg->idx_heads; d.Di = cfg->idx_dim; d.ratio = cfg->ratio; d.K = cfg->topk;
+  d.win = cfg->win; d.hca_ratio = cfg->hca_ratio; d.dtype = cfg->dtype;
+  d.scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : (float)(1.0 / sqrt((double)cfg->row_dim));
+  d.rope_base = cfg->rope_base;
+  d.max_context = cfg->max_context;
+  d.max_vis = cfg->max_context / cfg->ratio;
+
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaGetDevice"); }
+  e = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaDeviceGetAttribute"); }
+
+  const int maxT = cfg->max_batch * cfg->max_queries_per_req;
+  const int64_t ld = d.max_vis > 0 ? d.max_vis : 1;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  size_t off = 0;
+  const size_t o_status = off; off += al(sizeof(int));
+  const size_t o_plan = off; off += al(sizeof(csa::QueryPlan) * maxT);
+  const size_t o_prefix = off; off += al(sizeof(int) * (cfg->max_batch + 1));
+  const size_t o_rows = off; off += al(sizeof(int) * cfg->max_batch);
+  const size_t o_scores = off; off += al(sizeof(float) * ld * maxT);
+  const size_t o_idx = off; off += al(sizeof(int) * (size_t)cfg->topk * maxT);
+  const size_t o_cnt = off; off += al(sizeof(int) * maxT);
+  h->ws_bytes = off;
+  e = cudaMalloc(&h->ws_base, off);
+  if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaMalloc(workspace)"); }
+  char* base = static_cast<char*>(h->ws_base);
+  e = cudaMemset(base + o_status, 0, sizeof(int));
+  if (e != cudaSuccess) { cudaFree(h->ws_base); delete h; return cuda_fail(e, "cudaMemset"); }
+  csa::Workspace& w = h->ws;
+  w.status = reinterpret_cast<int*>(base + o_status);
+  w.plan = reinterpret_cast<csa::QueryPlan*>(base + o_plan);
+  w.item_prefix = reinterpret_cast<int*>(base + o_prefix);
+  w.req_rows = reinterpret_cast<int*>(base + o_rows);
+  w.scores = reinterpret_cast<float*>(base + o_scores);
+  w.topk_idx = reinterpret_cast<int*>(base + o_idx);
+  w.topk_cnt = reinterpret_cast<int*>(base + o_cnt);
+  w.max_T = maxT;
+  w.max_batch = cfg->max_batch;
+  w.scores_ld = ld;
+  *out = h;
+  g_err.clear();
+  return CSA_OK;
+}
+
+void csa_decode_destroy(csa_handle* h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (auto& m : h->marks) { cudaEventDestroy(m.a); cudaEventDestroy(m.b); }
+  for (auto e : h->spare) cudaEventDestroy(e);
+  cudaFree(h->ws_base);
+  delete h;
+}
+
+int csa_indexer_topk(csa_handle* h, const csa_batch* b, int32_t* topk_idx, int32_t* topk_cnt,
+                     void* stream) {
+  int rc = validate_batch(h, b);
+  if (rc) return rc;
+  if (!topk_idx || !topk_cnt) return fail(CSA_ERR_INVALID_ARG, "topk_idx/topk_cnt NULL");
+  if (b->B == 0) { h->last_launches = 0; return CSA_OK; }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const csa::DevBatch db = dev_batch(b);
+  Launches L;
+  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, 0, nullptr, st); }));
+  L.add(staged(h, kStageIndexer, st, [&] { return csa::launch_indexer(h->dc, db, h->ws, h->ws.scores, h->ws.scores_ld, host_items(h, b, 0),
+                            h->num_sms, st); }));
+  L.add(staged(h, kStageTopk, st, [&] { return csa::launch_topk(h->dc, b->B * b->S, h->ws.plan, h->ws.scores, h->ws.scores_ld, nullptr,
+                         topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st); }));
+  return finish(h, L);
+}
+
+int csa_sparse_attn(csa_handle* h, const csa_batch* b, const int32_t* topk_idx,
+                    const int32_t* topk_cnt, void* out, float* lse_out, void* stream) {
+  int rc = validate_batch(h, b);
+  if (rc) return rc;
+  if (!topk_idx || !topk_cnt || !out) return fail(CSA_ERR_INVALID_ARG, "topk_idx/topk_cnt/out NULL");
+  if (!aligned16(out)) return fail(CSA_ERR_INVALID_ARG, "out is not 16-byte aligned");
+  if (b->B == 0) { h->last_launches = 0; return CSA_OK; }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const csa::DevBatch db = dev_batch(b);
+  Launches L;
+  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, 0, topk_cnt, st); }));
+  L.add(staged(h, kStageAttention, st, [&] { return csa::launch_attention(h->dc, db, h->ws, topk_idx, topk_cnt, out, lse_out, h->num_sms, st); }));
+  return finish(h, L);
+}
+
+int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out,
+                    int32_t* topk_idx_out, int32_t* topk_cnt_out, void* stream) {
+  int rc = validate_batch(h, b);
+  if (rc) return rc;
+  if (!out) return fail(CSA_ERR_INVALID_ARG, "out is NULL");
+  if (!aligned16(out)) return fail(CSA_ERR_INVALID_ARG, "out is not 16-byte aligned");
+  if (b->B == 0) { h->last_launches = 0; return CSA_OK; }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const csa::DevBatch db = dev_batch(b);
+  int* idx = topk_idx_out ? topk_idx_out : h->ws.topk_idx;
+  int* cnt = topk_cnt_out ? topk_cnt_out : h->ws.topk_cnt;
+  Launches L;
+  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, 0, nullptr, st); }));
+  L.add(staged(h, kStageIndexer, st, [&] { return csa::launch_indexer(h->dc, db, h->ws, h->ws.scores, h->ws.scores_ld, host_items(h, b, 0),
+                            h->num_sms, st); }));
+  L.add(staged(h, kStageTopk, st, [&] { return csa::launch_topk(h->dc, b->B * b->S, h->ws.plan, h->ws.scores, h->ws.scores_ld, nullptr,
+                         idx, cnt, h->ws.status, h->dc.max_vis, st); }));
+  L.add(staged(h, kStageAttention, st, [&] { return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse_out, h->num_sms, st); }));
+  return finish(h, L);
+}
+
+int csa_indexer_scores(csa_handle* h, const csa_batch* b, float* scores, int64_t ld,
+                       int32_t score_all, void* stream) {
+  int rc = validate_batch(h, b);
+  if (rc) return rc;
+  if (!scores) return fail(CSA_ERR_INVALID_ARG, "scores is NULL");
+  if (ld < h->dc.max_vis) return fail(CSA_ERR_INVALID_ARG, "ld below max_context / ratio");
+  if (b->B == 0) { h->last_launches = 0; return CSA_OK; }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const csa::DevBatch db = dev_batch(b);
+  Launches L;
+  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, score_all ? 1 : 0, nullptr, st); }));
+  L.add(staged(h, kStageIndexer, st, [&] { return csa::launch_indexer(h->dc, db, h->ws, scores, ld, host_items(h, b, score_all ? 1 : 0),
+                            h->num_sms, st); }));
+  return finish(h, L);
+}
+
+int csa_topk_select(csa_handle* h, int32_t nq, const float* scores, int64_t ld, const int32_t* n,
+                    int32_t* topk_idx, int32_t* topk_cnt, void* stream) {
+  if (!h) return fail(CSA_ERR_INVALID_ARG, "handle is NULL");
+  if (nq < 0) return fail(CSA_ERR_INVALID_ARG, "nq < 0");
+  if (nq == 0) { h->last_launches = 0; return CSA_OK; }
+  if (!scores || !n || !topk_idx || !topk_cnt) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
+  if (ld < 1) return fail(CSA_ERR_INVALID_ARG, "ld < 1");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Launches L;
+  L.add(staged(h, kStageTopk, st, [&] { return csa::launch_topk(h->dc, nq, nullptr, scores, ld, n, topk_idx, topk_cnt, h->ws.status,
+                         h->dc.max_vis, st); }));
+  return finish(h, L);
+}
+
+int csa_profile_enable(csa_handle* h, int32_t enable) {
+  if (!h) return fail(CSA_ERR_INVALID_ARG, "handle is NULL");
+  h->prof = enable != 0;
+  return CSA_OK;
+}
+
+int csa_profile_read(csa_handle* h, float* ms, int32_t* launches) {
+  if (!h || !ms || !launches) return fail(CSA_ERR_INVALID_ARG, "NULL argument");
+  for (int i = 0; i < kStages; ++i) { ms[i] = 0.f; launches[i] = 0; }
+  for (auto& m : h->marks) {
+    cudaError_t e = cudaEventSynchronize(m.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float t = 0.f;
+    e = cudaEventElapsedTime(&t, m.a, m.b);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    ms[m.stage] += t;
+    launches[m.stage] += 1;
+    h->spare.push_back(m.a);
+    h->spare.push_back(m.b);
+  }
+  h->marks.clear();
+  return CSA_OK;
+}
+
+int csa_check_batch(const csa_config* cfg, const csa_batch* b) {
+  int rc = validate_cfg(cfg);
+  if (rc) return rc;
+  return validate_batch_cfg(*cfg, b);
+}
+
+int csa_get_status(csa_handle* h, void* stream) {
+  if (!h) return fail(CSA_ERR_INVALID_ARG, "handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, h->ws.status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  e = cudaMemset(h->ws.status, 0, sizeof(int));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  if (v & csa::kStatusTimeout) return fail(CSA_ERR_TIMEOUT, "a device wait gave up");
+  if (v & csa::kStatusBadIndex)
+    return fail(CSA_ERR_BAD_INDEX, "a length or row index in device memory was out of range");
+  return CSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,265 @@
+// Step (a): the lightning-indexer score of every visible compressed row,
+//   score_j = sum_h w_h * ReLU(q_idx[h] . k_idx[j]),
+// written to an fp32 score buffer.  hw-native-sys/pypto-lib "Perf: skip
+// redundant CSA scoring and fuse gather unpack" (the indexer and the query
+// scoring it skips) and "Fix: port the DeepSeek-V4 MoE, hc_pre and prefill
+// fixes to DSpark" (partials reduced in a fixed ascending order, no atomics).
+//
+// Tensor-core path (bf16, Hi = 64, Di = 128): a persistent grid walks the
+// work list of 128-row chunks made by the plan kernel.  Each chunk of k_idx
+// rows is streamed from HBM once into shared memory through a multi-stage
+// cp.async ring and reused by every scored query of its request.  The
+// contraction is rows x heads x 128 on warp MMA (rows are the M side, heads
+// the N side), so each row ends in registers of one quad; the epilogue
+// applies ReLU, and one lane per row and head-half sums w_h * ReLU(.) over
+// h in ascending order, then the two halves are added in order.
+//
+// SIMT path: any shape and dtype, one warp per row, fp32 FMA.
+#include "csa_internal.cuh"
+#include "ptx.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr int kIdxThreads = 256;                    // 8 warps x 16 rows = kIdxChunk
+constexpr int kQBytes = kTcHi * kTcDi * 2;          // one query's q_idx: 16 KB
+constexpr int kKStageBytes = kIdxChunk * kTcDi * 2; // one chunk of keys: 32 KB
+constexpr int kStashLd = 65;                        // 64 heads + 1 pad (bank spread)
+constexpr int kStashBytes = (kIdxThreads / 32) * 16 * kStashLd * 4;
+
+__device__ __forceinline__ void wait_stages(int nst) {
+  // keep at most nst-2 groups pending
+  if (nst >= 4) cp_async_wait<2>();
+  else if (nst == 3) cp_async_wait<1>();
+  else cp_async_wait<0>();
+}
+
+__global__ void __launch_bounds__(kIdxThreads, 1)
+    indexer_tc_kernel(DevCfg c, DevBatch b, Workspace ws, float* __restrict__ scores,
+                      int64_t ld, int SG, int NST) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* Qs = smem;
+  uint8_t* Ks = Qs + SG * kQBytes;
+  float* stash = reinterpret_cast<float*>(Ks + NST * kKStageBytes);
+  float* w_s = stash + (kIdxThreads / 32) * 16 * kStashLd;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int* __restrict__ prefix = ws.item_prefix;
+  const int N = prefix[b.B];
+  const int G = gridDim.x;
+  const int lo = (int)((int64_t)blockIdx.x * N / G);
+  const int hi = (int)((int64_t)(blockIdx.x + 1) * N / G);
+  if (lo >= hi) return;
+
+  // request owning item lo: the last bi with prefix[bi] <= lo
+  int b0 = 0;
+  {
+    int l = 0, r = b.B - 1;
+    while (l < r) {
+      const int m = (l + r + 1) >> 1;
+      if (prefix[m] <= lo) l = m; else r = m - 1;
+    }
+    b0 = l;
+  }
+  const __nv_bfloat16* __restrict__ kbase = static_cast<const __nv_bfloat16*>(b.idx);
+
+  int ib = b0;  // issue cursor
+  auto issue = [&](int item) {
+    while (item >= prefix[ib + 1]) ++ib;
+    const int c0 = (item - prefix[ib]) * kIdxChunk;
+    const int rows = ws.req_rows[ib];
+    const int64_t off = b.idx_off[ib];
+    uint8_t* dst0 = Ks + (item % NST) * kKStageBytes;
+#pragma unroll
+    for (int i = 0; i < (kIdxChunk * 16) / kIdxThreads; ++i) {
+      const int id = tid + i * kIdxThreads;
+      const int row = id >> 4, ch = id & 15;
+      const int r = c0 + row;
+      const int64_t gr = off + r;
+      const bool inb = gr >= 0 && gr < b.idx_rows;
+      const bool want = r < rows;
+      if (want && !inb && ch == 0) set_status(ws.status, kStatusBadIndex);
+      const bool ok = want && inb;
+      const void* src = ok ? (const void*)(kbase + gr * b.idx_stride + ch * 8) : (const void*)kbase;
+      cp_async16(smem_u32(dst0 + row * 256 + ((ch ^ (row & 7)) << 4)), src, ok ? 16 : 0);
+    }
+  };
+
+  for (int k = 0; k < NST - 1; ++k) {
+    if (lo + k < hi) issue(lo + k);
+    cp_async_commit();
+  }
+
+  int cb = b0, q_b = -1, q_g = -1;
+  for (int it = lo; it < hi; ++it) {
+    wait_stages(NST);
+    __syncthreads();
+    {
+      const int nxt = it + NST - 1;
+      if (nxt < hi) issue(nxt);
+      cp_async_commit();
+    }
+    while (it >= prefix[cb + 1]) ++cb;
+    const int c0 = (it - prefix[cb]) * kIdxChunk;
+    const uint8_t* Kst = Ks + (it % NST) * kKStageBytes;
+
+    // A fragments: this warp's 16 key rows x 128 dims, kept across queries
+    uint32_t a[8][4];
+    {
+      const int row = warp * 16 + (lane & 15);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int ch = 2 * kk + (lane >> 4);
+        ldsm_x4(smem_u32(Kst + row * 256 + ((ch ^ (row & 7)) << 4)), a[kk][0], a[kk][1],
+                a[kk][2], a[kk][3]);
+      }
+    }
+
+    for (int g0 = 0; g0 < b.S; g0 += SG) {
+      const int ng = min(SG, b.S - g0);
+      if (cb != q_b || g0 != q_g) {
+        __syncthreads();  // every warp is done with the previous q_idx group
+        const uint4* src = reinterpret_cast<const uint4*>(
+            static_cast<const __nv_bfloat16*>(b.q_idx) + ((int64_t)cb * b.S + g0) * kTcHi * kTcDi);
+        for (int v = tid; v < ng * kTcHi * 16; v += kIdxThreads) {
+          const int row = v >> 4, ch = v & 15;  // row = s_local*64 + h
+          const uint4 x = __ldg(src + v);
+          *reinterpret_cast<uint4*>(Qs + row * 256 + ((ch ^ (row & 7)) << 4)) = x;
+        }
+        for (int v = tid; v < ng * kTcHi; v += kIdxThreads)
+          w_s[v] = __ldg(b.w + ((int64_t)cb * b.S + g0) * kTcHi + v);
+        __syncthreads();
+        q_b = cb;
+        q_g = g0;
+      }
+      for (int sl = 0; sl < ng; ++sl) {
+        const int qid = cb * b.S + g0 + sl;
+        const QueryPlan p = ws.plan[qid];
+        if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
+        float acc[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+        const uint8_t* Qq = Qs + sl * kQBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+          for (int pp = 0; pp < 4; ++pp) {
+            const int head = 16 * pp + ((lane >> 4) << 3) + (lane & 7);
+            const int ch = 2 * kk + ((lane >> 3) & 1);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(smem_u32(Qq + head * 256 + ((ch ^ (head & 7)) << 4)), r0, r1, r2, r3);
+            mma_bf16_16816(acc[2 * pp], a[kk], r0, r1);
+            mma_bf16_16816(acc[2 * pp + 1], a[kk], r2, r3);
+          }
+        }
+        // epilogue: ReLU, then w-weighted sum over heads in ascending order
+        float* st = stash + warp * 16 * kStashLd;
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          st[g * kStashLd + 8 * j + 2 * t] = fmaxf(acc[j][0], 0.f);
+          st[g * kStashLd + 8 * j + 2 * t + 1] = fmaxf(acc[j][1], 0.f);
+          st[(g + 8) * kStashLd + 8 * j + 2 * t] = fmaxf(acc[j][2], 0.f);
+          st[(g + 8) * kStashLd + 8 * j + 2 * t + 1] = fmaxf(acc[j][3], 0.f);
+        }
+        __syncwarp();
+        const int row = lane & 15, half = lane >> 4;
+        const float* wq = w_s + sl * kTcHi + half * 32;
+        const float* sr = st + row * kStashLd + half * 32;
+        float sum = 0.f;
+#pragma unroll 8
+        for (int h = 0; h < 32; ++h) sum = fmaf(wq[h], sr[h], sum);
+        const float upper = __shfl_down_sync(0xffffffffu, sum, 16);
+        const int j = c0 + warp * 16 + row;
+        if (half == 0 && j < p.vis) scores[(int64_t)qid * ld + j] = sum + upper;
+        __syncwarp();
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p, int64_t i);
+template <>
+__device__ __forceinline__ float ldf<float>(const float* p, int64_t i) { return p[i]; }
+template <>
+__device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) indexer_simt_kernel(DevCfg c, DevBatch b, Workspace ws,
+                                                           float* __restrict__ scores,
+                                                           int64_t ld) {
+  const int q = blockIdx.x;
+  const QueryPlan p = ws.plan[q];
+  if (!(p.flags & kPlanScore)) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int bi = q / b.S;
+  const T* qi = static_cast<const T*>(b.q_idx) + (int64_t)q * c.Hi * c.Di;
+  const float* wq = b.w + (int64_t)q * c.Hi;
+  const T* kp = static_cast<const T*>(b.idx);
+  for (int j = blockIdx.y * 8 + warp; j < p.vis; j += gridDim.y * 8) {
+    const int64_t gr = b.idx_off[bi] + j;
+    float acc;
+    if (gr < 0 || gr >= b.idx_rows) {
+      if (lane == 0) set_status(ws.status, kStatusBadIndex);
+      acc = -INFINITY;
+    } else {
+      acc = 0.f;
+      const T* kr = kp + gr * b.idx_stride;
+      for (int h = 0; h < c.Hi; ++h) {
+        float dot = 0.f;
+        for (int d = lane; d < c.Di; d += 32) dot = fmaf(ldf(qi, (int64_t)h * c.Di + d), ldf(kr, d), dot);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        acc = fmaf(wq[h], fmaxf(dot, 0.f), acc);
+      }
+    }
+    if (lane == 0) scores[(int64_t)q * ld + j] = acc;
+  }
+}
+
+}  // namespace
+
+bool tensor_core_shape(const DevCfg& c) {
+  return c.dtype == CSA_DTYPE_BF16 && c.H == kTcH && c.D == kTcD && c.V == kTcV &&
+         c.Hi == kTcHi && c.Di == kTcDi;
+}
+
+int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, float* scores,
+                   int64_t ld, int total_items_hint, int num_sms, cudaStream_t st) {
+  if (total_items_hint == 0) return 0;
+  if (tensor_core_shape(c)) {
+    const int SG = b.S < 8 ? b.S : 8;
+    const int fixed = SG * kQBytes + kStashBytes + SG * kTcHi * 4;
+    int NST = (227 * 1024 - fixed) / kKStageBytes;
+    NST = NST > 4 ? 4 : NST;
+    if (NST < 2) return -1;
+    const int smem = fixed + NST * kKStageBytes;
+    static bool attr_done = false;
+    if (!attr_done) {
+      cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           227 * 1024);
+      attr_done = true;
+    }
+    int grid = num_sms;
+    if (total_items_hint > 0 && total_items_hint < grid) grid = total_items_hint;
+    indexer_tc_kernel<<<grid, kIdxThreads, smem, st>>>(c, b, ws, scores, ld, SG, NST);
+  } else {
+    int y = (c.max_vis + 7) / 8;
+    if (y > 64) y = 64;
+    if (y < 1) y = 1;
+    dim3 grid(b.B * b.S, y);
+    if (c.dtype == CSA_DTYPE_BF16)
+      indexer_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(c, b, ws, scores, ld);
+    else
+      indexer_simt_kernel<float><<<grid, 256, 0, st>>>(c, b, ws, scores, ld);
+  }
+  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace csa

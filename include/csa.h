@@ -1,0 +1,200 @@
+/*
+ * csa.h -- C ABI of the GB300 compressed sparse attention (CSA) decode step.
+ *
+ * One decode step of DeepSeek-V4-style compressed sparse attention, per query
+ * token (hw-native-sys/pypto-lib pages):
+ *   (a) indexer score of every causally visible ratio-r compressed row,
+ *       score_j = sum_h w_h * ReLU(q_idx[h] . k_idx[j]), summed over h in
+ *       ascending order (no atomics: "Fix: port the DeepSeek-V4 MoE, hc_pre
+ *       and prefill fixes to DSpark", PR description, deterministic ordered
+ *       reduction);
+ *   (b) Top-K of those scores, ties to the lower index; when the visible rows
+ *       fit K (vis <= K) scoring and sorting are skipped and every visible
+ *       row is taken ("Perf: skip redundant CSA scoring and fuse gather
+ *       unpack", PR description);
+ *   (c) gather of the selected compressed rows plus the last WIN raw rows,
+ *       at most WIN + min(vis, K) rows ("Fix: port the DeepSeek-V4 MoE ...",
+ *       PR description, packed sparse CSA row bound);
+ *   (d) attention of H heads over rows shared by all heads (row width D, the
+ *       first V dims are values), one softmax stream for the window rows,
+ *       one for the compressed rows (and one for heavy-compression rows when
+ *       enabled), a log-sum-exp merge of the streams, then inverse RoPE on
+ *       the last R = D - V output dims ("Perf: fuse HCA merge, inverse RoPE,
+ *       and packing", PR description).
+ *
+ * Definitions used throughout (query s of request b, context length L_b
+ * including the S new tokens):
+ *   pos  = L_b - S + s                (0-based position of the query)
+ *   vis  = floor((pos + 1) / ratio)   (compressed rows whose raw span ends at or before pos)
+ *   nwin = min(WIN, pos + 1)          (window = raw rows pos-nwin+1 .. pos)
+ *   cnt  = min(vis, K)
+ *   vis2 = floor((pos + 1) / hca_ratio) when the heavy-compression stream is on
+ * Inverse RoPE: for i < R/2, output dims (V-R+2i, V-R+2i+1) are rotated by
+ * -pos * base^(-2i/R).
+ *
+ * Conventions
+ *  - Every pointer in csa_batch and every output pointer is DEVICE memory
+ *    owned by the caller.  The library never frees or retains them.
+ *  - Every call is asynchronous on the given CUDA stream (a cudaStream_t
+ *    passed as void*; NULL = legacy default stream).  No call synchronises
+ *    except csa_get_status and csa_decode_destroy.
+ *  - Element types: CSA_DTYPE_BF16 (bf16 storage, fp32 arithmetic) or
+ *    CSA_DTYPE_F32.  Strides are in ELEMENTS; every row must start on a
+ *    16-byte boundary (pointer and stride*element_size multiples of 16).
+ *  - Row r of pool X for request b is at X + (X_off[b] + r) * X_stride.
+ *    X_rows is the number of rows the pool holds; a row index outside
+ *    [0, X_rows) is never dereferenced: it sets CSA_ERR_BAD_INDEX in the
+ *    handle's status word and the row is skipped.
+ *  - Errors found on the host return a non-zero code before any launch and
+ *    leave the outputs untouched; csa_last_error() describes the last one
+ *    on the calling thread.  Errors found on the device (bad lengths or row
+ *    indices in device memory) are recorded in the status word, the affected
+ *    query's output is written as zeros, and csa_get_status reports them.
+ *  - A handle may be used from one host thread at a time.  Calls that share
+ *    a handle must be ordered on the GPU (same stream, or the caller orders
+ *    them): they share the handle's workspace.
+ */
+#ifndef CSA_H
+#define CSA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CSA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define CSA_API __attribute__((visibility("default")))
+#else
+#define CSA_API
+#endif
+
+/* return codes */
+enum {
+    CSA_OK = 0,
+    CSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer or stride  */
+    CSA_ERR_UNSUPPORTED = 2, /* shape or dtype outside the compiled set               */
+    CSA_ERR_WORKSPACE = 3,   /* B, S or a length above the create-time maxima         */
+    CSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (message in last_error)    */
+    CSA_ERR_BAD_INDEX = 5,   /* device-side: a length or row index out of range       */
+    CSA_ERR_TIMEOUT = 6      /* device-side: a bounded wait gave up                   */
+};
+
+enum { CSA_DTYPE_F32 = 0, CSA_DTYPE_BF16 = 1 };
+
+/* Static shape of one attention layer; fixed at csa_decode_create. */
+typedef struct {
+    int32_t heads;     /* H: attention heads                                   */
+    int32_t row_dim;   /* D: width of a KV row (values + rope dims)            */
+    int32_t v_dim;     /* V: value / output dims, V < D, R = D - V even        */
+    int32_t idx_heads; /* Hi: indexer heads                                    */
+    int32_t idx_dim;   /* Di: indexer dim                                      */
+    int32_t ratio;     /* compression ratio of the CSA rows (4)                */
+    int32_t topk;      /* K                                                    */
+    int32_t win;       /* WIN: sliding window, >= 1                            */
+    int32_t hca_ratio; /* ratio of the heavy-compression stream; 0 = off       */
+    int32_t dtype;     /* CSA_DTYPE_BF16 or CSA_DTYPE_F32                      */
+    float softmax_scale; /* <= 0 selects 1/sqrt(D)                             */
+    float rope_base;     /* RoPE base (10000)                                  */
+    int32_t max_batch;   /* workspace bound on B                               */
+    int32_t max_queries_per_req; /* workspace bound on S                       */
+    int32_t max_context; /* workspace bound on every L_b                       */
+} csa_config;
+
+/* One batch.  All pointers: caller-owned device memory. */
+typedef struct {
+    int32_t B, S;             /* requests, queries per request (B = 0: no-op)   */
+    const int32_t *ctx_len;   /* [B] L_b, including the S new tokens; S <= L_b <= max_context */
+    const int32_t *ctx_len_host; /* optional HOST copy of ctx_len (same values):
+                                    lets the host size grids exactly and skip
+                                    launches with no work; NULL = size for the
+                                    create-time maxima                          */
+    const void *q;            /* [B,S,H,D]                                      */
+    const void *q_idx;        /* [B,S,Hi,Di]                                    */
+    const float *w;           /* [B,S,Hi] fp32 indexer head weights             */
+    const void *raw_kv;  const int64_t *raw_off; int64_t raw_stride; int64_t raw_rows; /* raw rows, width D */
+    const void *cmp_kv;  const int64_t *cmp_off; int64_t cmp_stride; int64_t cmp_rows; /* ratio rows, width D */
+    const void *idx_k;   const int64_t *idx_off; int64_t idx_stride; int64_t idx_rows; /* indexer keys, width Di */
+    const void *hca_kv;  const int64_t *hca_off; int64_t hca_stride; int64_t hca_rows; /* heavy rows, width D; NULL if off */
+} csa_batch;
+
+typedef struct csa_handle csa_handle;
+
+/* Validates cfg and allocates the handle's device workspace on the current
+ * device (scores [B*S, max_context/ratio] fp32, plan and status words).
+ * Returns CSA_ERR_INVALID_ARG / CSA_ERR_UNSUPPORTED for a bad cfg,
+ * CSA_ERR_CUDA if allocation fails.  *out is set only on success. */
+CSA_API int csa_decode_create(const csa_config *cfg, csa_handle **out);
+
+/* Synchronises the device, frees the workspace and the handle.  NULL is a no-op. */
+CSA_API void csa_decode_destroy(csa_handle *h);
+
+/* Steps (a)+(b).  topk_idx [B,S,K] int32: the selected compressed-row
+ * indices of each query in ascending order, slots >= count set to -1;
+ * topk_cnt [B,S] int32: count = min(vis, K).  ("Perf: skip redundant CSA
+ * scoring and fuse gather unpack": bounded Top-K indices, bypass.) */
+CSA_API int csa_indexer_topk(csa_handle *h, const csa_batch *b, int32_t *topk_idx,
+                     int32_t *topk_cnt, void *stream);
+
+/* Steps (c)+(d) with caller-supplied indices (layout as csa_indexer_topk
+ * writes them; every index must lie in [0, vis) and count <= min(vis, K),
+ * else CSA_ERR_BAD_INDEX is recorded and the bad entries are skipped).
+ * out [B,S,H,V] in the config dtype; lse_out [B,S,H] fp32 natural-log
+ * log-sum-exp of the merged streams, may be NULL. */
+CSA_API int csa_sparse_attn(csa_handle *h, const csa_batch *b, const int32_t *topk_idx,
+                    const int32_t *topk_cnt, void *out, float *lse_out, void *stream);
+
+/* The whole step (a)-(d).  topk_idx_out / topk_cnt_out may be NULL (the
+ * handle's workspace holds them); when given they receive what
+ * csa_indexer_topk would write. */
+CSA_API int csa_decode_step(csa_handle *h, const csa_batch *b, void *out, float *lse_out,
+                    int32_t *topk_idx_out, int32_t *topk_cnt_out, void *stream);
+
+/* Step (a) alone, for inspection: scores [B*S, ld] fp32, row j < vis of each
+ * query.  score_all = 0 scores only queries with vis > K (as the step does);
+ * 1 scores every query.  Entries j >= vis are not written. */
+CSA_API int csa_indexer_scores(csa_handle *h, const csa_batch *b, float *scores, int64_t ld,
+                       int32_t score_all, void *stream);
+
+/* Step (b) alone on caller scores: for each of nq queries, the K best of
+ * scores[q*ld + 0 .. n[q]) (ties to the lower index, -0.0 == +0.0), written
+ * like csa_indexer_topk.  n: [nq] int32 device, 0 <= n[q] <= ld, and
+ * n[q] <= max_context/ratio.  Uses the handle's K. */
+CSA_API int csa_topk_select(csa_handle *h, int32_t nq, const float *scores, int64_t ld,
+                    const int32_t *n, int32_t *topk_idx, int32_t *topk_cnt, void *stream);
+
+/* Host-side checks of a batch against a config, exactly those every entry
+ * point runs before launching (null / misaligned pointers, strides, sizes
+ * against the maxima, ctx_len_host values).  Touches no device memory and
+ * needs no GPU.  Returns CSA_OK or the code the entry point would return. */
+CSA_API int csa_check_batch(const csa_config *cfg, const csa_batch *b);
+
+/* Synchronises `stream`, then returns and clears the handle's device status:
+ * CSA_OK, CSA_ERR_BAD_INDEX or CSA_ERR_TIMEOUT (or CSA_ERR_CUDA). */
+CSA_API int csa_get_status(csa_handle *h, void *stream);
+
+/* Per-stage timing.  While enabled, every kernel launch of the handle is
+ * bracketed by CUDA events recorded on its stream (stages, in order: plan,
+ * indexer, Top-K, attention).  csa_profile_read waits for the recorded
+ * events, writes the summed milliseconds ms[4] and launch counts
+ * launches[4] since the last read, and resets them.  Timing adds two event
+ * records per launch; leave it off for end-to-end timing. */
+CSA_API int csa_profile_enable(csa_handle *h, int32_t enable);
+CSA_API int csa_profile_read(csa_handle *h, float *ms, int32_t *launches);
+
+/* Message for the last error on this host thread ("" if none). */
+CSA_API const char *csa_last_error(void);
+
+/* Number of kernel launches the last call on this handle made. */
+CSA_API int32_t csa_last_launch_count(const csa_handle *h);
+
+/* CSA_ABI_VERSION of the built library. */
+CSA_API int32_t csa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSA_H */

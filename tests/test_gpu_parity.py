@@ -1,0 +1,336 @@
+"""GPU parity: every step of the CUDA path, through the C ABI, against the CPU oracle.
+
+Same seeded inputs on both sides.  Top-K index sets must match exactly except
+for elements whose oracle score is within 1e-6 (relative) of the K-th
+oracle score; attention outputs within 2e-2 max-abs / 1e-2 mean-abs of the
+fp64 oracle for bf16 inputs and 1e-5 for the fp32 workload.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compressed_sparse_attention_indexer_gb300 import build as csa_build
+from compressed_sparse_attention_indexer_gb300 import csa
+from compressed_sparse_attention_indexer_gb300.workloads import (
+    BF16_CFG, CsaConfig, Dists, Workload, WORKLOADS, make_batch, to_device)
+from helpers import TOL_BF16, assert_close, assert_topk_sets, tol_for
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    csa_build.build()
+    oracle.build()
+    torch.cuda.set_device(0)
+
+
+def run_step(wl, hb, max_context=None, host_lens=False):
+    cfg = wl.cfg
+    db = to_device(hb, DEV)
+    B, S = hb["B"], hb["S"]
+    mc = max_context or max(int(hb["ctx_len"].max()), 4)
+    dec = csa.Decoder(cfg, B, S, mc)
+    out = torch.full((B, S, cfg.H, cfg.V), float("nan"), dtype=cfg.torch_dtype, device=DEV)
+    lse = torch.full((B, S, cfg.H), float("nan"), dtype=torch.float32, device=DEV)
+    idx = torch.full((B, S, cfg.topk), -7, dtype=torch.int32, device=DEV)
+    cnt = torch.full((B, S), -7, dtype=torch.int32, device=DEV)
+    lens_host = hb["ctx_len"].clone() if host_lens else None
+    cb = csa.make_batch_struct(db, lens_host)
+    dec.decode_step(cb, out, lse, idx, cnt)
+    st = dec.status()
+    nq = B * S
+    return dict(dec=dec, db=db, cb=cb, status=st, lens_host=lens_host,
+                out=out.float().cpu().numpy().reshape(nq, cfg.H, cfg.V),
+                lse=lse.cpu().numpy().reshape(nq, cfg.H),
+                idx=idx.cpu().numpy().reshape(nq, cfg.topk), cnt=cnt.cpu().numpy().reshape(nq))
+
+
+def scores_fn(cfg, hb):
+    S = hb["S"]
+    return lambda q: oracle.query_scores(cfg, hb, q // S, q % S)
+
+
+def check_against_oracle(wl, hb, g, ref=None, what=""):
+    cfg = wl.cfg
+    ref = ref if ref is not None else oracle.decode(cfg, hb)
+    assert g["status"] == csa.CSA_OK, csa.last_error()
+    assert_topk_sets(g["idx"], g["cnt"], ref, scores_fn(cfg, hb), cfg.topk, what)
+    assert_close(g["out"], ref["out"], tol_for(cfg), what + " out")
+    lse_tol = (1e-5, 1e-5) if cfg.dtype == "f32" else (1e-3, 1e-4)
+    assert_close(g["lse"], ref["lse"], lse_tol, what + " lse")
+    return ref
+
+
+# ---------------------------------------------------------------------------
+# the five named workloads, full size
+
+@pytest.mark.parametrize("name", ["tiny_f32", "bypass_b16_l256", "topk_b16_l8192",
+                                  "long_ragged_b64", "multitoken_hca_b16_s8"])
+def test_workload_decode_step(name):
+    wl = WORKLOADS[name]
+    hb = make_batch(wl)
+    g = run_step(wl, hb, max_context=65536 if name == "long_ragged_b64" else None)
+    ref = check_against_oracle(wl, hb, g, what=name)
+    # attention alone on the oracle's own selection isolates steps (c)-(d)
+    cfg = wl.cfg
+    B, S = hb["B"], hb["S"]
+    idx = torch.from_numpy(ref["topk_idx"]).to(DEV).view(B, S, cfg.topk)
+    cnt = torch.from_numpy(ref["cnt"].astype(np.int32)).to(DEV).view(B, S)
+    out = torch.empty(B, S, cfg.H, cfg.V, dtype=cfg.torch_dtype, device=DEV)
+    g["dec"].sparse_attn(g["cb"], idx, cnt, out)
+    assert g["dec"].status() == csa.CSA_OK
+    assert_close(out.float().cpu().numpy().reshape(B * S, cfg.H, cfg.V), ref["out"], tol_for(cfg),
+                 name + " sparse_attn")
+    # bypass workload: no scoring launch when the host knows every query fits K
+    if name == "bypass_b16_l256":
+        assert (ref["cnt"] == ref["vis"]).all()
+
+
+def test_indexer_topk_entry_matches_decode_step():
+    wl = WORKLOADS["topk_b16_l8192"]
+    hb = make_batch(wl)
+    g = run_step(wl, hb)
+    B, S = hb["B"], hb["S"]
+    idx = torch.empty(B, S, wl.cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(B, S, dtype=torch.int32, device=DEV)
+    g["dec"].indexer_topk(g["cb"], idx, cnt)
+    assert g["dec"].status() == csa.CSA_OK
+    np.testing.assert_array_equal(idx.cpu().numpy().reshape(B * S, -1), g["idx"])
+    np.testing.assert_array_equal(cnt.cpu().numpy().reshape(-1), g["cnt"])
+
+
+# ---------------------------------------------------------------------------
+# step (a) alone: fp32 scores against fp64
+
+@pytest.mark.parametrize("name,lens", [("topk_b16_l8192", [8192, 300, 1029, 4097]),
+                                       ("tiny_f32", None)])
+def test_indexer_scores_against_oracle(name, lens):
+    wl = WORKLOADS[name]
+    cfg = wl.cfg
+    hb = make_batch(wl, lens=lens)
+    db = to_device(hb, DEV)
+    B, S = hb["B"], hb["S"]
+    mc = int(hb["ctx_len"].max())
+    dec = csa.Decoder(cfg, B, S, mc)
+    ld = mc // cfg.ratio
+    scores = torch.full((B * S, ld), float("nan"), dtype=torch.float32, device=DEV)
+    dec.indexer_scores(csa.make_batch_struct(db), scores, score_all=True)
+    assert dec.status() == csa.CSA_OK
+    sc = scores.cpu().numpy()
+    qi = hb["q_idx"].double().numpy()
+    w = hb["w"].double().numpy()
+    for q in range(B * S):
+        b, s = divmod(q, S)
+        ref = oracle.query_scores(cfg, hb, b, s)
+        n = len(ref)
+        got = sc[q, :n]
+        assert np.isnan(sc[q, n:]).all(), "entries past vis must stay untouched"
+        # error bound of fp32 accumulation: relative to sum_h w_h sum_d |q_hd k_jd|
+        off = int(hb["idx_off"][b])
+        k = hb["idx_k"][off:off + n].double().numpy()
+        mag = np.abs(k) @ np.abs(qi[b, s]).T @ w[b, s]
+        bound = 2e-6 * mag + 1e-30
+        assert (np.abs(got - ref) <= bound).all(), \
+            f"q{q}: max err {np.abs(got - ref).max():.3e}, ratio {(np.abs(got - ref) / bound).max():.2f}"
+
+
+# ---------------------------------------------------------------------------
+# step (b) alone, bit exact on seeded fp32 scores
+
+def _topk_cases(rng):
+    cases = []
+    for n in (255, 256, 257, 511, 512, 513, 1023, 1024, 1025, 4096, 16384):
+        s = rng.standard_normal(n).astype(np.float32)
+        cases.append(("normal", s))
+        q = (np.round(rng.standard_normal(n) * 4) / 4).astype(np.float32)    # many exact ties
+        cases.append(("ties", q))
+        p = rng.uniform(-1, 0, n).astype(np.float32)
+        planted = rng.choice(np.arange(n // 2, n), size=min(512, n // 2), replace=False)
+        p[planted] = rng.uniform(1, 2, planted.size).astype(np.float32)
+        cases.append(("planted_tail", p))
+    cases.append(("all_equal", np.full(3000, 2.5, np.float32)))
+    z = np.zeros(2000, np.float32)
+    z[::2] = -0.0
+    z[1500:] = -1.0
+    cases.append(("signed_zero", z))
+    cases.append(("neg_and_inf", np.concatenate([-np.abs(rng.standard_normal(900)).astype(np.float32),
+                                                 np.full(3, -np.inf, np.float32)])))
+    cases.append(("narrow_band", (100.0 + rng.standard_normal(16384) * 1e-4).astype(np.float32)))
+    return cases
+
+
+def test_topk_select_bit_exact():
+    rng = np.random.default_rng(2024)
+    cfg = BF16_CFG
+    cases = _topk_cases(rng)
+    dec = csa.Decoder(cfg, len(cases), 1, 65536)
+    ld = 16384
+    sc = np.full((len(cases), ld), np.nan, np.float32)
+    n = np.zeros(len(cases), np.int32)
+    for i, (_, s) in enumerate(cases):
+        sc[i, :s.size] = s
+        n[i] = s.size
+    idx = torch.empty(len(cases), cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(len(cases), dtype=torch.int32, device=DEV)
+    dec.topk_select(torch.from_numpy(sc).to(DEV), torch.from_numpy(n).to(DEV), idx, cnt)
+    assert dec.status() == csa.CSA_OK
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    for i, (name, s) in enumerate(cases):
+        ref = oracle.topk(s.astype(np.float64), cfg.topk)
+        assert gc[i] == ref.size, name
+        assert gi[i, :ref.size].tolist() == ref.tolist(), f"{name} n={s.size}"
+        assert (gi[i, ref.size:] == -1).all()
+
+
+# ---------------------------------------------------------------------------
+# edge cases: tiny and ragged lengths, bypass boundary, maximum length, poison
+
+def test_edge_lengths_flagship_shape():
+    # vis 0 (empty compressed stream), pos+1 not a multiple of 4, vis = K-1,K,K+1
+    # (bypass boundary), 1023..1025, ragged tails, and the maximum 16384
+    lens = [1, 2, 3, 4, 5, 130, 2047, 2048, 2051, 2052, 2055, 4095, 4096, 4100, 4103, 65536]
+    wl = Workload("edge", BF16_CFG, B=len(lens), S=1, L=1, seed=77)
+    hb = make_batch(wl, lens=lens, gap_rows=3)
+    g = run_step(wl, hb, max_context=65536, host_lens=True)
+    check_against_oracle(wl, hb, g, what="edge")
+
+
+def test_edge_lengths_without_host_lengths():
+    lens = [7, 2049, 3000, 700]
+    wl = Workload("edge2", BF16_CFG, B=len(lens), S=1, L=1, seed=78)
+    hb = make_batch(wl, lens=lens, gap_rows=2)
+    g = run_step(wl, hb, max_context=8192, host_lens=False)
+    check_against_oracle(wl, hb, g, what="edge2")
+
+
+def test_planted_tail_candidates_flagship_shape():
+    # key rows aligned with indexer head 0 planted past rows 256 and 1024: the
+    # selection must be exactly the planted rows
+    wl = Workload("planted", BF16_CFG, B=3, S=1, L=1, seed=91)
+    lens = [4 * 1100, 4 * 1500, 4 * 2100]
+    hb = make_batch(wl, lens=lens)
+    K = BF16_CFG.topk
+    rng = np.random.default_rng(5)
+    planted_all = []
+    for b, L in enumerate(lens):
+        vis = L // 4
+        qi = hb["q_idx"][b, 0].float()
+        qi[:] = qi[0]                           # every indexer head = head 0
+        hb["q_idx"][b, 0] = qi.to(torch.bfloat16)
+        off = int(hb["idx_off"][b])
+        u = qi[0] / qi[0].norm()
+        keys = -torch.rand(vis, 1) * u[None, :] * 4
+        planted = np.sort(rng.choice(np.arange(300, vis), size=K, replace=False))
+        keys[planted] = (1.0 + torch.rand(K, 1)) * u[None, :] * 4
+        hb["idx_k"][off:off + vis] = keys.to(torch.bfloat16)
+        planted_all.append(planted)
+    g = run_step(wl, hb)
+    assert g["status"] == csa.CSA_OK
+    for b in range(3):
+        assert g["idx"][b].tolist() == planted_all[b].tolist()
+    check_against_oracle(wl, hb, g, what="planted")
+
+
+def test_duplicate_keys_tie_to_lower_index():
+    wl = Workload("dups", BF16_CFG, B=1, S=1, L=1, seed=92)
+    L = 4 * 1000
+    hb = make_batch(wl, lens=[L])
+    off = int(hb["idx_off"][0])
+    hb["idx_k"][off:off + 1000] = hb["idx_k"][off]     # every key identical: all scores tie
+    g = run_step(wl, hb)
+    assert g["idx"][0].tolist() == list(range(BF16_CFG.topk))
+    check_against_oracle(wl, hb, g, what="dups")
+
+
+def test_multi_token_small():
+    cfg = CsaConfig(hca_ratio=128)
+    wl = Workload("mt", cfg, B=3, S=8, L=1, seed=93)
+    hb = make_batch(wl, lens=[2052, 700, 40000], gap_rows=1)
+    g = run_step(wl, hb, max_context=40000, host_lens=True)
+    check_against_oracle(wl, hb, g, what="multi-token")
+
+
+def test_generic_shapes_simt_path():
+    # shapes outside the tensor-core set (bf16 and fp32) run on the SIMT kernels
+    for dt in ("bf16", "f32"):
+        cfg = CsaConfig(H=6, D=48, V=32, Hi=3, Di=16, ratio=4, topk=5, win=4, hca_ratio=16, dtype=dt)
+        wl = Workload("generic", cfg, B=4, S=3, L=1, seed=94)
+        hb = make_batch(wl, lens=[3, 9, 40, 131], gap_rows=1)
+        g = run_step(wl, hb)
+        check_against_oracle(wl, hb, g, what=f"generic-{dt}")
+
+
+# ---------------------------------------------------------------------------
+# determinism, empty batch, device-side error reporting
+
+def test_bitwise_deterministic():
+    wl = WORKLOADS["topk_b16_l8192"]
+    hb = make_batch(wl)
+    g1 = run_step(wl, hb)
+    g2 = run_step(wl, hb)
+    np.testing.assert_array_equal(g1["out"], g2["out"])
+    np.testing.assert_array_equal(g1["idx"], g2["idx"])
+    np.testing.assert_array_equal(g1["lse"], g2["lse"])
+
+
+def test_empty_batch_is_a_noop():
+    wl = WORKLOADS["bypass_b16_l256"]
+    hb = make_batch(wl, lens=[256])
+    db = to_device(hb, DEV)
+    dec = csa.Decoder(wl.cfg, 4, 1, 256)
+    cb = csa.make_batch_struct(db)
+    cb.B = 0
+    out = torch.zeros(1, dtype=torch.bfloat16, device=DEV)
+    dec.decode_step(cb, out)
+    assert dec.last_launch_count() == 0 and dec.status() == csa.CSA_OK
+
+
+def test_device_side_bad_length_and_index_are_reported():
+    wl = Workload("bad", BF16_CFG, B=3, S=1, L=1, seed=95)
+    hb = make_batch(wl, lens=[3000, 2500, 600])
+    db = to_device(hb, DEV)
+    dec = csa.Decoder(wl.cfg, 3, 1, 4096)
+    # (1) a length beyond max_context in device memory: that query reads
+    # nothing and writes zeros; the others are unaffected
+    db["ctx_len"][1] = 5000
+    out = torch.full((3, 1, 64, 512), 7.0, dtype=torch.bfloat16, device=DEV)
+    dec.decode_step(csa.make_batch_struct(db), out)
+    assert dec.status() == csa.CSA_ERR_BAD_INDEX
+    assert (out[1] == 0).all()
+    ref = oracle.decode(wl.cfg, hb, qids=[0, 2])
+    assert_close(out[[0, 2]].float().cpu().numpy().reshape(2, 64, 512), ref["out"], TOL_BF16, "bad-len")
+    assert dec.status() == csa.CSA_OK   # the status was cleared by the read
+    # (2) caller indices out of range in csa_sparse_attn are skipped and reported
+    db["ctx_len"][1] = 2500
+    idx = torch.full((3, 1, 512), -1, dtype=torch.int32, device=DEV)
+    cnt = torch.zeros(3, 1, dtype=torch.int32, device=DEV)
+    idx[0, 0, :3] = torch.tensor([5, 10**6, 7])
+    cnt[0, 0] = 3
+    dec.sparse_attn(csa.make_batch_struct(db), idx, cnt, out)
+    assert dec.status() == csa.CSA_ERR_BAD_INDEX
+    assert torch.isfinite(out.float()).all()
+    # (3) a pool offset that points past the pool
+    db["cmp_off"][2] = 10**9
+    dec.decode_step(csa.make_batch_struct(db), out)
+    assert dec.status() == csa.CSA_ERR_BAD_INDEX
+    assert torch.isfinite(out.float()).all()
+
+
+def test_host_errors_leave_outputs_untouched():
+    wl = WORKLOADS["bypass_b16_l256"]
+    hb = make_batch(wl)
+    db = to_device(hb, DEV)
+    dec = csa.Decoder(wl.cfg, 16, 1, 256)
+    out = torch.full((16, 1, 64, 512), 3.0, dtype=torch.bfloat16, device=DEV)
+    cb = csa.make_batch_struct(db)
+    cb.B = 17   # above max_batch
+    with pytest.raises(csa.CsaError) as e:
+        dec.decode_step(cb, out)
+    assert e.value.code == csa.CSA_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert (out == 3.0).all()
