@@ -3,6 +3,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <string>
@@ -25,6 +26,7 @@ struct csa_handle {
   struct Mark { int stage; cudaEvent_t a, b; };
   std::vector<Mark> marks;
   std::vector<cudaEvent_t> spare;
+  csa::ItemList items;  // host-built indexer work list of the current call
 };
 
 namespace {
@@ -164,21 +166,39 @@ csa::DevBatch dev_batch(const csa_batch* b) {
   return d;
 }
 
-// Indexer work items (128-row chunks) when the host knows the lengths; -1 otherwise.
-int host_items(const csa_handle* h, const csa_batch* b, int score_all) {
-  if (!b->ctx_len_host) return -1;
+// The indexer's work list (see csa::ItemList): built here when the host knows
+// the lengths and B is small enough to pass by value; otherwise host_B = -1
+// and the prep kernel builds it on the device.
+void host_items(const csa_handle* h, const csa_batch* b, int score_all, csa::ItemList* it) {
+  it->host_B = -1;
+  if (!b->ctx_len_host || b->B > csa::kMaxHostReq) return;
   const csa_config& c = h->cfg;
-  int64_t items = 0;
+  int acc = 0;
   for (int i = 0; i < b->B; ++i) {
+    it->prefix[i] = acc;
     const int L = b->ctx_len_host[i];
     int rows = 0;
     for (int s = 0; s < b->S; ++s) {
       const int vis = (L - b->S + s + 1) / c.ratio;
       if (vis > c.topk || (score_all && vis > 0)) rows = vis > rows ? vis : rows;
     }
-    items += (rows + csa::kIdxChunk - 1) / csa::kIdxChunk;
+    acc += (rows + csa::kIdxChunk - 1) / csa::kIdxChunk;
   }
-  return (int)items;
+  it->prefix[b->B] = acc;
+  it->host_B = b->B;
+}
+
+// Programmatic dependent launch between the kernels of a call (and with the
+// stream's previous kernel): on unless CSA_PDL=0.  Every kernel waits for its
+// predecessor before touching global memory, so the overlap is only of launch
+// latency and prologues.
+bool use_pdl() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("CSA_PDL");
+    v = (e && strcmp(e, "0") == 0) ? 0 : 1;
+  }
+  return v == 1;
 }
 
 struct Launches {
@@ -196,6 +216,20 @@ int finish(csa_handle* h, const Launches& L) {
     return cuda_fail(e, "kernel launch");
   }
   return CSA_OK;
+}
+
+// plan (if needed) + indexer into `scores`
+void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int score_all,
+                 float* scores, int64_t ld, cudaStream_t st, Launches& L) {
+  csa::ItemList& items = h->items;
+  host_items(h, b, score_all, &items);
+  const bool pdl = use_pdl();
+  if (items.host_B < 0)
+    L.add(staged(h, kStagePlan, st,
+                 [&] { return csa::launch_prep(h->dc, db, h->ws, score_all, st, pdl); }));
+  L.add(staged(h, kStageIndexer, st, [&] {
+    return csa::launch_indexer(h->dc, db, h->ws, items, score_all, scores, ld, h->num_sms, st, pdl);
+  }));
 }
 
 }  // namespace
@@ -233,9 +267,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   size_t off = 0;
   const size_t o_status = off; off += al(sizeof(int));
-  const size_t o_plan = off; off += al(sizeof(csa::QueryPlan) * maxT);
   const size_t o_prefix = off; off += al(sizeof(int) * (cfg->max_batch + 1));
-  const size_t o_rows = off; off += al(sizeof(int) * cfg->max_batch);
   const size_t o_scores = off; off += al(sizeof(float) * ld * maxT);
   const size_t o_idx = off; off += al(sizeof(int) * (size_t)cfg->topk * maxT);
   const size_t o_cnt = off; off += al(sizeof(int) * maxT);
@@ -247,9 +279,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   if (e != cudaSuccess) { cudaFree(h->ws_base); delete h; return cuda_fail(e, "cudaMemset"); }
   csa::Workspace& w = h->ws;
   w.status = reinterpret_cast<int*>(base + o_status);
-  w.plan = reinterpret_cast<csa::QueryPlan*>(base + o_plan);
   w.item_prefix = reinterpret_cast<int*>(base + o_prefix);
-  w.req_rows = reinterpret_cast<int*>(base + o_rows);
   w.scores = reinterpret_cast<float*>(base + o_scores);
   w.topk_idx = reinterpret_cast<int*>(base + o_idx);
   w.topk_cnt = reinterpret_cast<int*>(base + o_cnt);
@@ -278,12 +308,13 @@ int csa_indexer_topk(csa_handle* h, const csa_batch* b, int32_t* topk_idx, int32
   if (b->B == 0) { h->last_launches = 0; return CSA_OK; }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const csa::DevBatch db = dev_batch(b);
+  const bool pdl = use_pdl();
   Launches L;
-  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, 0, nullptr, st); }));
-  L.add(staged(h, kStageIndexer, st, [&] { return csa::launch_indexer(h->dc, db, h->ws, h->ws.scores, h->ws.scores_ld, host_items(h, b, 0),
-                            h->num_sms, st); }));
-  L.add(staged(h, kStageTopk, st, [&] { return csa::launch_topk(h->dc, b->B * b->S, h->ws.plan, h->ws.scores, h->ws.scores_ld, nullptr,
-                         topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st); }));
+  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
+  L.add(staged(h, kStageTopk, st, [&] {
+    return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr,
+                            topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st, pdl);
+  }));
   return finish(h, L);
 }
 
@@ -296,9 +327,12 @@ int csa_sparse_attn(csa_handle* h, const csa_batch* b, const int32_t* topk_idx,
   if (b->B == 0) { h->last_launches = 0; return CSA_OK; }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const csa::DevBatch db = dev_batch(b);
+  const bool pdl = use_pdl();
   Launches L;
-  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, 0, topk_cnt, st); }));
-  L.add(staged(h, kStageAttention, st, [&] { return csa::launch_attention(h->dc, db, h->ws, topk_idx, topk_cnt, out, lse_out, h->num_sms, st); }));
+  L.add(staged(h, kStageAttention, st, [&] {
+    return csa::launch_attention(h->dc, db, h->ws, topk_idx, topk_cnt, out, lse_out, h->num_sms,
+                                 st, pdl);
+  }));
   return finish(h, L);
 }
 
@@ -313,13 +347,16 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
   const csa::DevBatch db = dev_batch(b);
   int* idx = topk_idx_out ? topk_idx_out : h->ws.topk_idx;
   int* cnt = topk_cnt_out ? topk_cnt_out : h->ws.topk_cnt;
+  const bool pdl = use_pdl();
   Launches L;
-  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, 0, nullptr, st); }));
-  L.add(staged(h, kStageIndexer, st, [&] { return csa::launch_indexer(h->dc, db, h->ws, h->ws.scores, h->ws.scores_ld, host_items(h, b, 0),
-                            h->num_sms, st); }));
-  L.add(staged(h, kStageTopk, st, [&] { return csa::launch_topk(h->dc, b->B * b->S, h->ws.plan, h->ws.scores, h->ws.scores_ld, nullptr,
-                         idx, cnt, h->ws.status, h->dc.max_vis, st); }));
-  L.add(staged(h, kStageAttention, st, [&] { return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse_out, h->num_sms, st); }));
+  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
+  L.add(staged(h, kStageTopk, st, [&] {
+    return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr, idx,
+                            cnt, h->ws.status, h->dc.max_vis, st, pdl);
+  }));
+  L.add(staged(h, kStageAttention, st, [&] {
+    return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse_out, h->num_sms, st, pdl);
+  }));
   return finish(h, L);
 }
 
@@ -333,9 +370,7 @@ int csa_indexer_scores(csa_handle* h, const csa_batch* b, float* scores, int64_t
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const csa::DevBatch db = dev_batch(b);
   Launches L;
-  L.add(staged(h, kStagePlan, st, [&] { return csa::launch_plan(h->dc, db, h->ws, score_all ? 1 : 0, nullptr, st); }));
-  L.add(staged(h, kStageIndexer, st, [&] { return csa::launch_indexer(h->dc, db, h->ws, scores, ld, host_items(h, b, score_all ? 1 : 0),
-                            h->num_sms, st); }));
+  run_indexer(h, b, db, score_all ? 1 : 0, scores, ld, st, L);
   return finish(h, L);
 }
 
@@ -347,9 +382,12 @@ int csa_topk_select(csa_handle* h, int32_t nq, const float* scores, int64_t ld, 
   if (!scores || !n || !topk_idx || !topk_cnt) return fail(CSA_ERR_INVALID_ARG, "NULL pointer");
   if (ld < 1) return fail(CSA_ERR_INVALID_ARG, "ld < 1");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool pdl = use_pdl();
   Launches L;
-  L.add(staged(h, kStageTopk, st, [&] { return csa::launch_topk(h->dc, nq, nullptr, scores, ld, n, topk_idx, topk_cnt, h->ws.status,
-                         h->dc.max_vis, st); }));
+  L.add(staged(h, kStageTopk, st, [&] {
+    return csa::launch_topk(h->dc, nullptr, nq, scores, ld, n, topk_idx, topk_cnt, h->ws.status,
+                            h->dc.max_vis, st, pdl);
+  }));
   return finish(h, L);
 }
 

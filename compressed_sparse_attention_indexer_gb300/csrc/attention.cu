@@ -83,9 +83,31 @@ __device__ __forceinline__ const __nv_bfloat16* row_pointer(const DevBatch& b, c
   return base + gr * stride;
 }
 
+// The query's plan, with its Top-K count taken from topk_cnt (written by the
+// Top-K kernel or supplied by the caller).  A count outside [0, min(vis, K)]
+// is clamped and reported, as is a bad length.
+__device__ __forceinline__ QueryPlan attn_plan(const DevCfg& c, const DevBatch& b, int q,
+                                               const int* __restrict__ topk_cnt, int* status,
+                                               bool report) {
+  const int bi = q / b.S;
+  QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
+  if (p.flags & kPlanBad) {
+    if (report) set_status(status, kStatusBadIndex);
+    return p;
+  }
+  int ci = topk_cnt[q];
+  if (ci < 0 || ci > p.cnt) {
+    if (report) set_status(status, kStatusBadIndex);
+    ci = ci < 0 ? 0 : p.cnt;
+  }
+  p.cnt = ci;
+  return p;
+}
+
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_tc_kernel(DevCfg c, DevBatch b, Workspace ws, const int* __restrict__ topk_idx,
-                   __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+                   const int* __restrict__ topk_cnt, __nv_bfloat16* __restrict__ out,
+                   float* __restrict__ lse_out) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* Qs = smem;
   uint8_t* Rs = Qs + kQsBytes;
@@ -93,7 +115,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __shared__ AttnShared sh;
 
   const int q = blockIdx.x >> 1, hh = blockIdx.x & 1;
-  const QueryPlan p = ws.plan[q];
+  pdl_wait();
+  pdl_trigger();
+  const QueryPlan p = attn_plan(c, b, q, topk_cnt, ws.status, threadIdx.x == 0 && hh == 0);
   const int bi = q / b.S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
@@ -368,11 +392,14 @@ constexpr int kSimtMaxVPerLane = 16;  // V <= 512
 template <typename T>
 __global__ void __launch_bounds__(256) attn_simt_kernel(DevCfg c, DevBatch b, Workspace ws,
                                                         const int* __restrict__ topk_idx,
+                                                        const int* __restrict__ topk_cnt,
                                                         T* __restrict__ out,
                                                         float* __restrict__ lse_out) {
   extern __shared__ float sbuf[];  // [warps][V]
   const int q = blockIdx.x;
-  const QueryPlan p = ws.plan[q];
+  pdl_wait();
+  pdl_trigger();
+  const QueryPlan p = attn_plan(c, b, q, topk_cnt, ws.status, threadIdx.x == 0);
   const int bi = q / b.S;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int V = c.V, D = c.D, R = c.R;
@@ -463,8 +490,7 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(DevCfg c, DevBatch b, Wo
 
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
-                     cudaStream_t st) {
-  (void)topk_cnt;
+                     cudaStream_t st, bool pdl) {
   (void)num_sms;
   const int T = b.B * b.S;
   if (T == 0) return 0;
@@ -474,19 +500,16 @@ int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, co
       cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
       attr_done = true;
     }
-    attn_tc_kernel<<<T * 2, kAttnThreads, kAttnSmem, st>>>(
-        c, b, ws, topk_idx, static_cast<__nv_bfloat16*>(out), lse_out);
-  } else {
-    const int threads = 256;
-    const int smem = (threads / 32) * c.V * 4;
-    if (c.dtype == CSA_DTYPE_BF16)
-      attn_simt_kernel<__nv_bfloat16><<<T, threads, smem, st>>>(
-          c, b, ws, topk_idx, static_cast<__nv_bfloat16*>(out), lse_out);
-    else
-      attn_simt_kernel<float><<<T, threads, smem, st>>>(c, b, ws, topk_idx,
-                                                        static_cast<float*>(out), lse_out);
+    return launch_kernel(attn_tc_kernel, dim3(T * 2), dim3(kAttnThreads), kAttnSmem, st, pdl, c, b,
+                         ws, topk_idx, topk_cnt, static_cast<__nv_bfloat16*>(out), lse_out);
   }
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  const int threads = 256;
+  const int smem = (threads / 32) * c.V * 4;
+  if (c.dtype == CSA_DTYPE_BF16)
+    return launch_kernel(attn_simt_kernel<__nv_bfloat16>, dim3(T), dim3(threads), smem, st, pdl, c,
+                         b, ws, topk_idx, topk_cnt, static_cast<__nv_bfloat16*>(out), lse_out);
+  return launch_kernel(attn_simt_kernel<float>, dim3(T), dim3(threads), smem, st, pdl, c, b, ws,
+                       topk_idx, topk_cnt, static_cast<float*>(out), lse_out);
 }
 
 }  // namespace csa

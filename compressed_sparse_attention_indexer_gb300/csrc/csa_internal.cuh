@@ -39,16 +39,65 @@ struct DevBatch {
   const void* hca; const int64_t* hca_off; int64_t hca_stride, hca_rows;
 };
 
+// Per-query quantities of the step (visibility, window, bypass).
 struct QueryPlan {
   int pos, vis, nwin, cnt, vis2, flags;
+};
+
+// Rows of one indexer work item (tensor-core and SIMT paths).
+constexpr int kIdxChunk = 128;
+
+// Query q = b*S + s of the batch: pos = L_b - S + s, vis = floor((pos+1)/ratio),
+// nwin = min(WIN, pos+1), cnt = min(vis, K), vis2 = floor((pos+1)/hca_ratio).
+// The indexer scores the query when vis > K (or every query with score_all).
+// A length outside [S, max_context] marks the query bad: nothing is read.
+// ("Perf: skip redundant CSA scoring and fuse gather unpack": bypass when the
+// visible rows fit Top-K; "Fix: port the DeepSeek-V4 MoE, hc_pre and prefill
+// fixes to DSpark": at most WIN + min(vis, K) sparse rows per query.)
+__device__ __forceinline__ QueryPlan query_plan(const DevCfg& c, int S, int L, int s,
+                                                int score_all) {
+  QueryPlan p;
+  p.pos = p.vis = p.nwin = p.cnt = p.vis2 = 0;
+  p.flags = 0;
+  if (L < S || L > c.max_context) {
+    p.flags = kPlanBad;
+    return p;
+  }
+  p.pos = L - S + s;
+  p.vis = (p.pos + 1) / c.ratio;
+  p.nwin = min(c.win, p.pos + 1);
+  p.vis2 = c.hca_ratio > 0 ? (p.pos + 1) / c.hca_ratio : 0;
+  p.cnt = min(p.vis, c.K);
+  p.flags = (p.vis > c.K || (score_all && p.vis > 0)) ? kPlanScore : 0;
+  return p;
+}
+
+// Rows the indexer scores for a request: the largest vis among its scored
+// queries (vis grows with s, so the last scored query decides).
+__device__ __forceinline__ int request_rows(const DevCfg& c, int S, int L, int score_all) {
+  if (L < S || L > c.max_context) return 0;
+  int rows = 0;
+  for (int s = 0; s < S; ++s) {
+    const int vis = (L - S + s + 1) / c.ratio;
+    if (vis > c.K || (score_all && vis > 0)) rows = max(rows, vis);
+  }
+  return rows;
+}
+
+// Indexer work list: prefix[b] = first item (128-row chunk) of request b,
+// prefix[B] = number of items.  Passed by value when the host knows the
+// lengths and B <= kMaxHostReq, else computed on the device by the prep
+// kernel into the workspace (host_B = -1 then).
+constexpr int kMaxHostReq = 1024;
+struct ItemList {
+  int host_B;
+  int prefix[kMaxHostReq + 1];
 };
 
 // Device workspace owned by a handle.
 struct Workspace {
   int* status;        // [1]
-  QueryPlan* plan;    // [max_T]
-  int* item_prefix;   // [max_batch + 1] indexer work items (row chunks) per request, prefix
-  int* req_rows;      // [max_batch] rows the indexer scores for request b
+  int* item_prefix;   // [max_batch + 1] device-computed work list (see ItemList)
   float* scores;      // [max_T, max_vis]
   int* topk_idx;      // [max_T, K]
   int* topk_cnt;      // [max_T]
@@ -56,26 +105,54 @@ struct Workspace {
   int64_t scores_ld;
 };
 
-// Rows of one indexer work item (tensor-core and SIMT paths).
-constexpr int kIdxChunk = 128;
+__device__ __forceinline__ void set_status(int* status, int bit) { atomicOr(status, bit); }
 
-__device__ __forceinline__ void set_status(int* status, int bit) {
-  atomicOr(status, bit);
+// Programmatic dependent launch: wait for the grid this one depends on to
+// complete (a no-op when launched without the attribute), and let the next
+// grid in the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Launch with or without the programmatic-stream-serialisation attribute.
+// Returns 1 on a successful launch, -1 otherwise.
+template <typename... KArgs, typename... Args>
+int launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                  bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? at : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...) == cudaSuccess ? 1 : -1;
 }
 
 // ---- launch wrappers (defined in the kernel files) -------------------------
 // Each returns the number of kernels launched (>= 0) or -1 on a launch error.
-int launch_plan(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all,
-                const int* topk_cnt_in, cudaStream_t st);
-int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, float* scores,
-                   int64_t ld, int total_items_hint, int num_sms, cudaStream_t st);
-int launch_topk(const DevCfg& c, int nq, const QueryPlan* plan, const float* scores, int64_t ld,
+// `pdl`: launch as a programmatic dependent of the previous kernel.
+int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all,
+                cudaStream_t st, bool pdl);
+int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
+                   int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
+                   bool pdl);
+int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
+                       const ItemList& items, int score_all, float* scores, int64_t ld,
+                       int num_sms, cudaStream_t st, bool pdl);
+int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st);
+                cudaStream_t st, bool pdl);
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
-                     cudaStream_t st);
+                     cudaStream_t st, bool pdl);
 
 bool tensor_core_shape(const DevCfg& c);
+constexpr int kIndexerMma = 0, kIndexerTc5 = 1;
+int indexer_impl();
 
 }  // namespace csa

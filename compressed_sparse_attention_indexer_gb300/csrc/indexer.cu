@@ -5,16 +5,19 @@
 // scoring it skips) and "Fix: port the DeepSeek-V4 MoE, hc_pre and prefill
 // fixes to DSpark" (partials reduced in a fixed ascending order, no atomics).
 //
-// Tensor-core path (bf16, Hi = 64, Di = 128): a persistent grid walks the
-// work list of 128-row chunks made by the plan kernel.  Each chunk of k_idx
-// rows is streamed from HBM once into shared memory through a multi-stage
-// cp.async ring and reused by every scored query of its request.  The
-// contraction is rows x heads x 128 on warp MMA (rows are the M side, heads
-// the N side), so each row ends in registers of one quad; the epilogue
-// applies ReLU, and one lane per row and head-half sums w_h * ReLU(.) over
-// h in ascending order, then the two halves are added in order.
-//
-// SIMT path: any shape and dtype, one warp per row, fp32 FMA.
+// This file holds the launcher and two kernels:
+//  - a warp-MMA (mma.sync) kernel for the tensor-core shape, kept as the
+//    measured baseline of the tcgen05 kernel (indexer_tc5.cu), selected with
+//    CSA_INDEXER=mma: a persistent grid walks the work list of 128-row
+//    chunks; each chunk of k_idx rows is streamed once into shared memory
+//    through a multi-stage cp.async ring and reused by every scored query of
+//    its request; rows are the M side of the MMA, heads the N side; lanes of
+//    a row sum w_h * ReLU(.) over h = 0..31 and 32..63 in order and the two
+//    halves are added in that order;
+//  - a SIMT kernel for any other shape / dtype: one warp per row, fp32 FMA.
+#include <stdlib.h>
+#include <string.h>
+
 #include "csa_internal.cuh"
 #include "ptx.cuh"
 
@@ -35,50 +38,59 @@ __device__ __forceinline__ void wait_stages(int nst) {
   else cp_async_wait<0>();
 }
 
+__device__ __forceinline__ int request_of(const int* prefix, int B, int item) {
+  int l = 0, r = B - 1;
+  while (l < r) {
+    const int m = (l + r + 1) >> 1;
+    if (prefix[m] <= item) l = m; else r = m - 1;
+  }
+  return l;
+}
+
 __global__ void __launch_bounds__(kIdxThreads, 1)
-    indexer_tc_kernel(DevCfg c, DevBatch b, Workspace ws, float* __restrict__ scores,
-                      int64_t ld, int SG, int NST) {
+    indexer_mma_kernel(const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
+                       int score_all, float* __restrict__ scores, int64_t ld, int SG, int NST) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* Qs = smem;
   uint8_t* Ks = Qs + SG * kQBytes;
   float* stash = reinterpret_cast<float*>(Ks + NST * kKStageBytes);
   float* w_s = stash + (kIdxThreads / 32) * 16 * kStashLd;
 
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int* __restrict__ prefix = ws.item_prefix;
+  const int* __restrict__ prefix = items.host_B >= 0 ? items.prefix : ws.item_prefix;
   const int N = prefix[b.B];
   const int G = gridDim.x;
   const int lo = (int)((int64_t)blockIdx.x * N / G);
   const int hi = (int)((int64_t)(blockIdx.x + 1) * N / G);
+  pdl_trigger();
   if (lo >= hi) return;
 
-  // request owning item lo: the last bi with prefix[bi] <= lo
-  int b0 = 0;
-  {
-    int l = 0, r = b.B - 1;
-    while (l < r) {
-      const int m = (l + r + 1) >> 1;
-      if (prefix[m] <= lo) l = m; else r = m - 1;
-    }
-    b0 = l;
-  }
+  const int b0 = request_of(prefix, b.B, lo);
   const __nv_bfloat16* __restrict__ kbase = static_cast<const __nv_bfloat16*>(b.idx);
 
-  int ib = b0;  // issue cursor
+  // issue cursor, with the request's values cached
+  int ib = b0, ib_end = prefix[b0 + 1], ib_first = prefix[b0];
+  int ib_rows = request_rows(c, b.S, b.ctx_len[b0], score_all);
+  int64_t ib_off = b.idx_off[b0];
   auto issue = [&](int item) {
-    while (item >= prefix[ib + 1]) ++ib;
-    const int c0 = (item - prefix[ib]) * kIdxChunk;
-    const int rows = ws.req_rows[ib];
-    const int64_t off = b.idx_off[ib];
+    while (item >= ib_end) {
+      ++ib;
+      ib_first = ib_end;
+      ib_end = prefix[ib + 1];
+      ib_rows = request_rows(c, b.S, b.ctx_len[ib], score_all);
+      ib_off = b.idx_off[ib];
+    }
+    const int c0 = (item - ib_first) * kIdxChunk;
     uint8_t* dst0 = Ks + (item % NST) * kKStageBytes;
 #pragma unroll
     for (int i = 0; i < (kIdxChunk * 16) / kIdxThreads; ++i) {
       const int id = tid + i * kIdxThreads;
       const int row = id >> 4, ch = id & 15;
       const int r = c0 + row;
-      const int64_t gr = off + r;
+      const int64_t gr = ib_off + r;
       const bool inb = gr >= 0 && gr < b.idx_rows;
-      const bool want = r < rows;
+      const bool want = r < ib_rows;
       if (want && !inb && ch == 0) set_status(ws.status, kStatusBadIndex);
       const bool ok = want && inb;
       const void* src = ok ? (const void*)(kbase + gr * b.idx_stride + ch * 8) : (const void*)kbase;
@@ -91,7 +103,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
     cp_async_commit();
   }
 
-  int cb = b0, q_b = -1, q_g = -1;
+  int cb = b0, cb_end = prefix[b0 + 1], cb_first = prefix[b0], cb_L = b.ctx_len[b0];
+  int q_b = -1, q_g = -1;
   for (int it = lo; it < hi; ++it) {
     wait_stages(NST);
     __syncthreads();
@@ -100,8 +113,13 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       if (nxt < hi) issue(nxt);
       cp_async_commit();
     }
-    while (it >= prefix[cb + 1]) ++cb;
-    const int c0 = (it - prefix[cb]) * kIdxChunk;
+    while (it >= cb_end) {
+      ++cb;
+      cb_first = cb_end;
+      cb_end = prefix[cb + 1];
+      cb_L = b.ctx_len[cb];
+    }
+    const int c0 = (it - cb_first) * kIdxChunk;
     const uint8_t* Kst = Ks + (it % NST) * kKStageBytes;
 
     // A fragments: this warp's 16 key rows x 128 dims, kept across queries
@@ -135,7 +153,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
       for (int sl = 0; sl < ng; ++sl) {
         const int qid = cb * b.S + g0 + sl;
-        const QueryPlan p = ws.plan[qid];
+        const QueryPlan p = query_plan(c, b.S, cb_L, g0 + sl, score_all);
         if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
         float acc[8][4];
 #pragma unroll
@@ -192,13 +210,16 @@ __device__ __forceinline__ float ldf<__nv_bfloat16>(const __nv_bfloat16* p, int6
 
 template <typename T>
 __global__ void __launch_bounds__(256) indexer_simt_kernel(DevCfg c, DevBatch b, Workspace ws,
+                                                           int score_all,
                                                            float* __restrict__ scores,
                                                            int64_t ld) {
+  pdl_wait();
+  pdl_trigger();
   const int q = blockIdx.x;
-  const QueryPlan p = ws.plan[q];
+  const int bi = q / b.S;
+  const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, score_all);
   if (!(p.flags & kPlanScore)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int bi = q / b.S;
   const T* qi = static_cast<const T*>(b.q_idx) + (int64_t)q * c.Hi * c.Di;
   const float* wq = b.w + (int64_t)q * c.Hi;
   const T* kp = static_cast<const T*>(b.idx);
@@ -225,14 +246,32 @@ __global__ void __launch_bounds__(256) indexer_simt_kernel(DevCfg c, DevBatch b,
 
 }  // namespace
 
+// Indexer kernel for the tensor-core shape: the tcgen05 kernel by default;
+// CSA_INDEXER=mma in the environment selects the warp-MMA kernel (kept as the
+// measured baseline of the tcgen05 one).
+int indexer_impl() {
+  static int impl = -1;
+  if (impl < 0) {
+    const char* e = getenv("CSA_INDEXER");
+    impl = (e && strcmp(e, "mma") == 0) ? kIndexerMma : kIndexerTc5;
+  }
+  return impl;
+}
+
 bool tensor_core_shape(const DevCfg& c) {
   return c.dtype == CSA_DTYPE_BF16 && c.H == kTcH && c.D == kTcD && c.V == kTcV &&
          c.Hi == kTcHi && c.Di == kTcDi;
 }
 
-int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, float* scores,
-                   int64_t ld, int total_items_hint, int num_sms, cudaStream_t st) {
-  if (total_items_hint == 0) return 0;
+int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
+                   int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
+                   bool pdl) {
+  const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;  // items, if known
+  if (known == 0) return 0;
+  if (tensor_core_shape(c) && indexer_impl() == kIndexerTc5) {
+    const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, st, pdl);
+    if (r != -2) return r;  // -2: shape outside the tcgen05 kernel, use warp MMA
+  }
   if (tensor_core_shape(c)) {
     const int SG = b.S < 8 ? b.S : 8;
     const int fixed = SG * kQBytes + kStashBytes + SG * kTcHi * 4;
@@ -242,24 +281,24 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, floa
     const int smem = fixed + NST * kKStageBytes;
     static bool attr_done = false;
     if (!attr_done) {
-      cudaFuncSetAttribute(indexer_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(indexer_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            227 * 1024);
       attr_done = true;
     }
     int grid = num_sms;
-    if (total_items_hint > 0 && total_items_hint < grid) grid = total_items_hint;
-    indexer_tc_kernel<<<grid, kIdxThreads, smem, st>>>(c, b, ws, scores, ld, SG, NST);
-  } else {
-    int y = (c.max_vis + 7) / 8;
-    if (y > 64) y = 64;
-    if (y < 1) y = 1;
-    dim3 grid(b.B * b.S, y);
-    if (c.dtype == CSA_DTYPE_BF16)
-      indexer_simt_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(c, b, ws, scores, ld);
-    else
-      indexer_simt_kernel<float><<<grid, 256, 0, st>>>(c, b, ws, scores, ld);
+    if (known > 0 && known < grid) grid = known;
+    return launch_kernel(indexer_mma_kernel, dim3(grid), dim3(kIdxThreads), smem, st, pdl, items,
+                         c, b, ws, score_all, scores, ld, SG, NST);
   }
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  int y = (c.max_vis + 7) / 8;
+  if (y > 64) y = 64;
+  if (y < 1) y = 1;
+  const dim3 grid(b.B * b.S, y);
+  if (c.dtype == CSA_DTYPE_BF16)
+    return launch_kernel(indexer_simt_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, pdl, c, b, ws,
+                         score_all, scores, ld);
+  return launch_kernel(indexer_simt_kernel<float>, grid, dim3(256), 0, st, pdl, c, b, ws,
+                       score_all, scores, ld);
 }
 
 }  // namespace csa

@@ -1,0 +1,336 @@
+// Step (a) on the fifth-generation tensor cores: the lightning-indexer score
+//   score_j = sum_h w_h * ReLU(q_idx[h] . k_idx[j])
+// with TMA-fed shared memory, tcgen05 MMA and TMEM accumulators.
+// hw-native-sys/pypto-lib "Perf: skip redundant CSA scoring and fuse gather
+// unpack" (the indexer) and "Fix: port the DeepSeek-V4 MoE, hc_pre and
+// prefill fixes to DSpark" (fixed, ascending reduction order; no atomics).
+//
+// Persistent kernel, one CTA per SM, warp-specialised:
+//   warp 4  TMA producer: per work item (128 key rows of one request) two
+//           128x64 bf16 boxes, 128-byte swizzled, into a ring of stages;
+//           the request's q_idx (S queries x 64 heads x 128) when the
+//           request changes;
+//   warp 5  allocates 512 TMEM columns; one thread issues the MMAs:
+//           D[128 rows x 64*G heads] = K_tile[128 x 128] . Q^T, M = 128,
+//           N = 64*G (G <= 4 queries per MMA), eight K = 16 steps, into one
+//           of two TMEM accumulators, then commits to mbarriers;
+//   warps 0-3 epilogue: thread t owns TMEM lane t = key row t of the item;
+//           it reads that row's 64 head dot products of a query and sums
+//           w_h * ReLU(.) over h = 0..63 in order, then writes the score.
+// HBM reads per item are the 32 KB of keys (q_idx comes from L2), so the
+// kernel runs at the HBM roofline when enough stages are in flight.
+// Every mbarrier wait is bounded; a wait that gives up records
+// CSA_ERR_TIMEOUT in the status word and the whole block winds down.
+#include <cudaTypedefs.h>
+
+#include "csa_internal.cuh"
+#include "tc5.cuh"
+
+namespace csa {
+
+namespace {
+
+constexpr int kT5Threads = 192;
+constexpr int kSubBytes = kIdxChunk * 64 * 2;   // 128 rows x 64 dims bf16 = 16 KB
+constexpr int kStageBytes = 2 * kSubBytes;      // 32 KB: one item of keys
+constexpr int kQSubBytes = kTcHi * 64 * 2;      // 64 heads x 64 dims = 8 KB
+constexpr int kTmemCols = 512;
+constexpr int kAccCols = 256;                   // one accumulator buffer (N <= 256)
+constexpr int kMaxG = 4;                        // queries per MMA group
+
+struct T5Smem {
+  uint64_t full[8], empty[8], qfull[2], qempty[2], tfull[2], tempty[2], done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Walks the work list in item order: the request owning the current item and
+// its item range, re-read only when the request changes (the single-thread
+// roles would otherwise pay a dependent global load per item).
+struct ReqCursor {
+  const int* prefix;
+  int bi, first, end;
+  __device__ __forceinline__ void init(const int* p, int B, int item) {
+    prefix = p;
+    int l = 0, r = B - 1;
+    while (l < r) {
+      const int m = (l + r + 1) >> 1;
+      if (p[m] <= item) l = m; else r = m - 1;
+    }
+    bi = l;
+    first = p[l];
+    end = p[l + 1];
+  }
+  // advances to the request owning `item`; true if it changed
+  __device__ __forceinline__ bool advance(int item) {
+    bool moved = false;
+    while (item >= end) {
+      ++bi;
+      first = end;
+      end = prefix[bi + 1];
+      moved = true;
+    }
+    return moved;
+  }
+};
+
+__global__ void __launch_bounds__(kT5Threads, 1)
+    indexer_tc5_kernel(const __grid_constant__ CUtensorMap kmap,
+                       const __grid_constant__ CUtensorMap qmap,
+                       const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
+                       int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 below
+  __shared__ T5Smem sm;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t kbuf = base;                                  // NST x 32 KB
+  const int S = b.S;
+  const uint32_t qbytes = (uint32_t)S * 2u * kQSubBytes;       // one request's q_idx
+  const uint32_t qbuf = kbuf + (uint32_t)NST * kStageBytes;    // NQB x qbytes
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();
+  const int* __restrict__ prefix = items.host_B >= 0 ? items.prefix : ws.item_prefix;
+  const int N = prefix[b.B];
+  const int lo = (int)((int64_t)blockIdx.x * N / gridDim.x);
+  const int hi = (int)((int64_t)(blockIdx.x + 1) * N / gridDim.x);
+  pdl_trigger();
+  if (lo >= hi) return;
+
+  const int G = S < kMaxG ? S : kMaxG;
+  const int ngroups = (S + G - 1) / G;
+  volatile int* abort = &sm.abort;
+
+  if (warp == 5) {
+    tc5::tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tc5::tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      tc5::mbar_init(smem_u32(&sm.full[i]), 1);
+      tc5::mbar_init(smem_u32(&sm.empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc5::mbar_init(smem_u32(&sm.qfull[i]), 1);
+      tc5::mbar_init(smem_u32(&sm.qempty[i]), 1);
+      tc5::mbar_init(smem_u32(&sm.tfull[i]), 1);
+      tc5::mbar_init(smem_u32(&sm.tempty[i]), 128);
+    }
+    tc5::mbar_init(smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    tc5::fence_mbar_init();
+  }
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tc5::prefetch_tmap(&kmap);
+      tc5::prefetch_tmap(&qmap);
+      int kc = 0, qc = 0;
+      ReqCursor cur;
+      cur.init(prefix, b.B, lo);
+      int64_t off = 0;
+      for (int it = lo; it < hi && !*abort; ++it) {
+        if (cur.advance(it) || it == lo) {
+          off = b.idx_off[cur.bi];
+          const int qb = qc % NQB;
+          if (qc >= NQB && !tc5::mbar_wait(smem_u32(&sm.qempty[qb]), ((qc / NQB) - 1) & 1, abort))
+            break;
+          tc5::mbar_expect_tx(smem_u32(&sm.qfull[qb]), qbytes);
+          for (int s = 0; s < S; ++s)
+            for (int kt = 0; kt < 2; ++kt)
+              tc5::tma_load_2d(qbuf + qb * qbytes + kt * (S * kQSubBytes) + s * kQSubBytes, &qmap,
+                               kt * 64, (cur.bi * S + s) * kTcHi, smem_u32(&sm.qfull[qb]));
+          ++qc;
+        }
+        const int st = kc % NST;
+        if (kc >= NST && !tc5::mbar_wait(smem_u32(&sm.empty[st]), ((kc / NST) - 1) & 1, abort))
+          break;
+        const int y = (int)(off + (int64_t)(it - cur.first) * kIdxChunk);
+        tc5::mbar_expect_tx(smem_u32(&sm.full[st]), kStageBytes);
+        tc5::tma_load_2d(kbuf + st * kStageBytes, &kmap, 0, y, smem_u32(&sm.full[st]));
+        tc5::tma_load_2d(kbuf + st * kStageBytes + kSubBytes, &kmap, 64, y, smem_u32(&sm.full[st]));
+        ++kc;
+      }
+      // let every copy this thread started land before the block exits
+      for (int k = (kc > NST ? kc - NST : 0); k < kc; ++k)
+        tc5::mbar_wait_drain(smem_u32(&sm.full[k % NST]), (k / NST) & 1);
+      if (qc > 0) tc5::mbar_wait_drain(smem_u32(&sm.qfull[(qc - 1) % NQB]), ((qc - 1) / NQB) & 1);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int kc = 0, qc = 0, job = 0;
+      ReqCursor cur;
+      cur.init(prefix, b.B, lo);
+      for (int it = lo; it < hi && !*abort; ++it) {
+        if (cur.advance(it) || it == lo) {
+          if (qc > 0) tc5::mma_commit(smem_u32(&sm.qempty[(qc - 1) % NQB]));
+          const int qb = qc % NQB;
+          if (!tc5::mbar_wait(smem_u32(&sm.qfull[qb]), (qc / NQB) & 1, abort)) break;
+          ++qc;
+        }
+        const int st = kc % NST;
+        if (!tc5::mbar_wait(smem_u32(&sm.full[st]), (kc / NST) & 1, abort)) break;
+        tc5::fence_after_sync();
+        const uint32_t ka = kbuf + st * kStageBytes;
+        const uint32_t qa = qbuf + ((qc - 1) % NQB) * qbytes;
+        bool ok = true;
+        for (int g = 0; g < ngroups; ++g) {
+          const int gn = min(G, S - g * G);
+          const int tb = job & 1;
+          if (job >= 2 && !tc5::mbar_wait(smem_u32(&sm.tempty[tb]), ((job >> 1) - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc5::fence_after_sync();
+          const uint32_t idesc = tc5::idesc_bf16_f32(128, 64 * gn);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (uint32_t)(k & 3) * 32u;
+            const uint64_t ad = tc5::sdesc_k_sw128(ka + (k >> 2) * kSubBytes + off);
+            const uint64_t bd =
+                tc5::sdesc_k_sw128(qa + (k >> 2) * (S * kQSubBytes) + g * G * kQSubBytes + off);
+            tc5::mma_bf16(tmem + tb * kAccCols, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          tc5::mma_commit(smem_u32(&sm.tfull[tb]));
+          ++job;
+        }
+        if (!ok) break;
+        tc5::mma_commit(smem_u32(&sm.empty[st]));
+        ++kc;
+      }
+      // every MMA issued above has finished before TMEM is freed
+      tc5::mma_commit(smem_u32(&sm.done));
+      tc5::mbar_wait_drain(smem_u32(&sm.done), 0);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int row = warp * 32 + lane;  // TMEM lane = key row within the item
+    int job = 0;
+    ReqCursor cur;
+    cur.init(prefix, b.B, lo);
+    int L = 0;
+    int64_t off = 0;
+    for (int it = lo; it < hi && !*abort; ++it) {
+      if (cur.advance(it) || it == lo) {
+        L = b.ctx_len[cur.bi];
+        off = b.idx_off[cur.bi];
+      }
+      const int bi = cur.bi;
+      const int c0 = (it - cur.first) * kIdxChunk;
+      const int64_t gr = off + c0 + row;
+      const bool in_pool = gr >= 0 && gr < b.idx_rows;
+      bool ok = true;
+      for (int g = 0; g < ngroups; ++g) {
+        const int gn = min(G, S - g * G);
+        const int tb = job & 1;
+        if (!tc5::mbar_wait(smem_u32(&sm.tfull[tb]), (job >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc5::fence_after_sync();
+        for (int sl = 0; sl < gn; ++sl) {
+          const int qid = bi * S + g * G + sl;
+          const QueryPlan p = query_plan(c, S, L, g * G + sl, score_all);
+          if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
+          const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + tb * kAccCols + sl * kTcHi;
+          const float* wq = b.w + (int64_t)qid * kTcHi;
+          float v[32];
+          float sum = 0.f;
+          tc5::tmem_ld32(ta, v);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) sum = fmaf(__ldg(wq + h), fmaxf(v[h], 0.f), sum);
+          tc5::tmem_ld32(ta + 32, v);
+#pragma unroll
+          for (int h = 0; h < 32; ++h) sum = fmaf(__ldg(wq + 32 + h), fmaxf(v[h], 0.f), sum);
+          const int j = c0 + row;
+          if (j < p.vis) {
+            if (!in_pool) set_status(ws.status, kStatusBadIndex);
+            scores[(int64_t)qid * ld + j] = sum;
+          }
+        }
+        tc5::fence_before_sync();
+        tc5::mbar_arrive(smem_u32(&sm.tempty[tb]));
+        ++job;
+      }
+      if (!ok) break;
+    }
+  }
+
+  if (tid == 0 && *abort) set_status(ws.status, kStatusTimeout);
+  tc5::fence_before_sync();
+  __syncthreads();
+  tc5::fence_after_sync();
+  if (warp == 5) tc5::tmem_dealloc(tmem, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2D bf16 tensor [rows, cols] with a row stride in elements; boxes of
+// [box_rows, 64] (64 bf16 = one 128-byte swizzle row).
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t stride,
+              uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {stride * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Launches the tcgen05 indexer; returns 1 on launch, 0 with nothing to do,
+// -1 if the launch (or the tensor-map encoding) failed, -2 if the shape does
+// not fit this kernel (the caller then uses the warp-MMA kernel).
+int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
+                       const ItemList& items, int score_all, float* scores, int64_t ld,
+                       int num_sms, cudaStream_t st, bool pdl) {
+  const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;
+  if (known == 0) return 0;
+  if (b.idx_rows <= 0 || b.idx_rows > 0x7fffffffLL) return -2;
+  const int S = b.S;
+  const int qbytes = S * 2 * kQSubBytes;
+  int NQB = 2, NST = 0;
+  const int budget = 227 * 1024 - 1024 - (int)sizeof(T5Smem) - 64;
+  for (NQB = 2; NQB >= 1; --NQB) {
+    NST = (budget - NQB * qbytes) / kStageBytes;
+    if (NST > 8) NST = 8;
+    if (NST >= 3) break;
+  }
+  if (NQB < 1 || NST < 2) return -2;
+  CUtensorMap kmap, qmap;
+  if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk)) return -1;
+  if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
+  const int smem = 1024 + NST * kStageBytes + NQB * qbytes;
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(indexer_tc5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         227 * 1024 - (int)sizeof(T5Smem));
+    attr = true;
+  }
+  int grid = num_sms;
+  if (known > 0 && known < grid) grid = known;
+  return launch_kernel(indexer_tc5_kernel, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap, qmap,
+                       items, c, b, ws, score_all, scores, ld, NST, NQB);
+}
+
+}  // namespace csa

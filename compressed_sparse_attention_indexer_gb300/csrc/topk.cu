@@ -10,8 +10,8 @@
 // keys in shared memory (-0.0 folded onto +0.0, NaN below every number).  The
 // bits above the highest bit on which the keys differ are skipped; then
 // radix-select passes of up to 11 bits each build a histogram of the next
-// digit among keys that still match the prefix (warp-aggregated shared
-// atomics: integer counts, so the result is order independent) and pick the
+// digit among keys that still match the prefix (shared-memory integer
+// atomics: counts, so the result is order independent) and pick the
 // digit holding the K-th largest key.  The passes stop as soon as the digit's
 // keys are exactly the ones still needed.  A final pass over contiguous index
 // ranges keeps every key above the prefix and the lowest-index keys equal to
@@ -33,9 +33,13 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Key i lives at keys[kpad(i)]: one pad word per 16 keys, so the final pass
+// (thread t reads keys 16t .. 16t+15) hits 32 different banks.
+__device__ __forceinline__ int kpad(int i) { return i + (i >> 4); }
+
 __global__ void __launch_bounds__(kTopkThreads, 1)
-    topk_kernel(int K, const QueryPlan* __restrict__ plan, const float* __restrict__ scores,
-                int64_t ld, const int* __restrict__ n_override, int* __restrict__ idx_out,
+    topk_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
+                const int* __restrict__ n_override, int* __restrict__ idx_out,
                 int* __restrict__ cnt_out, int* __restrict__ status, int max_vis) {
   extern __shared__ __align__(16) uint32_t keys[];
   __shared__ int hist[kBins];
@@ -43,7 +47,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   __shared__ uint32_t s_or;
   __shared__ int s_bin, s_above;
 
+  const int K = c.K;
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  pdl_wait();
+  pdl_trigger();
   int n;
   bool do_select;
   if (n_override) {
@@ -54,8 +61,10 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     }
     do_select = n > K;
   } else {
-    const QueryPlan p = plan[q];
-    n = (p.flags & kPlanBad) ? 0 : p.vis;
+    const int bi = q / b.S;
+    const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
+    if ((p.flags & kPlanBad) && tid == 0) set_status(status, kStatusBadIndex);
+    n = p.vis;
     do_select = n > K;  // vis > K: scored; otherwise the bypass
   }
   int* out = idx_out + (int64_t)q * K;
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   uint32_t acc_or = 0u;
   for (int i = tid; i < n; i += kTopkThreads) {
     const uint32_t k = score_key(sc[i]);
-    keys[i] = k;
+    keys[kpad(i)] = k;
     acc_or |= k ^ k0;
   }
 #pragma unroll
@@ -94,17 +103,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     __syncthreads();
     for (int r = 0; r < rounds; ++r) {
       const int i = r * kTopkThreads + tid;
-      bool valid = false;
-      uint32_t digit = 0;
       if (i < n) {
-        const uint32_t k = keys[i];
-        valid = (start >= 32) || ((k >> start) == prefix);
-        digit = (k >> sh) & mask;
-      }
-      const unsigned act = __ballot_sync(0xffffffffu, valid);
-      if (valid) {
-        const unsigned peers = __match_any_sync(act, digit);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[digit], __popc(peers));
+        const uint32_t k = keys[kpad(i)];
+        if ((start >= 32) || ((k >> start) == prefix)) atomicAdd(&hist[(k >> sh) & mask], 1);
       }
     }
     __syncthreads();
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   const int i0 = tid * per, i1 = min(n, i0 + per);
   int gt = 0, eq = 0;
   for (int i = i0; i < i1; ++i) {
-    const uint32_t hk = start >= 32 ? 0u : (keys[i] >> start);
+    const uint32_t hk = start >= 32 ? 0u : (keys[kpad(i)] >> start);
     gt += hk > prefix;
     eq += hk == prefix;
   }
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   const int pos0 = block_exclusive_scan(gt + eq_take, scan_tmp, &tot);
   int pos = pos0, taken_eq = 0;
   for (int i = i0; i < i1; ++i) {
-    const uint32_t hk = start >= 32 ? 0u : (keys[i] >> start);
+    const uint32_t hk = start >= 32 ? 0u : (keys[kpad(i)] >> start);
     bool sel = hk > prefix;
     if (hk == prefix && taken_eq < eq_take) {
       sel = true;
@@ -167,19 +168,20 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 
 }  // namespace
 
-int launch_topk(const DevCfg& c, int nq, const QueryPlan* plan, const float* scores, int64_t ld,
+int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st) {
+                cudaStream_t st, bool pdl) {
   if (nq == 0) return 0;
-  const int smem = max_vis * 4 > 16 ? max_vis * 4 : 16;
+  const int smem = (max_vis + max_vis / 16 + 1) * 4;
   static int attr_smem = 0;
   if (smem > 48 * 1024 && smem > attr_smem) {
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attr_smem = smem;
   }
-  topk_kernel<<<nq, kTopkThreads, smem, st>>>(c.K, plan, scores, ld, n_override, idx_out,
-                                             cnt_out, status, max_vis);
-  return cudaGetLastError() == cudaSuccess ? 1 : -1;
+  DevBatch none = {};
+  none.S = 1;
+  return launch_kernel(topk_kernel, dim3(nq), dim3(kTopkThreads), smem, st, pdl, c, b ? *b : none,
+                       scores, ld, n_override, idx_out, cnt_out, status, max_vis);
 }
 
 }  // namespace csa

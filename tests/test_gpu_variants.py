@@ -1,0 +1,54 @@
+"""The same parity check under the other kernel selections and launch modes.
+
+CSA_INDEXER=mma selects the warp-MMA indexer (the measured baseline of the
+tcgen05 one); CSA_PDL=0 launches without programmatic dependent launch.  Both
+are read once per process, so each variant runs in a child process.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import sys, numpy as np, torch
+sys.path.insert(0, ROOT); sys.path.insert(0, ROOT + "/tests")
+import oracle
+from compressed_sparse_attention_indexer_gb300 import csa
+from compressed_sparse_attention_indexer_gb300.workloads import BF16_CFG, Workload, make_batch, to_device
+from helpers import TOL_BF16, assert_close, assert_topk_sets
+cfg = BF16_CFG
+for lens, host in (([8192, 2049, 300, 5000, 3], True), ([4100, 7, 2052], False)):
+    wl = Workload("v", cfg, B=len(lens), S=1, L=1, seed=321)
+    hb = make_batch(wl, lens=lens, gap_rows=2)
+    db = to_device(hb, "cuda:0")
+    B = hb["B"]
+    dec = csa.Decoder(cfg, B, 1, 8192)
+    out = torch.empty(B, 1, 64, 512, dtype=torch.bfloat16, device="cuda:0")
+    idx = torch.empty(B, 1, 512, dtype=torch.int32, device="cuda:0")
+    cnt = torch.empty(B, 1, dtype=torch.int32, device="cuda:0")
+    lh = hb["ctx_len"].clone() if host else None
+    for _ in range(2):
+        dec.decode_step(csa.make_batch_struct(db, lh), out, None, idx, cnt)
+    assert dec.status() == csa.CSA_OK, csa.last_error()
+    ref = oracle.decode(cfg, hb)
+    assert_topk_sets(idx.cpu().numpy().reshape(B, -1), cnt.cpu().numpy().reshape(-1), ref,
+                     lambda q: oracle.query_scores(cfg, hb, q, 0), 512, "variant")
+    assert_close(out.float().cpu().numpy().reshape(B, 64, 512), ref["out"], TOL_BF16, "variant")
+print("variant ok")
+'''
+
+
+@pytest.mark.parametrize("env", [{"CSA_INDEXER": "mma"}, {"CSA_PDL": "0"},
+                                 {"CSA_INDEXER": "mma", "CSA_PDL": "0"}])
+def test_variant_parity(env):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    code = "ROOT = %r\n" % ROOT + CHILD
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "variant ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
