@@ -36,8 +36,8 @@ L2_BYTES = 126 * 1024 * 1024
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="long_ragged_b64")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--copies", type=int, default=3, help="device copies of the inputs, rotated per step")
@@ -51,6 +51,26 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Weak scaling: every rank decodes its own batch, drawn from its own seed."""
+    return base_seed + 7919 * rank
+
+
+def reduce_max(value: float, dist, device) -> float:
+    """Max over ranks (the slowest rank defines the step time); identity at N=1."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(queries_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job queries/s: every rank's queries over the slowest rank's step time."""
+    return queries_per_rank * world / (ms_per_step * 1e-3)
 
 
 def measured_peaks():
@@ -264,7 +284,7 @@ def run_ours(args):
     wl = WORKLOADS[args.workload]
     cfg = wl.cfg
     # weak scaling: every rank decodes its own batch (different seed per rank)
-    hb = make_batch(wl, seed=wl.seed + 7919 * rank)
+    hb = make_batch(wl, seed=rank_seed(wl.seed, rank))
     B, S = hb["B"], hb["S"]
     T = B * S
     lens = [int(x) for x in hb["ctx_len"]]
@@ -304,11 +324,8 @@ def run_ours(args):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, dist if ws > 1 else None, dev)
     if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
         dist.barrier()
 
     # ---- per-kernel times (events around each launch, same stream), separate pass
@@ -360,12 +377,8 @@ def run_ours(args):
             out_host.copy_(out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / args.steps
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": T * ws / (ems * 1e-3), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
+        ems = reduce_max(e0.elapsed_time(e1) / args.steps, dist if ws > 1 else None, dev)
+        e2e = {"value": job_throughput(T, ws, ems), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "ms_per_step": ems,
                "note": "per-step activations (q, q_idx, w, lengths, pool offsets) copied H2D from "
                        "pinned memory and the output D2H each step; KV/indexer caches stay resident"}
@@ -379,7 +392,7 @@ def run_ours(args):
         cpu = cpu_baseline(wl, hb)
     foot = sum(v.numel() * v.element_size() for v in copies[0].values() if isinstance(v, torch.Tensor))
     line = {
-        "metric": "csa_decode_queries_per_s", "value": T * ws / (ms * 1e-3), "unit": "queries/s",
+        "metric": "csa_decode_queries_per_s", "value": job_throughput(T, ws, ms), "unit": "queries/s",
         "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
         "data": "synthetic (seeded normal / uniform draws, shapes of the workload)",

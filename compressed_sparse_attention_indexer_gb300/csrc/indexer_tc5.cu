@@ -16,7 +16,9 @@
 //           of two TMEM accumulators, then commits to mbarriers;
 //   warps 0-3 epilogue: thread t owns TMEM lane t = key row t of the item;
 //           it reads that row's 64 head dot products of a query and sums
-//           w_h * ReLU(.) over h = 0..63 in order, then writes the score.
+//           w_h * ReLU(.) as four 16-head partials (h ascending within each),
+//           added in ascending order, then writes the score.  w of the
+//           request is cached in shared memory.
 // HBM reads per item are the 32 KB of keys (q_idx comes from L2), so the
 // kernel runs at the HBM roofline when enough stages are in flight.
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -86,6 +88,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
   const int S = b.S;
   const uint32_t qbytes = (uint32_t)S * 2u * kQSubBytes;       // one request's q_idx
   const uint32_t qbuf = kbuf + (uint32_t)NST * kStageBytes;    // NQB x qbytes
+  float* w_sm = reinterpret_cast<float*>(smem_raw + (qbuf + (uint32_t)NQB * qbytes - smem_u32(smem_raw)));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_wait();
@@ -219,6 +222,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
       if (cur.advance(it) || it == lo) {
         L = b.ctx_len[cur.bi];
         off = b.idx_off[cur.bi];
+        // the request's w (S x 64) into shared memory, shared by its items
+        named_barrier_sync(1, 128);
+        for (int v = row; v < S * kTcHi; v += 128) w_sm[v] = __ldg(b.w + (int64_t)cur.bi * S * kTcHi + v);
+        named_barrier_sync(1, 128);
       }
       const int bi = cur.bi;
       const int c0 = (it - cur.first) * kIdxChunk;
@@ -238,15 +245,27 @@ __global__ void __launch_bounds__(kT5Threads, 1)
           const QueryPlan p = query_plan(c, S, L, g * G + sl, score_all);
           if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
           const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + tb * kAccCols + sl * kTcHi;
-          const float* wq = b.w + (int64_t)qid * kTcHi;
-          float v[32];
-          float sum = 0.f;
-          tc5::tmem_ld32(ta, v);
+          float v[64];
+          tc5::tmem_ld32x2(ta, v, v + 32);
+          // four disjoint 16-head partials, each summed in ascending h, then
+          // added in ascending order
+          const float4* w4 = reinterpret_cast<const float4*>(w_sm + (g * G + sl) * kTcHi);
+          float part[4];
 #pragma unroll
-          for (int h = 0; h < 32; ++h) sum = fmaf(__ldg(wq + h), fmaxf(v[h], 0.f), sum);
-          tc5::tmem_ld32(ta + 32, v);
+          for (int k = 0; k < 4; ++k) {
+            float acc = 0.f;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) sum = fmaf(__ldg(wq + 32 + h), fmaxf(v[h], 0.f), sum);
+            for (int i = 0; i < 4; ++i) {
+              const float4 wv = w4[k * 4 + i];
+              const int h = k * 16 + i * 4;
+              acc = fmaf(wv.x, fmaxf(v[h], 0.f), acc);
+              acc = fmaf(wv.y, fmaxf(v[h + 1], 0.f), acc);
+              acc = fmaf(wv.z, fmaxf(v[h + 2], 0.f), acc);
+              acc = fmaf(wv.w, fmaxf(v[h + 3], 0.f), acc);
+            }
+            part[k] = acc;
+          }
+          const float sum = ((part[0] + part[1]) + part[2]) + part[3];
           const int j = c0 + row;
           if (j < p.vis) {
             if (!in_pool) set_status(ws.status, kStatusBadIndex);
@@ -310,7 +329,7 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   const int S = b.S;
   const int qbytes = S * 2 * kQSubBytes;
   int NQB = 2, NST = 0;
-  const int budget = 227 * 1024 - 1024 - (int)sizeof(T5Smem) - 64;
+  const int budget = 227 * 1024 - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
   for (NQB = 2; NQB >= 1; --NQB) {
     NST = (budget - NQB * qbytes) / kStageBytes;
     if (NST > 8) NST = 8;
@@ -320,7 +339,7 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   CUtensorMap kmap, qmap;
   if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk)) return -1;
   if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
-  const int smem = 1024 + NST * kStageBytes + NQB * qbytes;
+  const int smem = 1024 + NST * kStageBytes + NQB * qbytes + S * kTcHi * 4;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(indexer_tc5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

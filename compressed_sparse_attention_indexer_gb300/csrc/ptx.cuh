@@ -53,6 +53,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Barrier over `count` threads (a multiple of 32) of the block, id 1..15.
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of
 // 32, <= 1024).  `warp_tmp` holds >= 33 ints of shared memory.  Returns the
 // exclusive prefix; *total receives the block sum.  Contains __syncthreads.

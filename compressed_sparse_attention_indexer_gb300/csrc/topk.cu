@@ -80,10 +80,22 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   // which the keys differ
   const uint32_t k0 = score_key(sc[0]);
   uint32_t acc_or = 0u;
-  for (int i = tid; i < n; i += kTopkThreads) {
-    const uint32_t k = score_key(sc[i]);
-    keys[kpad(i)] = k;
-    acc_or |= k ^ k0;
+  for (int base = 0; base < n; base += 8 * kTopkThreads) {
+    float v[8];  // eight loads in flight per thread
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + j * kTopkThreads + tid;
+      v[j] = i < n ? __ldg(sc + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = base + j * kTopkThreads + tid;
+      if (i < n) {
+        const uint32_t k = score_key(v[j]);
+        keys[kpad(i)] = k;
+        acc_or |= k ^ k0;
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc_or |= __shfl_xor_sync(0xffffffffu, acc_or, o);
