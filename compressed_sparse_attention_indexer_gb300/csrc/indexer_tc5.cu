@@ -10,10 +10,12 @@
 //           128x64 bf16 boxes, 128-byte swizzled, into a ring of stages;
 //           the request's q_idx (S queries x 64 heads x 128) when the
 //           request changes;
-//   warp 5  allocates 512 TMEM columns; one thread issues the MMAs:
+//   warp 5  allocates TMEM; one thread issues the MMAs:
 //           D[128 rows x 64*G heads] = K_tile[128 x 128] . Q^T, M = 128,
 //           N = 64*G (G <= 4 queries per MMA), eight K = 16 steps, into one
-//           of two TMEM accumulators, then commits to mbarriers;
+//           of NB TMEM accumulators (8 of 64 columns when S = 1, so the MMAs
+//           run up to 8 items ahead of the epilogue), then commits to
+//           mbarriers;
 //   warps 0-3 epilogue: thread t owns TMEM lane t = key row t of the item;
 //           it reads that row's 64 head dot products of a query and sums
 //           w_h * ReLU(.) as four 16-head partials (h ascending within each),
@@ -24,6 +26,7 @@
 // Every mbarrier wait is bounded; a wait that gives up records
 // CSA_ERR_TIMEOUT in the status word and the whole block winds down.
 #include <cudaTypedefs.h>
+#include <stdlib.h>
 
 #include "csa_internal.cuh"
 #include "tc5.cuh"
@@ -36,12 +39,10 @@ constexpr int kT5Threads = 192;
 constexpr int kSubBytes = kIdxChunk * 64 * 2;   // 128 rows x 64 dims bf16 = 16 KB
 constexpr int kStageBytes = 2 * kSubBytes;      // 32 KB: one item of keys
 constexpr int kQSubBytes = kTcHi * 64 * 2;      // 64 heads x 64 dims = 8 KB
-constexpr int kTmemCols = 512;
-constexpr int kAccCols = 256;                   // one accumulator buffer (N <= 256)
 constexpr int kMaxG = 4;                        // queries per MMA group
 
 struct T5Smem {
-  uint64_t full[8], empty[8], qfull[2], qempty[2], tfull[2], tempty[2], done;
+  uint64_t full[8], empty[8], qfull[2], qempty[2], tfull[8], tempty[8], done;
   uint32_t tmem_base;
   int abort;
 };
@@ -80,7 +81,11 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     indexer_tc5_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
-                       int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB) {
+                       int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
+                       int acc_cols, int NB) {
+  // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
+  // MMAs run up to NB jobs ahead of the epilogue
+  const uint32_t tmem_cols = (uint32_t)(NB * acc_cols);
   extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 below
   __shared__ T5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
   volatile int* abort = &sm.abort;
 
   if (warp == 5) {
-    tc5::tmem_alloc(smem_u32(&sm.tmem_base), kTmemCols);
+    tc5::tmem_alloc(smem_u32(&sm.tmem_base), tmem_cols);
     tc5::tmem_relinquish();
   }
   if (tid == 0) {
@@ -115,6 +120,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     for (int i = 0; i < 2; ++i) {
       tc5::mbar_init(smem_u32(&sm.qfull[i]), 1);
       tc5::mbar_init(smem_u32(&sm.qempty[i]), 1);
+    }
+    for (int i = 0; i < NB; ++i) {
       tc5::mbar_init(smem_u32(&sm.tfull[i]), 1);
       tc5::mbar_init(smem_u32(&sm.tempty[i]), 128);
     }
@@ -184,8 +191,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         bool ok = true;
         for (int g = 0; g < ngroups; ++g) {
           const int gn = min(G, S - g * G);
-          const int tb = job & 1;
-          if (job >= 2 && !tc5::mbar_wait(smem_u32(&sm.tempty[tb]), ((job >> 1) - 1) & 1, abort)) {
+          const int tb = job % NB;
+          if (job >= NB && !tc5::mbar_wait(smem_u32(&sm.tempty[tb]), ((job / NB) - 1) & 1, abort)) {
             ok = false;
             break;
           }
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             const uint64_t ad = tc5::sdesc_k_sw128(ka + (k >> 2) * kSubBytes + off);
             const uint64_t bd =
                 tc5::sdesc_k_sw128(qa + (k >> 2) * (S * kQSubBytes) + g * G * kQSubBytes + off);
-            tc5::mma_bf16(tmem + tb * kAccCols, ad, bd, idesc, k > 0 ? 1u : 0u);
+            tc5::mma_bf16(tmem + tb * acc_cols, ad, bd, idesc, k > 0 ? 1u : 0u);
           }
           tc5::mma_commit(smem_u32(&sm.tfull[tb]));
           ++job;
@@ -234,8 +241,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
       bool ok = true;
       for (int g = 0; g < ngroups; ++g) {
         const int gn = min(G, S - g * G);
-        const int tb = job & 1;
-        if (!tc5::mbar_wait(smem_u32(&sm.tfull[tb]), (job >> 1) & 1, abort)) {
+        const int tb = job % NB;
+        if (!tc5::mbar_wait(smem_u32(&sm.tfull[tb]), (job / NB) & 1, abort)) {
           ok = false;
           break;
         }
@@ -244,7 +251,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
           const int qid = bi * S + g * G + sl;
           const QueryPlan p = query_plan(c, S, L, g * G + sl, score_all);
           if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
-          const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + tb * kAccCols + sl * kTcHi;
+          const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + tb * acc_cols + sl * kTcHi;
           float v[64];
           tc5::tmem_ld32x2(ta, v, v + 32);
           // four disjoint 16-head partials, each summed in ascending h, then
@@ -284,7 +291,7 @@ __global__ void __launch_bounds__(kT5Threads, 1)
   tc5::fence_before_sync();
   __syncthreads();
   tc5::fence_after_sync();
-  if (warp == 5) tc5::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 5) tc5::tmem_dealloc(tmem, tmem_cols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -328,12 +335,34 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   if (b.idx_rows <= 0 || b.idx_rows > 0x7fffffffLL) return -2;
   const int S = b.S;
   const int qbytes = S * 2 * kQSubBytes;
+  // CTAs per SM: two independent pipelines per SM stream measurably faster
+  // than one deeper ring (the ring depth beyond three stages does not
+  // matter), so two whenever a request's q_idx leaves room for two stages
+  // each.  Tuning knobs, read once: CSA_T5_STAGES caps the ring depth,
+  // CSA_T5_CTAS forces the CTAs per SM (1..4).
+  static int max_stages = -1, forced_ctas = 0;
+  if (max_stages < 0) {
+    const char* e = getenv("CSA_T5_STAGES");
+    max_stages = e ? atoi(e) : 8;
+    if (max_stages < 2 || max_stages > 8) max_stages = 8;
+    const char* f = getenv("CSA_T5_CTAS");
+    forced_ctas = f ? atoi(f) : 0;
+    if (forced_ctas < 0 || forced_ctas > 4) forced_ctas = 0;
+  }
+  const int ctas_per_sm = forced_ctas ? forced_ctas : (S <= 2 ? 2 : 1);
+  const int G = S < 4 ? S : 4;
+  int acc_cols = 32;
+  while (acc_cols < 64 * G) acc_cols <<= 1;  // power of two >= 32
+  int NB = 512 / ctas_per_sm / acc_cols;     // accumulators that fit in TMEM
+  if (NB > 8) NB = 8;
+  if (NB < 2) return -2;
+  const int per_cta = 228 * 1024 / ctas_per_sm - 1024;  // per-SM shared memory / CTAs
   int NQB = 2, NST = 0;
-  const int budget = 227 * 1024 - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
+  const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
   for (NQB = 2; NQB >= 1; --NQB) {
     NST = (budget - NQB * qbytes) / kStageBytes;
-    if (NST > 8) NST = 8;
-    if (NST >= 3) break;
+    if (NST > max_stages) NST = max_stages;
+    if (NST >= 3 || (ctas_per_sm >= 2 && NST >= 2)) break;
   }
   if (NQB < 1 || NST < 2) return -2;
   CUtensorMap kmap, qmap;
@@ -346,10 +375,10 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                          227 * 1024 - (int)sizeof(T5Smem));
     attr = true;
   }
-  int grid = num_sms;
+  int grid = num_sms * ctas_per_sm;
   if (known > 0 && known < grid) grid = known;
   return launch_kernel(indexer_tc5_kernel, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap, qmap,
-                       items, c, b, ws, score_all, scores, ld, NST, NQB);
+                       items, c, b, ws, score_all, scores, ld, NST, NQB, acc_cols, NB);
 }
 
 }  // namespace csa
