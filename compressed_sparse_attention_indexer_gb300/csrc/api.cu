@@ -27,6 +27,8 @@ struct csa_handle {
   std::vector<Mark> marks;
   std::vector<cudaEvent_t> spare;
   csa::ItemList items;  // host-built indexer work list of the current call
+  csa::ItemList jobs;   // host-built attention job list of the current call
+  int max_jobs = 0;     // attention tiles per query, at most
 };
 
 namespace {
@@ -201,6 +203,20 @@ bool use_pdl() {
   return v == 1;
 }
 
+// attention: the tcgen05 tile kernel + merge for the tensor-core shape
+// (unless CSA_ATTN=mma or the batch does not fit it), else the warp-MMA or
+// SIMT kernel
+int run_attention(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, const int* idx,
+                  const int* cnt, void* out, float* lse, cudaStream_t st, bool pdl) {
+  if (csa::tensor_core_shape(h->dc) && csa::attention_impl() == csa::kAttnTc5) {
+    csa::host_jobs(h->dc, b->B, b->S, b->ctx_len_host, &h->jobs);
+    const int r = csa::launch_attention_tc5(h->dc, db, h->ws, h->jobs, idx, cnt, out, lse,
+                                            h->num_sms, st, pdl);
+    if (r != -2) return r;
+  }
+  return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse, h->num_sms, st, pdl);
+}
+
 struct Launches {
   int n = 0;
   bool ok = true;
@@ -256,6 +272,9 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   d.rope_base = cfg->rope_base;
   d.max_context = cfg->max_context;
   d.max_vis = cfg->max_context / cfg->ratio;
+  for (int i = 0; i < csa::kRopeTable; ++i)
+    d.rope_theta[i] = (d.R > 0 && i < d.R / 2)
+                          ? pow((double)cfg->rope_base, -2.0 * (double)i / (double)d.R) : 0.0;
 
   cudaError_t e = cudaGetDevice(&h->device);
   if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaGetDevice"); }
@@ -271,6 +290,11 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   const size_t o_scores = off; off += al(sizeof(float) * ld * maxT);
   const size_t o_idx = off; off += al(sizeof(int) * (size_t)cfg->topk * maxT);
   const size_t o_cnt = off; off += al(sizeof(int) * maxT);
+  const bool tc = csa::tensor_core_shape(d);
+  h->max_jobs = tc ? csa::max_jobs_per_query(d) : 0;
+  const size_t o_jobs = off; off += al(sizeof(int) * (maxT + 1));
+  const size_t o_part = off; off += tc ? al(sizeof(__half) * (size_t)maxT * h->max_jobs * d.H * d.V) : 0;
+  const size_t o_plse = off; off += tc ? al(sizeof(float) * (size_t)maxT * h->max_jobs * d.H) : 0;
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws_base, off);
   if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaMalloc(workspace)"); }
@@ -283,6 +307,9 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   w.scores = reinterpret_cast<float*>(base + o_scores);
   w.topk_idx = reinterpret_cast<int*>(base + o_idx);
   w.topk_cnt = reinterpret_cast<int*>(base + o_cnt);
+  w.job_prefix = reinterpret_cast<int*>(base + o_jobs);
+  w.part_o = tc ? reinterpret_cast<__half*>(base + o_part) : nullptr;
+  w.part_lse = tc ? reinterpret_cast<float*>(base + o_plse) : nullptr;
   w.max_T = maxT;
   w.max_batch = cfg->max_batch;
   w.scores_ld = ld;
@@ -330,8 +357,7 @@ int csa_sparse_attn(csa_handle* h, const csa_batch* b, const int32_t* topk_idx,
   const bool pdl = use_pdl();
   Launches L;
   L.add(staged(h, kStageAttention, st, [&] {
-    return csa::launch_attention(h->dc, db, h->ws, topk_idx, topk_cnt, out, lse_out, h->num_sms,
-                                 st, pdl);
+    return run_attention(h, b, db, topk_idx, topk_cnt, out, lse_out, st, pdl);
   }));
   return finish(h, L);
 }
@@ -355,7 +381,7 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
                             cnt, h->ws.status, h->dc.max_vis, st, pdl);
   }));
   L.add(staged(h, kStageAttention, st, [&] {
-    return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse_out, h->num_sms, st, pdl);
+    return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl);
   }));
   return finish(h, L);
 }

@@ -27,6 +27,8 @@
 //
 // SIMT path: any shape / dtype, one warp per head, fp32 arithmetic.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "csa_internal.cuh"
 #include "ptx.cuh"
@@ -137,12 +139,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             nt2 = (ns[2] + kTR - 1) / kTR;
   const int Tt = nt0 + nt1 + nt2;
 
-  if (tid < 32) {
-    const double ang = (double)p.pos * pow((double)c.rope_base, -2.0 * (double)tid / (double)c.R);
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    sh.rope[tid] = make_float2((float)cs, (float)sn);
-  }
+  if (tid < 32) sh.rope[tid] = rope_cos_sin((double)p.pos, c.rope_theta[tid]);
 
   auto tile_stream = [&](int t, int& sid, int& lt) {
     if (t < nt0) { sid = 0; lt = t; }
@@ -487,6 +484,18 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(DevCfg c, DevBatch b, Wo
 }
 
 }  // namespace
+
+// Attention kernel for the tensor-core shape: the warp-MMA kernel by
+// default (measured faster so far); CSA_ATTN=tc5 selects the tcgen05 tile
+// kernel + merge.
+int attention_impl() {
+  static int impl = -1;
+  if (impl < 0) {
+    const char* e = getenv("CSA_ATTN");
+    impl = (e && strcmp(e, "tc5") == 0) ? kAttnTc5 : kAttnMma;
+  }
+  return impl;
+}
 
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,

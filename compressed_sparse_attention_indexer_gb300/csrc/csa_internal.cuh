@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,11 +22,29 @@ constexpr int kStatusTimeout = 2;
 constexpr int kPlanScore = 1;  // the indexer scores this query (vis > K, or forced)
 constexpr int kPlanBad = 2;    // invalid length: output zeros, nothing read
 
+constexpr int kRopeTable = 32;  // rotary frequencies kept in the config (R <= 64)
+
 struct DevCfg {
   int H, D, V, R, Hi, Di, ratio, K, win, hca_ratio, dtype;
   float scale, rope_base;
   int max_context, max_vis;
+  double rope_theta[kRopeTable];  // base^(-2i/R), i < min(R/2, kRopeTable), set on the host
 };
+
+// cos and sin of pos * theta for inverse RoPE.  The angle (up to ~6.6e4 rad)
+// is formed in fp64 and reduced to [-pi, pi] by Cody-Waite reduction with
+// 2*pi split into two fp64 parts (each step one fused multiply-add, so the
+// reduction is exact to fp64 rounding), then sincosf of the reduced fp32
+// argument.
+__device__ __forceinline__ float2 rope_cos_sin(double pos, double theta) {
+  const double a = pos * theta;
+  const double k = rint(a * 0.15915494309189535);   // a / (2 pi)
+  double r = fma(-k, 6.283185307179586, a);          // 2 pi, leading part
+  r = fma(-k, 2.4492935982947064e-16, r);            // 2 pi, trailing part
+  float sn, cs;
+  sincosf((float)r, &sn, &cs);
+  return make_float2(cs, sn);
+}
 
 struct DevBatch {
   int B, S;
@@ -101,6 +120,9 @@ struct Workspace {
   float* scores;      // [max_T, max_vis]
   int* topk_idx;      // [max_T, K]
   int* topk_cnt;      // [max_T]
+  int* job_prefix;    // [max_T + 1] attention tiles per query, prefix (device-built)
+  __half* part_o;     // [max_T * max_jobs, H, V] per-tile normalised attention output
+  float* part_lse;    // [max_T * max_jobs, H] per-tile log-sum-exp (log2 units)
   int max_T, max_batch;
   int64_t scores_ld;
 };
@@ -150,6 +172,13 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
                      cudaStream_t st, bool pdl);
+int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
+                         const ItemList& jobs, const int* topk_idx, const int* topk_cnt, void* out,
+                         float* lse_out, int num_sms, cudaStream_t st, bool pdl);
+void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, ItemList* jobs);
+int max_jobs_per_query(const DevCfg& c);
+constexpr int kAttnMma = 0, kAttnTc5 = 1;
+int attention_impl();
 
 bool tensor_core_shape(const DevCfg& c);
 constexpr int kIndexerMma = 0, kIndexerTc5 = 1;

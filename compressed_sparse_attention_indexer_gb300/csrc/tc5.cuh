@@ -24,10 +24,13 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// Non-blocking test of the phase with the given parity.  (A suspending
+// try_wait was measured to wake late, tens of microseconds, on phases
+// completed by tcgen05.commit; polling test_wait does not.)
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
@@ -36,10 +39,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after a
-// bounded number of polls (each poll suspends in hardware for a while) or
-// when *abort is set by another thread; returns false then, after setting
-// *abort so that every other waiter of the block gives up too.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// bounded number of polls (about a second) or when *abort is set by another
+// thread; returns false then, after setting *abort so that every other waiter
+// of the block gives up too.
+constexpr uint32_t kWaitPolls = 1u << 26;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
