@@ -485,14 +485,14 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(DevCfg c, DevBatch b, Wo
 
 }  // namespace
 
-// Attention kernel for the tensor-core shape: the warp-MMA kernel by
-// default (measured faster so far); CSA_ATTN=tc5 selects the tcgen05 tile
-// kernel + merge.
+// Attention kernel for the tensor-core shape: the tcgen05 tile kernel +
+// merge by default (measured faster); CSA_ATTN=mma selects the warp-MMA
+// kernel.
 int attention_impl() {
   static int impl = -1;
   if (impl < 0) {
     const char* e = getenv("CSA_ATTN");
-    impl = (e && strcmp(e, "tc5") == 0) ? kAttnTc5 : kAttnMma;
+    impl = (e && strcmp(e, "mma") == 0) ? kAttnMma : kAttnTc5;
   }
   return impl;
 }

@@ -10,30 +10,34 @@
 //    and compressed softmax results are merged, then inverse RoPE is applied.
 //
 // attn_tile_kernel: persistent, one CTA per SM, warp-specialised.  A job is
-// one 128-row tile of one stream (window, compressed, heavy) of one query.
-//   warps 5-8 gather the tile's rows with coalesced 16-byte cp.async into
-//            128-byte-swizzled sub-tiles (value dims as four 32 KB pairs of
-//            64-dim sub-tiles, rope dims as one 16 KB sub-tile), each thread
-//            fencing its copies for the async proxy before it arrives on the
-//            stage barrier; the query's 64 heads x 576 (72 KB) are loaded by
-//            TMA when the query changes and stay resident;
-//   warp 4   issues tcgen05 MMAs: S^T[128 rows x 64 heads] = R . Q^T over
-//            576 dims (36 MMAs, M = 128, N = 64, K = 16) into TMEM; after the
-//            softmax, O^T[512 dims x 64 heads] = V^T . P^T (four 128-dim
-//            chunks x eight K = 16 steps, V read in place as an MN-major
-//            operand, P^T from the rope slot that QK no longer needs) into
-//            TMEM;
-//   warps 0-3 thread r owns TMEM lane r = row r: it reads the row's 64 head
-//            scores, masks rows that do not exist, and the block takes the
-//            exact per-head max and sum over the tile (shuffle transposes,
-//            fixed order); P^T goes to shared memory as bf16.  After PV each
-//            thread reads its 128-dim slice of O^T and writes the tile's
-//            normalised output (fp16) and its lse per head to the workspace.
-// attn_merge_kernel: per query and head, the log-sum-exp merge of its tiles
-// in fixed order (window, compressed, heavy; tiles ascending), then inverse
-// RoPE on the last R dims and the bf16 store.  Because the LSE merge is
-// exact, the per-tile softmax + merge equals one softmax per stream merged
-// across streams.
+// one 64-row tile of one stream (window, compressed, heavy) of one query; a
+// CTA takes a contiguous range of the job list, and the jobs of one query
+// inside that range form a segment whose output accumulates in TMEM.
+//   warps 5-10, two groups of three: group g gathers every other job into
+//            job buffer g with coalesced 16-byte cp.async, rows scattered
+//            over the pools, into nine 128-byte-swizzled 64-dim sub-tiles
+//            (72 KB); each thread fences its copies for the async proxy and
+//            arrives on the buffer's barrier.  Two buffers: one job's rows
+//            land while the previous job is computed;
+//   warp 4   loads the query's 64 heads x 576 (72 KB, TMA) when the query
+//            changes and issues the tcgen05 MMAs as their inputs become
+//            ready: S[64 heads x 64 rows] = Q . R^T over 576 dims (M = 64,
+//            N = 64) into one of two TMEM score buffers; after the softmax,
+//            O^T[512 dims x 64 heads] += V^T . P^T (M = 128 per 128-dim
+//            chunk, N = 64; V read in place as an MN-major operand, P^T
+//            from the rope sub-tile that QK no longer needs) into TMEM;
+//   warps 0-3 softmax, one thread per head (lanes 0-15: the M = 64 layout
+//            puts head 16w + i in lane 32w + i): scale and mask the job's 64
+//            scores, keep a per-head reference max that moves only when a
+//            tile max exceeds it by 2^8 (then O^T is rescaled in TMEM by all
+//            128 threads), write the head's row of P^T as bf16 and sum the
+//            rounded weights.  At a segment's end all four warps read O^T
+//            (thread = dim) and write the normalised partial output (fp16,
+//            heads x dims) and the heads' log-sum-exp to the workspace.
+// attn_merge_kernel: per query and 64 output dims, the log-sum-exp merge of
+// the query's segments in job order, inverse RoPE on the last R dims, the
+// bf16 store.  Because the merge is exact, segment softmax + merge equals
+// one softmax over the union of the streams' rows.
 #include <cudaTypedefs.h>
 #include <stddef.h>
 #include <stdlib.h>
@@ -45,31 +49,35 @@ namespace csa {
 
 namespace {
 
-constexpr int kA5Threads = 288;  // warps 0-3 softmax, 4 MMA, 5-8 row loaders
-constexpr int kTile = 128;
-constexpr int kSubBytes = kTile * 128;   // 128 rows x 64 dims bf16: 16 KB
-constexpr int kPairBytes = 2 * kSubBytes;
-constexpr int kQSub = kTcH * 128;        // 64 heads x 64 dims: 8 KB
-constexpr int kNPair = 4;               // one job's value dims, 4 x 32 KB
-constexpr int kQBytes = 9 * kQSub;      // the query's heads, resident: 72 KB
-// the rope sub-tile slot holds P^T (64 heads x 128 rows bf16) once QK is done
-constexpr int kA5Dyn = 1024 + kNPair * kPairBytes + kSubBytes + kQBytes;
+constexpr int kLoadWarps = 3;    // per loader group
+constexpr int kA5Threads = 32 * (5 + 2 * kLoadWarps);  // warps 0-3 softmax, 4 MMA + Q, 5-10 loaders
+constexpr int kTile = 64;                  // rows per job
+constexpr int kQuadsPerWarp = (kTile / 4 + kLoadWarps - 1) / kLoadWarps;
+constexpr int kSub = kTile * 128;          // 64 rows x 64 dims bf16: 8 KB
+constexpr int kBuf = 9 * kSub;             // a job's rows: 72 KB (rope sub-tile -> P^T)
+constexpr int kQSub = kTcH * 128;          // 64 heads x 64 dims: 8 KB
+constexpr int kQBytes = 9 * kQSub;         // the query's heads, resident: 72 KB
+constexpr int kA5Dyn = 1024 + kQBytes + 2 * kBuf;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMergeHeads = 4;     // heads per merge block
-constexpr int kMergeMaxJobs = 64;  // tiles per query the merge handles (else the warp-MMA path)
+constexpr float kRescale = 8.f;            // lazy rescale threshold (log2 units)
+constexpr int kMergeDims = 64;             // output dims per merge block
+constexpr int kMergeMaxJobs = 64;          // jobs per query the merge handles (else the warp-MMA path)
+// TMEM columns: two score buffers (M = 64 layout: head h in lane
+// 32(h / 16) + h % 16, row j in column j), four 128-dim chunks of O^T
+constexpr uint32_t kTmemS = 0, kTmemO = 256;
 
 struct __align__(16) A5Smem {
-  uint64_t pfull[kNPair], pempty[kNPair], rfull, rempty, qfull, qempty, mfull[2], mempty[2];
-  uint64_t s_full, s_empty, p_full, o_full, o_empty, done;
+  uint64_t full[2], empty[2], mfull[2], mempty[2], s_full[2], s_empty[2];
+  uint64_t p_full, pv_done, o_full, o_empty, qfull, qdone, done;
   uint32_t tmem_base;
   int abort;
-  uint32_t mask[2][4];  // per job: bit l of word w = row 32w + l exists
-  alignas(16) float red[4][kTcH];
-  alignas(16) float mtile[kTcH];  // read as float4
-  alignas(16) float ltile[kTcH];  // read as float4
+  int flag[2][4];                  // per job parity and warp: some head needs a rescale
+  uint64_t mask[2][kLoadWarps];    // per buffer and loader warp: bit i = row i exists
+  alignas(16) float alpha[2][kTcH];  // per job parity: per-head rescale factor
+  alignas(16) float linv[2][kTcH];   // per segment parity: per-head 1 / (sum of the weights)
 };
-static_assert(offsetof(A5Smem, mtile) % 16 == 0 && offsetof(A5Smem, ltile) % 16 == 0,
-              "per-head tile statistics are read with 16-byte loads");
+static_assert(offsetof(A5Smem, alpha) % 16 == 0 && offsetof(A5Smem, linv) % 16 == 0,
+              "per-head statistics are read with 16-byte loads");
 
 // descriptor of an MN-major operand in the 128-byte swizzle layout: 64
 // contiguous MN elements per 128-byte row, 8-row K groups 1024 bytes apart
@@ -84,13 +92,14 @@ __device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t lbo)
   return d;
 }
 
-__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1,
-                                        int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+// 2^x with the hardware approximation (relative error ~2^-22; -inf -> 0),
+// ample for weights that are rounded to bf16 next.  The argument is never
+// NaN here: a masked score is -inf and the reference is finite whenever a
+// row exists.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -99,10 +108,6 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 // Job list: jobs of query q are [prefix[q], prefix[q+1]); in each query the
 // window tiles, then the compressed tiles, then the heavy tiles.
-struct JobOf {
-  int q, sid, t;
-};
-
 struct JobCursor {
   const int* prefix;
   int q, first, end;
@@ -191,38 +196,16 @@ __device__ __forceinline__ int job_row(const DevCfg& c, const DevBatch& b, const
   return (int)gr;
 }
 
-// Max (op 0) or sum (op 1) of each of 64 per-row values over the 32 lanes of
-// a warp, by a butterfly that halves the values each step; lane l ends with
-// the results for heads 2l and 2l+1 in v[0], v[1].  Fixed order.
-template <int OP>
-__device__ __forceinline__ void warp_transpose_reduce(float* v, int lane) {
-#pragma unroll
-  for (int w = 32, o = 16; o >= 1; w >>= 1, o >>= 1) {
-    const bool up = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = up ? v[i] : v[i + w];
-      const float keep = up ? v[i + w] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
-      v[i] = OP == 0 ? fmaxf(keep, recv) : (up ? recv + keep : keep + recv);
-    }
-  }
-}
-
 __global__ void __launch_bounds__(kA5Threads, 1)
-    attn_tile_kernel(const __grid_constant__ CUtensorMap rawmap,
-                     const __grid_constant__ CUtensorMap cmpmap,
-                     const __grid_constant__ CUtensorMap hcamap,
-                     const __grid_constant__ CUtensorMap qmap,
+    attn_tile_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
                      const int* __restrict__ topk_idx, const int* __restrict__ topk_cnt) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ A5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t pairs = base;                            // 4 x 32 KB: value dims
-  const uint32_t rp = pairs + kNPair * kPairBytes;       // 16 KB: rope dims, then P^T
-  const uint32_t qres = rp + kSubBytes;                  // 72 KB: the query's 64 heads
-  uint8_t* rp_gen = smem_raw + (rp - smem_u32(smem_raw));
+  const uint32_t qres = base;                 // 72 KB: the query's 64 heads
+  const uint32_t bufs = qres + kQBytes;       // 2 x 72 KB: the jobs' rows
+  uint8_t* gen = smem_raw + (bufs - smem_u32(smem_raw));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = b.B * b.S;
@@ -240,23 +223,20 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     tc5::tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < kNPair; ++i) {
-      tc5::mbar_init(smem_u32(&sm.pfull[i]), 128);  // every loader thread arrives
-      tc5::mbar_init(smem_u32(&sm.pempty[i]), 1);
+    for (int g = 0; g < 2; ++g) {
+      tc5::mbar_init(smem_u32(&sm.full[g]), 32 * kLoadWarps);  // every thread of the group
+      tc5::mbar_init(smem_u32(&sm.empty[g]), 1);
+      tc5::mbar_init(smem_u32(&sm.mfull[g]), kLoadWarps);  // one arrival per loader warp
+      tc5::mbar_init(smem_u32(&sm.mempty[g]), 128);  // the softmax threads
+      tc5::mbar_init(smem_u32(&sm.s_full[g]), 1);
+      tc5::mbar_init(smem_u32(&sm.s_empty[g]), 128);
     }
-    tc5::mbar_init(smem_u32(&sm.rfull), 128);
-    tc5::mbar_init(smem_u32(&sm.rempty), 1);
-    tc5::mbar_init(smem_u32(&sm.qfull), 1);
-    tc5::mbar_init(smem_u32(&sm.qempty), 1);
-    for (int i = 0; i < 2; ++i) {
-      tc5::mbar_init(smem_u32(&sm.mfull[i]), 4);  // one arrival per loader warp
-      tc5::mbar_init(smem_u32(&sm.mempty[i]), 128);
-    }
-    tc5::mbar_init(smem_u32(&sm.s_full), 1);
-    tc5::mbar_init(smem_u32(&sm.s_empty), 128);
     tc5::mbar_init(smem_u32(&sm.p_full), 128);
+    tc5::mbar_init(smem_u32(&sm.pv_done), 1);
     tc5::mbar_init(smem_u32(&sm.o_full), 1);
     tc5::mbar_init(smem_u32(&sm.o_empty), 128);
+    tc5::mbar_init(smem_u32(&sm.qfull), 1);
+    tc5::mbar_init(smem_u32(&sm.qdone), 1);
     tc5::mbar_init(smem_u32(&sm.done), 1);
     sm.abort = 0;
     tc5::fence_mbar_init();
@@ -265,266 +245,331 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   __syncthreads();
   tc5::fence_after_sync();
   const uint32_t tmem = sm.tmem_base;
-  const uint32_t tmem_s = tmem;          // S^T: columns [0, 64)
-  const uint32_t tmem_o = tmem + 256;    // O^T: columns [256, 512), 64 per 128-dim chunk
 
   if (warp >= 5) {
     // ------------------------------------------------------------ row loaders
-    // loader warp lw gathers rows 32lw .. 32lw+31 of each job with 16-byte
-    // cp.async (two rows x 256 bytes per instruction, coalesced) into the
-    // 128-byte-swizzled sub-tiles the MMAs read; each thread waits for its
-    // own copies and makes them visible to the tensor core (proxy fence)
-    // before arriving on the stage's barrier
-    const int lw = warp - 5;
-    if (lw == 0 && lane == 0) tc5::prefetch_tmap(&qmap);
+    // group g takes jobs lo+g, lo+g+2, ...; an instruction moves four rows x
+    // 128 bytes, and warp lw of the group takes row quads lw, lw+3, ...
+    const int g = (warp - 5) / kLoadWarps, lw = (warp - 5) % kLoadWarps;
+    const uint32_t buf = bufs + g * kBuf;
     const __nv_bfloat16* null_src = static_cast<const __nv_bfloat16*>(b.q);
-    int nq = 0, n = 0, cur_q = -1;
+    const int ch = lane & 7;
     JobCursor cur;
     cur.init(prefix, T, lo);
-    bool ok = true;
-    for (int job = lo; job < hi && ok && !*abort; ++job, ++n) {
+    int m = 0;
+    for (int job = lo + g; job < hi && !*abort; job += 2, ++m) {
       cur.advance(job);
       const int q = cur.q;
       const JobCtx x = job_ctx(c, b, q, topk_cnt);
       int sid, t;
       job_stream(x, job - cur.first, sid, t);
-      const int row = 32 * lw + lane;  // this lane's row of the tile
-      const int gr = job_row(c, b, x, q, sid, t * kTile + row, topk_idx, ws.status);
       const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(
           sid == 0 ? b.raw : (sid == 1 ? b.cmp : b.hca));
       const int64_t stride = sid == 0 ? b.raw_stride : (sid == 1 ? b.cmp_stride : b.hca_stride);
-      const __nv_bfloat16* my = gr >= 0 ? pool + (int64_t)gr * stride : nullptr;
-      // the rows that exist, for the softmax
-      const int mb = n & 1;
-      if (lane == 0 && n >= 2 && !tc5::mbar_wait(smem_u32(&sm.mempty[mb]), ((n >> 1) - 1) & 1, abort))
-        ok = false;
+      // this lane's rows and their pool addresses (read before waiting for
+      // the buffer, so that the index loads overlap the wait)
+      const __nv_bfloat16* src[kQuadsPerWarp];
+      uint64_t bits = 0;
+#pragma unroll
+      for (int i = 0; i < kQuadsPerWarp; ++i) {
+        const int rq = lw + kLoadWarps * i;
+        src[i] = nullptr;
+        if (rq < kTile / 4) {
+          const int gr = job_row(c, b, x, q, sid, t * kTile + 4 * rq + (lane >> 3), topk_idx, ws.status);
+          if (gr >= 0) src[i] = pool + (int64_t)gr * stride;
+        }
+        const uint32_t v = __ballot_sync(0xffffffffu, src[i] != nullptr);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if ((v >> (8 * k)) & 1u) bits |= 1ull << (4 * rq + k);
+      }
+      bool ok = true;
+      if (lane == 0) {
+        if (m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.empty[g]), (m - 1) & 1, abort, 256)) ok = false;
+        if (ok && m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.mempty[g]), (m - 1) & 1, abort, 256)) ok = false;
+        if (ok) {
+          sm.mask[g][lw] = bits;
+          tc5::mbar_arrive(smem_u32(&sm.mfull[g]));
+        }
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
-      const uint32_t bits = __ballot_sync(0xffffffffu, gr >= 0);
-      if (lane == 0) {
-        sm.mask[mb][lw] = bits;
-        tc5::mbar_arrive(smem_u32(&sm.mfull[mb]));
-      }
-      // the query's heads (TMA, 9 boxes) when the query changes
-      if (q != cur_q) {
-        if (lw == 0 && lane == 0) {
-          if (nq > 0 && !tc5::mbar_wait(smem_u32(&sm.qempty), (nq - 1) & 1, abort)) ok = false;
-          if (ok) {
-            tc5::mbar_expect_tx(smem_u32(&sm.qfull), kQBytes);
-            for (int k = 0; k < 9; ++k)
-              tc5::tma_load_2d(qres + k * kQSub, &qmap, k * 64, q * kTcH, smem_u32(&sm.qfull));
+#pragma unroll 3
+      for (int sub = 0; sub < 9; ++sub) {
+#pragma unroll
+        for (int i = 0; i < kQuadsPerWarp; ++i) {
+          const int rq = lw + kLoadWarps * i;
+          if (rq < kTile / 4) {
+            const int rt = 4 * rq + (lane >> 3);  // row within the job
+            const uint32_t dst = buf + sub * kSub + rt * 128 + ((ch ^ (rt & 7)) << 4);
+            cp_async16(dst, src[i] ? (const void*)(src[i] + sub * 64 + ch * 8) : (const void*)null_src,
+                       src[i] ? 16 : 0);
           }
         }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        ++nq;
-        cur_q = q;
       }
-      // issue: four pairs of 64-dim sub-tiles, then the rope sub-tile
-      for (int cp = 0; cp < kNPair + 1 && ok; ++cp) {
-        const bool rope = cp == kNPair;
-        const uint32_t wbar = rope ? smem_u32(&sm.rempty) : smem_u32(&sm.pempty[cp]);
-        if (lane == 0 && n >= 1 && !tc5::mbar_wait(wbar, (n - 1) & 1, abort)) ok = false;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-        const uint32_t dst0 = rope ? rp : pairs + cp * kPairBytes;
-        const int nch = rope ? 8 : 16;   // 16-byte chunks per row in this stage
-        const int rows_per = 32 / nch;   // rows per warp instruction
-        for (int j = 0; j < 32; j += rows_per) {
-          const int rl = j + lane / nch;                 // row within the warp's 32
-          const int ch = lane % nch;
-          const __nv_bfloat16* src = reinterpret_cast<const __nv_bfloat16*>(
-              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(my), rl));
-          const int rt = 32 * lw + rl;                   // row within the tile
-          const uint32_t dst = dst0 + (ch >> 3) * kSubBytes + rt * 128 + (((ch & 7) ^ (rt & 7)) << 4);
-          const int col = (rope ? 512 : cp * 128) + ch * 8;
-          cp_async16(dst, src ? (const void*)(src + col) : (const void*)null_src, src ? 16 : 0);
-        }
-        cp_async_commit();
-      }
-      if (!ok) break;
-      // completion, stage by stage: copies landed, visible to the async proxy
-      cp_async_wait<4>();
-      fence_proxy_async();
-      tc5::mbar_arrive(smem_u32(&sm.pfull[0]));
-      cp_async_wait<3>();
-      fence_proxy_async();
-      tc5::mbar_arrive(smem_u32(&sm.pfull[1]));
-      cp_async_wait<2>();
-      fence_proxy_async();
-      tc5::mbar_arrive(smem_u32(&sm.pfull[2]));
-      cp_async_wait<1>();
-      fence_proxy_async();
-      tc5::mbar_arrive(smem_u32(&sm.pfull[3]));
+      cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async();
-      tc5::mbar_arrive(smem_u32(&sm.rfull));
+      tc5::mbar_arrive(smem_u32(&sm.full[g]));
     }
     cp_async_wait<0>();
-    if (lw == 0 && lane == 0 && nq > 0) tc5::mbar_wait_drain(smem_u32(&sm.qfull), (nq - 1) & 1);
   } else if (warp == 4) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ Q loads + MMA issue
+    // Event driven: each poll issues whichever of QK(next) and PV(oldest
+    // pending) is ready, so that a job's PV never waits behind the next
+    // job's rows.  Descriptors advance by (byte offset >> 4) from bases.
     if (lane == 0) {
-      const uint32_t idesc_s = tc5::idesc_bf16_f32(128, kTcH);
-      const uint32_t idesc_o = tc5::idesc_bf16_f32(128, kTcH) | (1u << 15);  // A (V^T) MN-major
-      JobCursor cur;
-      cur.init(prefix, T, lo);
-      int n = 0, nq = 0, cur_q = -1;
-      for (int job = lo; job < hi && !*abort; ++job, ++n) {
-        cur.advance(job);
-        if (cur.q != cur_q) {
-          if (nq > 0) tc5::mma_commit(smem_u32(&sm.qempty));  // previous query's MMAs
-          if (!tc5::mbar_wait(smem_u32(&sm.qfull), nq & 1, abort)) break;
-          ++nq;
-          cur_q = cur.q;
-        }
-        if (n > 0 && !tc5::mbar_wait(smem_u32(&sm.s_empty), (n - 1) & 1, abort)) break;
-        // S^T = R . Q^T over 9 sub-tiles of 64 dims
-        bool ok = true;
-        for (int k = 0; k < 9 && ok; ++k) {
-          uint32_t rsub;
-          if (k < 8) {
-            if ((k & 1) == 0 && !tc5::mbar_wait(smem_u32(&sm.pfull[k >> 1]), n & 1, abort)) ok = false;
-            rsub = pairs + (k >> 1) * kPairBytes + (k & 1) * kSubBytes;
-          } else {
-            if (!tc5::mbar_wait(smem_u32(&sm.rfull), n & 1, abort)) ok = false;
-            rsub = rp;
+      tc5::prefetch_tmap(&qmap);
+      const uint32_t idesc_s = tc5::idesc_bf16_f32(64, 64);                // QK: 64 heads x 64 rows
+      const uint32_t idesc_o = tc5::idesc_bf16_f32(128, kTcH) | (1u << 15);  // PV: A MN-major
+      const uint64_t dq = tc5::sdesc_k_sw128(qres);
+      const uint64_t dbuf = tc5::sdesc_k_sw128(bufs);
+      const uint64_t dv = sdesc_mn_sw128(bufs, kSub);
+      JobCursor qc, pc;  // cursors of the next QK job and the next PV job
+      qc.init(prefix, T, lo);
+      pc.init(prefix, T, lo);
+      const int J = hi - lo;
+      int nk = 0, np = 0;  // CTA-local index of the next job to QK / to PV
+      int nq = 0, nqd = 0, seg = 0, cur_q = -1;
+      int qstate = 0;      // 0 Q of cur_q resident, 1 waiting for qdone, 2 waiting for qfull
+      uint32_t idle = 0;
+      while (np < J) {
+        bool progressed = false;
+        if (np < nk) {
+          const int job = lo + np;
+          pc.advance(job);
+          const bool first = job == lo || job == pc.first;
+          const bool last = job + 1 == hi || job + 1 == pc.end;
+          if ((!first || seg == 0 || tc5::mbar_try_wait(smem_u32(&sm.o_empty), (seg - 1) & 1)) &&
+              tc5::mbar_try_wait(smem_u32(&sm.p_full), np & 1)) {
+            // O^T += V^T . P^T (overwrite at a segment's first job)
+            tc5::fence_after_sync();
+            const uint32_t vo = ((np & 1) * kBuf) >> 4;           // buffer offset, 16-byte units
+            const uint64_t dp = dbuf + vo + ((8 * kSub) >> 4);    // P^T in the rope sub-tile
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tc5::mma_bf16(tmem + kTmemO + 64 * cc, dv + vo + ((2 * cc * kSub + i * 2048) >> 4),
+                              dp + 2 * i, idesc_o, (!first || i > 0) ? 1u : 0u);
+            tc5::mma_commit(smem_u32(&sm.empty[np & 1]));
+            tc5::mma_commit(smem_u32(&sm.pv_done));
+            if (last) {
+              tc5::mma_commit(smem_u32(&sm.o_full));
+              ++seg;
+            }
+            ++np;
+            progressed = true;
           }
-          if (!ok) break;
-          tc5::fence_after_sync();
-          const uint32_t qsub = qres + k * kQSub;
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            tc5::mma_bf16(tmem_s, tc5::sdesc_k_sw128(rsub + 32 * i),
-                          tc5::sdesc_k_sw128(qsub + 32 * i), idesc_s, (k | i) ? 1u : 0u);
         }
-        if (!ok) break;
-        tc5::mma_commit(smem_u32(&sm.s_full));
-        // O^T = V^T . P^T once the softmax has written P^T into the rope slot
-        if (!tc5::mbar_wait(smem_u32(&sm.p_full), n & 1, abort)) break;
-        if (n > 0 && !tc5::mbar_wait(smem_u32(&sm.o_empty), (n - 1) & 1, abort)) break;
-        tc5::fence_after_sync();
-        for (int cc = 0; cc < kNPair; ++cc) {
-          const uint32_t vb = pairs + cc * kPairBytes;
+        if (nk < J) {
+          const int job = lo + nk;
+          qc.advance(job);
+          if (qc.q != cur_q) {
+            // a new query: its heads replace Q once the QK MMAs of the
+            // previous query are done (qdone)
+            if (qstate == 0) qstate = nk == 0 ? 3 : 1;
+            if (qstate == 1 && tc5::mbar_try_wait(smem_u32(&sm.qdone), nqd & 1)) {
+              ++nqd;
+              qstate = 3;
+            }
+            if (qstate == 3) {
+              tc5::mbar_expect_tx(smem_u32(&sm.qfull), kQBytes);
+              for (int k = 0; k < 9; ++k)
+                tc5::tma_load_2d(qres + k * kQSub, &qmap, k * 64, qc.q * kTcH, smem_u32(&sm.qfull));
+              qstate = 2;
+            }
+            if (qstate == 2 && tc5::mbar_try_wait(smem_u32(&sm.qfull), nq & 1)) {
+              ++nq;
+              qstate = 0;
+              cur_q = qc.q;
+            }
+          }
+          const int g = nk & 1, m = nk >> 1;
+          if (qc.q == cur_q && (m == 0 || tc5::mbar_try_wait(smem_u32(&sm.s_empty[g]), (m - 1) & 1)) &&
+              tc5::mbar_try_wait(smem_u32(&sm.full[g]), m & 1)) {
+            // S = Q . R^T over 576 dims (M = 64 heads, N = 64 rows)
+            tc5::fence_after_sync();
+            const uint64_t db = dbuf + ((g * kBuf) >> 4);
+            const uint32_t ds = tmem + kTmemS + 64 * g;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            tc5::mma_bf16(tmem_o + 64 * cc, sdesc_mn_sw128(vb + i * 2048, kSubBytes),
-                          tc5::sdesc_k_sw128(rp + (i >> 2) * (kTcH * 128) + (i & 3) * 32), idesc_o,
-                          i > 0 ? 1u : 0u);
-          tc5::mma_commit(smem_u32(&sm.pempty[cc]));
+            for (int k = 0; k < 9; ++k)
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tc5::mma_bf16(ds, dq + ((k * kQSub + 32 * i) >> 4), db + ((k * kSub + 32 * i) >> 4),
+                              idesc_s, (k | i) ? 1u : 0u);
+            tc5::mma_commit(smem_u32(&sm.s_full[g]));
+            if (job + 1 < hi && job + 1 == qc.end) tc5::mma_commit(smem_u32(&sm.qdone));
+            ++nk;
+            progressed = true;
+          }
         }
-        tc5::mma_commit(smem_u32(&sm.rempty));
-        tc5::mma_commit(smem_u32(&sm.o_full));
+        if (progressed) {
+          idle = 0;
+        } else {
+          if (++idle > (1u << 25)) {
+            *abort = 1;
+            break;
+          }
+          if (idle > 8) __nanosleep(32);
+          if ((idle & 63u) == 0 && *abort) break;
+        }
       }
+      if (qstate == 2) tc5::mbar_wait_drain(smem_u32(&sm.qfull), nq & 1);
       tc5::mma_commit(smem_u32(&sm.done));
       tc5::mbar_wait_drain(smem_u32(&sm.done), 0);
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int r = tid;  // row of the tile = TMEM lane
+    // lanes 0-15 of warp w own head h = 16w + lane (its TMEM lane in the
+    // score buffers): the job's 64 scores, the reference max and the sum of
+    // the weights stay in the thread
+    const bool owner = lane < 16;
+    const int h = 16 * warp + (lane & 15);
+    const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const float sc2 = c.scale * kLog2e;
-    __half* part = ws.part_o;
-    float* part_lse = ws.part_lse;
-    int n = 0;
+    float mref = -INFINITY, lrun = 0.f;
+    JobCursor cur;
+    cur.init(prefix, T, lo);
+    int n = 0, seg = 0, slot = lo;
     for (int job = lo; job < hi && !*abort; ++job, ++n) {
-      const int mb = n & 1;
-      if (!tc5::mbar_wait(smem_u32(&sm.mfull[mb]), (n >> 1) & 1, abort)) break;
-      const bool valid = (sm.mask[mb][r >> 5] >> (r & 31)) & 1u;
-      tc5::mbar_arrive(smem_u32(&sm.mempty[mb]));
-
-      if (!tc5::mbar_wait(smem_u32(&sm.s_full), n & 1, abort)) break;
+      cur.advance(job);
+      const bool first = job == lo || job == cur.first;
+      const bool last = job + 1 == hi || job + 1 == cur.end;
+      if (first) slot = job;
+      const int g = n & 1, m = n >> 1;
+      if (!tc5::mbar_wait_backoff(smem_u32(&sm.mfull[g]), m & 1, abort, 64)) break;
+      uint64_t mk = 0;
+#pragma unroll
+      for (int w = 0; w < kLoadWarps; ++w) mk |= sm.mask[g][w];
+      tc5::mbar_arrive(smem_u32(&sm.mempty[g]));
+      if (!tc5::mbar_wait_backoff(smem_u32(&sm.s_full[g]), m & 1, abort, 64)) break;
       tc5::fence_after_sync();
       float s[64];
-      tc5::tmem_ld32x2(tmem_s + ((uint32_t)(warp * 32) << 16), s, s + 32);
+      tc5::tmem_ld32x2(tmem + kTmemS + 64 * g + lanes, s, s + 32);
       tc5::fence_before_sync();
-      tc5::mbar_arrive(smem_u32(&sm.s_empty));
+      tc5::mbar_arrive(smem_u32(&sm.s_empty[g]));
+      // tile max of the scaled scores over the rows that exist (log2 units)
+      float mt = -INFINITY;
 #pragma unroll
-      for (int h = 0; h < 64; ++h) s[h] = valid ? s[h] * sc2 : -INFINITY;
-
-      // per-head max over the 128 rows
-      float v[64];
+      for (int j = 0; j < 64; ++j) {
+        s[j] = ((mk >> j) & 1u) ? s[j] * sc2 : -INFINITY;
+        mt = fmaxf(mt, s[j]);
+      }
+      // lazy rescale: keep the reference unless the tile max exceeds it by 2^8
+      float alpha = 1.f;
+      bool resc = false;
+      if (first) {
+        mref = mt;
+        lrun = 0.f;
+      } else if (mt > mref + kRescale) {
+        alpha = mref == -INFINITY ? 0.f : exp2f(mref - mt);
+        mref = mt;
+        resc = true;
+      }
+      // P = 2^(s - m_ref) as bf16: the head's 128-byte row of P^T (K-major B
+      // operand, 128-byte swizzle) in the job's rope sub-tile, which QK is
+      // done with; the weights are summed as rounded, like the MMA sees them
+      float psum = 0.f;
+      if (owner) {
+        uint8_t* prow = gen + g * kBuf + 8 * kSub + h * 128;
+        const float mo = mref == -INFINITY ? 0.f : mref;  // no row yet: every score is -inf
 #pragma unroll
-      for (int h = 0; h < 64; ++h) v[h] = s[h];
-      warp_transpose_reduce<0>(v, lane);
-      sm.red[warp][2 * lane] = v[0];
-      sm.red[warp][2 * lane + 1] = v[1];
-      named_barrier_sync(1, 128);
-      if (warp == 0) {
+        for (int c8 = 0; c8 < 8; ++c8) {
+          uint32_t w4[4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * lane + e;
-          sm.mtile[h] = fmaxf(fmaxf(sm.red[0][h], sm.red[1][h]), fmaxf(sm.red[2][h], sm.red[3][h]));
+          for (int e = 0; e < 4; ++e) {
+            const int j = 8 * c8 + 2 * e;
+            const float p0 = ex2_approx(s[j] - mo);  // 0 for a masked row (-inf)
+            const float p1 = ex2_approx(s[j + 1] - mo);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+            psum += __low2float(b2);
+            psum += __high2float(b2);
+            w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(prow + ((c8 ^ (h & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
+        fence_proxy_async();
+        lrun = lrun * alpha + psum;
+        sm.alpha[g][h] = alpha;
+        if (last) sm.linv[seg & 1][h] = lrun > 0.f ? 1.f / lrun : 0.f;
       }
+      const bool any = __any_sync(0xffffffffu, owner && resc);
+      if (lane == 0) sm.flag[g][warp] = any ? 1 : 0;
       named_barrier_sync(1, 128);
-      float p[64];
+      if (sm.flag[g][0] | sm.flag[g][1] | sm.flag[g][2] | sm.flag[g][3]) {
+        // O^T of the segment so far, times 2^(m_old - m_new) per head (column),
+        // once the previous job's PV is complete; thread = TMEM lane = dim
+        if (!tc5::mbar_wait_backoff(smem_u32(&sm.pv_done), (n - 1) & 1, abort, 64)) break;
+        tc5::fence_after_sync();
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            float o[32];
+            const uint32_t col = kTmemO + 64 * cc + 32 * half;
+            tc5::tmem_ld32(tmem + col + lanes, o);
 #pragma unroll
-      for (int h4 = 0; h4 < 16; ++h4) {
-        const float4 m4 = reinterpret_cast<const float4*>(sm.mtile)[h4];
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int h = h4 * 4 + e;
-          p[h] = mm[e] == -INFINITY ? 0.f : exp2f(s[h] - mm[e]);
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 a4 = reinterpret_cast<const float4*>(sm.alpha[g])[8 * half + i4];
+              o[4 * i4 + 0] *= a4.x;
+              o[4 * i4 + 1] *= a4.y;
+              o[4 * i4 + 2] *= a4.z;
+              o[4 * i4 + 3] *= a4.w;
+            }
+            tc5::tmem_st32(tmem + col + lanes, o);
+          }
         }
+        tc5::tmem_wait_st();
       }
-      // per-head sum over the rows (fixed order: butterfly, then warps 0..3)
-#pragma unroll
-      for (int h = 0; h < 64; ++h) v[h] = p[h];
-      warp_transpose_reduce<1>(v, lane);
-      sm.red[warp][2 * lane] = v[0];
-      sm.red[warp][2 * lane + 1] = v[1];
-      // P^T (bf16) into the rope slot, whose QK reads are complete (s_full):
-      // the K-major B operand [64-row sub-tile][head][64 rows]
-      {
-        uint8_t* pt = rp_gen + (r >> 6) * (kTcH * 128);
-        const int rr = r & 63;
-#pragma unroll
-        for (int h = 0; h < 64; ++h)
-          *reinterpret_cast<__nv_bfloat16*>(pt + h * 128 + ((((rr >> 3) ^ (h & 7)) << 4)) +
-                                            (rr & 7) * 2) = __float2bfloat16_rn(p[h]);
-      }
-      fence_proxy_async();
-      named_barrier_sync(1, 128);
-      if (warp == 0) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * lane + e;
-          sm.ltile[h] = ((sm.red[0][h] + sm.red[1][h]) + sm.red[2][h]) + sm.red[3][h];
-        }
-      }
+      tc5::fence_before_sync();
       tc5::mbar_arrive(smem_u32(&sm.p_full));
-      named_barrier_sync(1, 128);
 
-      // epilogue: normalised tile output (fp16) and lse (log2 units) per head
-      if (!tc5::mbar_wait(smem_u32(&sm.o_full), n & 1, abort)) break;
-      tc5::fence_after_sync();
-      float inv[64];
-#pragma unroll
-      for (int h4 = 0; h4 < 16; ++h4) {
-        const float4 l4 = reinterpret_cast<const float4*>(sm.ltile)[h4];
-        inv[h4 * 4 + 0] = l4.x > 0.f ? 1.f / l4.x : 0.f;
-        inv[h4 * 4 + 1] = l4.y > 0.f ? 1.f / l4.y : 0.f;
-        inv[h4 * 4 + 2] = l4.z > 0.f ? 1.f / l4.z : 0.f;
-        inv[h4 * 4 + 3] = l4.w > 0.f ? 1.f / l4.w : 0.f;
-      }
-      __half* pj = part + (int64_t)job * kTcH * kTcV;
-      for (int cc = 0; cc < 4; ++cc) {
-        float o[64];
-        tc5::tmem_ld32x2(tmem_o + 64 * cc + ((uint32_t)(warp * 32) << 16), o, o + 32);
-        const int vcol = cc * 128 + r;
-#pragma unroll
-        for (int h = 0; h < 64; ++h) pj[h * kTcV + vcol] = __float2half_rn(o[h] * inv[h]);
-      }
-      tc5::fence_before_sync();
-      tc5::mbar_arrive(smem_u32(&sm.o_empty));
-      if (warp == 0) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * lane + e;
-          const float l = sm.ltile[h];
-          part_lse[(int64_t)job * kTcH + h] = l > 0.f ? sm.mtile[h] + log2f(l) : -INFINITY;
+      if (last) {
+        // segment epilogue: thread (warp, lane) owns dim 128cc + 32warp + lane
+        // of each chunk; writes the normalised output and each head's
+        // log-sum-exp (log2 units)
+        if (owner) {
+          ws.part_lse[(int64_t)slot * kTcH + h] = lrun > 0.f ? mref + log2f(lrun) : -INFINITY;
         }
+        if (!tc5::mbar_wait_backoff(smem_u32(&sm.o_full), seg & 1, abort, 64)) break;
+        tc5::fence_after_sync();
+        // heads x dims, fp16: lanes 2i and 2i+1 swap values so that each
+        // holds dims 2i, 2i+1 of one head of a pair (j, j+1); a warp store
+        // covers 32 consecutive dims of two heads (two 64-byte runs)
+        __half* po = ws.part_o + (int64_t)slot * kTcH * kTcV;
+        const bool odd = lane & 1;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          float inv[32];
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 l4 = reinterpret_cast<const float4*>(sm.linv[seg & 1])[8 * half + i4];
+            inv[4 * i4 + 0] = l4.x;
+            inv[4 * i4 + 1] = l4.y;
+            inv[4 * i4 + 2] = l4.z;
+            inv[4 * i4 + 3] = l4.w;
+          }
+#pragma unroll 1
+          for (int cc = 0; cc < 4; ++cc) {
+            float o[32];
+            tc5::tmem_ld32(tmem + kTmemO + 64 * cc + 32 * half + lanes, o);
+            const int d0 = cc * 128 + warp * 32 + (lane & ~1);  // the pair's first dim
+            __half* row = po + (int64_t)(32 * half + (odd ? 1 : 0)) * kTcV + d0;
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              // even lane keeps head j, odd lane head j+1; each sends the other
+              const float mine = odd ? o[j + 1] * inv[j + 1] : o[j] * inv[j];
+              const float give = odd ? o[j] * inv[j] : o[j + 1] * inv[j + 1];
+              const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+              *reinterpret_cast<__half2*>(row + (int64_t)j * kTcV) =
+                  odd ? __floats2half2_rn(got, mine) : __floats2half2_rn(mine, got);
+            }
+          }
+        }
+        tc5::fence_before_sync();
+        tc5::mbar_arrive(smem_u32(&sm.o_empty));
+        ++seg;
       }
     }
   }
@@ -536,88 +581,136 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   if (warp == 4) tc5::tmem_dealloc(tmem, 512);
 }
 
-// Per (query, 16 heads): LSE merge of the query's tiles in job order, inverse
-// RoPE, bf16 store.  The tiles' lse values are staged in shared memory and
-// turned into merge weights once; thread t then owns output dims 2t, 2t+1 and
-// reads the partials of all tiles for a head at once.
-__global__ void __launch_bounds__(256)
+// Per (query, 64 output dims): LSE merge of the query's segment partials in
+// job order, inverse RoPE on the last R dims, bf16 store.  The segments are
+// the query's job range cut at the tile kernel's CTA boundaries (CTA i takes
+// jobs [iN/G, (i+1)N/G)).  Thread t owns head t >> 2 and 16 consecutive dims
+// (t & 3) of the block's 64: a 32-byte load per partial, a 32-byte store.
+__global__ void __launch_bounds__(256, 4)
     attn_merge_kernel(const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
-                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
-  __shared__ float wgt[kMergeMaxJobs][kMergeHeads];
-  __shared__ float Mh[kMergeHeads], tot[kMergeHeads];
+                      int G, __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+  __shared__ int seg[kMergeMaxJobs + 1];
+  __shared__ int nseg_s;
+  __shared__ float wgt[kMergeMaxJobs][kTcH];
+  __shared__ float tot[kTcH], Mh[kTcH], itot[kTcH];
+  __shared__ float2 rope[kRopeTable];  // cos, sin of the block's rotary pairs
   pdl_wait();
   pdl_trigger();
-  const int q = blockIdx.x, hg = blockIdx.y, t = threadIdx.x;
+  const int q = blockIdx.x, dg = blockIdx.y, t = threadIdx.x;
+  const int T = b.B * b.S;
   const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
-  const int j0 = prefix[q];
-  const int nj = min(prefix[q + 1] - j0, kMergeMaxJobs);
-  for (int e = t; e < nj * kMergeHeads; e += blockDim.x) {
-    const int j = e / kMergeHeads, hh = e - j * kMergeHeads;
-    wgt[j][hh] = ws.part_lse[(int64_t)(j0 + j) * kTcH + hg * kMergeHeads + hh];
-  }
+  const int N = prefix[T], j0 = prefix[q], j1 = prefix[q + 1];
+  const int rope0 = kTcV - c.R;  // first rotary dim
+  if (t == 0) nseg_s = 0;
   __syncthreads();
-  if (t < kMergeHeads) {
-    float M = -INFINITY;
-    for (int j = 0; j < nj; ++j) M = fmaxf(M, wgt[j][t]);
-    float sum = 0.f;
-    for (int j = 0; j < nj; ++j) {
-      const float wj = M == -INFINITY ? 0.f : exp2f(wgt[j][t] - M);
-      wgt[j][t] = wj;
-      sum += wj;
-    }
-    Mh[t] = M;
-    tot[t] = sum;
-  }
-  __syncthreads();
-  const int bi = q / b.S;
-  const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
-  const int v = 2 * t;
-  float acc0[kMergeHeads], acc1[kMergeHeads];
-#pragma unroll
-  for (int hh = 0; hh < kMergeHeads; ++hh) acc0[hh] = acc1[hh] = 0.f;
-  float cs = 1.f, sn = 0.f;
-  if (v >= kTcV - c.R && !(p.flags & kPlanBad)) {
-    const float2 r = rope_cos_sin((double)p.pos, c.rope_theta[(v - (kTcV - c.R)) >> 1]);
-    cs = r.x;
-    sn = r.y;
-  }
-  const __half* pbase = ws.part_o + ((int64_t)j0 * kTcH + hg * kMergeHeads) * kTcV + v;
-  // all tiles' partials of the block's heads are loaded before any is used
-  constexpr int kJ = 8;
-  for (int jb = 0; jb < nj; jb += kJ) {
-    __half2 o2[kMergeHeads][kJ];
-#pragma unroll
-    for (int hh = 0; hh < kMergeHeads; ++hh)
-#pragma unroll
-      for (int k = 0; k < kJ; ++k)
-        o2[hh][k] = jb + k < nj ? *reinterpret_cast<const __half2*>(
-                                      pbase + ((int64_t)(jb + k) * kTcH + hh) * kTcV)
-                                : __floats2half2_rn(0.f, 0.f);
-#pragma unroll
-    for (int hh = 0; hh < kMergeHeads; ++hh) {
-#pragma unroll
-      for (int k = 0; k < kJ; ++k) {
-        if (jb + k < nj) {
-          acc0[hh] = fmaf(wgt[jb + k][hh], __low2float(o2[hh][k]), acc0[hh]);
-          acc1[hh] = fmaf(wgt[jb + k][hh], __high2float(o2[hh][k]), acc1[hh]);
-        }
+  // segment starts, in parallel: j0 and every CTA start inside (j0, j1)
+  if (j1 > j0) {
+    const int i0 = (int)((int64_t)j0 * G / N);  // the CTA holding j0
+    for (int i = i0 + t; i < G; i += blockDim.x) {
+      const int l = (int)((int64_t)i * N / G);
+      if (l >= j1) break;
+      const int lprev = i > i0 ? (int)((int64_t)(i - 1) * N / G) : -1;
+      // the first CTA start >= j0 of a run of equal starts opens a segment;
+      // j0 itself opens one whether or not a CTA starts there
+      if (i == i0 || (l > j0 && l > lprev)) {
+        const int k = atomicAdd(&nseg_s, 1);
+        if (k < kMergeMaxJobs) seg[k] = i == i0 ? j0 : l;
       }
     }
   }
-#pragma unroll
-  for (int hh = 0; hh < kMergeHeads; ++hh) {
-    const float it = tot[hh] > 0.f ? 1.f / tot[hh] : 0.f;
-    const float x0 = acc0[hh] * it, x1 = acc1[hh] * it;
-    const int h = hg * kMergeHeads + hh;
-    const float y0 = x0 * cs + x1 * sn, y1 = -x0 * sn + x1 * cs;
-    *reinterpret_cast<uint32_t*>(out + ((int64_t)q * kTcH + h) * kTcV + v) = pack_bf16x2(y0, y1);
-    if (lse_out && t == 0)
-      lse_out[(int64_t)q * kTcH + h] =
-          Mh[hh] == -INFINITY ? -INFINITY : (Mh[hh] + log2f(tot[hh])) * 0.6931471805599453f;
+  if (dg * kMergeDims + kMergeDims > rope0 && t >= 64 && t < 64 + c.R / 2 && t - 64 < kRopeTable) {
+    const int bi = q / b.S;
+    const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
+    const int i = t - 64;
+    rope[i] = (p.flags & kPlanBad) ? make_float2(1.f, 0.f) : rope_cos_sin((double)p.pos, c.rope_theta[i]);
   }
+  __syncthreads();
+  const int nseg = min(nseg_s, kMergeMaxJobs);
+  if (t == 0) {
+    // order the starts (the atomic slots are unordered): insertion sort
+    for (int a = 1; a < nseg; ++a) {
+      const int x = seg[a];
+      int k = a - 1;
+      while (k >= 0 && seg[k] > x) {
+        seg[k + 1] = seg[k];
+        --k;
+      }
+      seg[k + 1] = x;
+    }
+  }
+  __syncthreads();
+  for (int e = t; e < nseg * kTcH; e += blockDim.x) {
+    const int k = e >> 6, h = e & 63;
+    wgt[k][h] = ws.part_lse[(int64_t)seg[k] * kTcH + h];
+  }
+  __syncthreads();
+  if (t < kTcH) {
+    float M = -INFINITY;
+    for (int k = 0; k < nseg; ++k) M = fmaxf(M, wgt[k][t]);
+    float sum = 0.f;
+    for (int k = 0; k < nseg; ++k) {
+      const float wk = M == -INFINITY ? 0.f : exp2f(wgt[k][t] - M);
+      wgt[k][t] = wk;
+      sum += wk;
+    }
+    Mh[t] = M;
+    tot[t] = sum;
+    itot[t] = sum > 0.f ? 1.f / sum : 0.f;
+  }
+  __syncthreads();
+  const int h = t >> 2;
+  const int v0 = dg * kMergeDims + 16 * (t & 3);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  // partials four at a time, all loads of a group issued before use
+  for (int k0 = 0; k0 < nseg; k0 += 4) {
+    uint4 u[4][2];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      if (k0 + kk < nseg) {
+        const uint4* src =
+            reinterpret_cast<const uint4*>(ws.part_o + ((int64_t)seg[k0 + kk] * kTcH + h) * kTcV + v0);
+        u[kk][0] = src[0];
+        u[kk][1] = src[1];
+      } else {
+        u[kk][0] = u[kk][1] = make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float w = k0 + kk < nseg ? wgt[k0 + kk][h] : 0.f;
+      const __half2* a = reinterpret_cast<const __half2*>(&u[kk][0]);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        acc[2 * e] = fmaf(w, __low2float(a[e]), acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, __high2float(a[e]), acc[2 * e + 1]);
+      }
+    }
+  }
+  const float it = itot[h];
+  uint32_t pk[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int v = v0 + 2 * e;
+    const float x0 = acc[2 * e] * it, x1 = acc[2 * e + 1] * it;
+    float cs = 1.f, sn = 0.f;
+    if (v >= rope0) {
+      const float2 r = rope[(v - rope0) >> 1];
+      cs = r.x;
+      sn = r.y;
+    }
+    pk[e] = pack_bf16x2(x0 * cs + x1 * sn, -x0 * sn + x1 * cs);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)q * kTcH + h) * kTcV + v0);
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (lse_out && dg == 0 && t < kTcH)
+    lse_out[(int64_t)q * kTcH + t] =
+        Mh[t] == -INFINITY ? -INFINITY : (Mh[t] + log2f(tot[t])) * 0.6931471805599453f;
 }
 
-// Counts each query's tiles into ws.job_prefix when the host has no lengths.
+// Counts each query's jobs into ws.job_prefix when the host has no lengths.
 __global__ void __launch_bounds__(1024) job_prep_kernel(DevCfg c, DevBatch b, Workspace ws) {
   __shared__ int scan_tmp[33];
   __shared__ int carry;
@@ -708,17 +801,10 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
                          float* lse_out, int num_sms, cudaStream_t st, bool pdl) {
   const int T = b.B * b.S;
   if (T == 0) return 0;
-  if (!ws.part_o || max_jobs_per_query(c) > kMergeMaxJobs || b.raw_rows > 0x7fffffffLL || b.cmp_rows > 0x7fffffffLL ||
-      b.hca_rows > 0x7fffffffLL || (int64_t)T * kTcH > 0x7fffffffLL)
+  if (!ws.part_o || max_jobs_per_query(c) > kMergeMaxJobs || b.raw_rows > 0x7fffffffLL ||
+      b.cmp_rows > 0x7fffffffLL || b.hca_rows > 0x7fffffffLL || (int64_t)T * kTcH > 0x7fffffffLL)
     return -2;
-  CUtensorMap rawmap, cmpmap, hcamap, qmap;
-  if (!make_map(&rawmap, b.raw, (uint64_t)(b.raw_rows > 0 ? b.raw_rows : 1), b.raw_stride, 1)) return -1;
-  if (!make_map(&cmpmap, b.cmp, (uint64_t)(b.cmp_rows > 0 ? b.cmp_rows : 1), b.cmp_stride, 1)) return -1;
-  if (c.hca_ratio > 0) {
-    if (!make_map(&hcamap, b.hca, (uint64_t)(b.hca_rows > 0 ? b.hca_rows : 1), b.hca_stride, 1)) return -1;
-  } else {
-    hcamap = cmpmap;
-  }
+  CUtensorMap qmap;
   if (!make_map(&qmap, b.q, (uint64_t)T * kTcH, kTcD, kTcH)) return -1;
   static bool attr = false;
   if (!attr) {
@@ -732,12 +818,12 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
   }
   int grid = num_sms;
   if (jobs.host_B >= 0 && jobs.prefix[T] < grid) grid = jobs.prefix[T] > 0 ? jobs.prefix[T] : 1;
-  if (launch_kernel(attn_tile_kernel, dim3(grid), dim3(kA5Threads), kA5Dyn, st, pdl, rawmap, cmpmap,
-                    hcamap, qmap, jobs, c, b, ws, topk_idx, topk_cnt) < 0)
+  if (launch_kernel(attn_tile_kernel, dim3(grid), dim3(kA5Threads), kA5Dyn, st, pdl, qmap, jobs, c,
+                    b, ws, topk_idx, topk_cnt) < 0)
     return -1;
   ++n;
-  if (launch_kernel(attn_merge_kernel, dim3(T, kTcH / kMergeHeads), dim3(256), 0, st, pdl, jobs, c, b, ws,
-                    static_cast<__nv_bfloat16*>(out), lse_out) < 0)
+  if (launch_kernel(attn_merge_kernel, dim3(T, kTcV / kMergeDims), dim3(256), 0, st, pdl, jobs, c,
+                    b, ws, grid, static_cast<__nv_bfloat16*>(out), lse_out) < 0)
     return -1;
   return n + 1;
 }

@@ -121,8 +121,8 @@ struct Workspace {
   int* topk_idx;      // [max_T, K]
   int* topk_cnt;      // [max_T]
   int* job_prefix;    // [max_T + 1] attention tiles per query, prefix (device-built)
-  __half* part_o;     // [max_T * max_jobs, H, V] per-tile normalised attention output
-  float* part_lse;    // [max_T * max_jobs, H] per-tile log-sum-exp (log2 units)
+  __half* part_o;     // [max_T * max_jobs, H, V] per-segment normalised attention output
+  float* part_lse;    // [max_T * max_jobs, H] per-segment log-sum-exp (log2 units)
   int max_T, max_batch;
   int64_t scores_ld;
 };

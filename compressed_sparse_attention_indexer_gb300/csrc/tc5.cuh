@@ -51,6 +51,25 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   *abort = 1;
   return false;
 }
+// As mbar_wait, but after a few tight polls the thread sleeps between polls
+// (32 ns doubling up to max_ns), so that waiting warps leave the issue slots
+// and the shared-memory pipe to the warps that work.  Gives up after about a
+// second in total.
+__device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int* abort,
+                                                  uint32_t max_ns) {
+  uint32_t ns = 32;
+  for (uint32_t i = 0; i < (1u << 23); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= 8) {
+      __nanosleep(ns);
+      ns = ns * 2 > max_ns ? max_ns : ns * 2;
+      if ((i & 15u) == 15u && *abort) return false;
+    }
+  }
+  *abort = 1;
+  return false;
+}
+
 // Bounded wait that ignores the abort flag: used while winding down, to let
 // copies and MMAs already started finish before the block exits.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -193,6 +212,29 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, float* v0, float* v1
     v0[i] = __uint_as_float(r[i]);
     v1[i] = __uint_as_float(r[32 + i]);
   }
+}
+
+// 32 lanes x 32 consecutive fp32 columns from registers (the store mirror of
+// tmem_ld32); tmem_wait_st orders the stores before later tcgen05 work.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
 }  // namespace tc5

@@ -61,7 +61,11 @@ def check_against_oracle(wl, hb, g, ref=None, what=""):
     assert g["status"] == csa.CSA_OK, csa.last_error()
     assert_topk_sets(g["idx"], g["cnt"], ref, scores_fn(cfg, hb), cfg.topk, what)
     assert_close(g["out"], ref["out"], tol_for(cfg), what + " out")
-    lse_tol = (1e-5, 1e-5) if cfg.dtype == "f32" else (1e-3, 1e-4)
+    # bf16 path: the softmax weights are rounded to bf16 (unit roundoff
+    # u = 2^-9) before they are summed, so ln(l) may move by up to u/(1-u)
+    # ~ 1.96e-3 (max bound, plus fp32 noise); the rounding errors are
+    # unbiased, so their mean over heads stays near u/sqrt(3n) for n terms.
+    lse_tol = (1e-5, 1e-5) if cfg.dtype == "f32" else (2.5e-3, 5e-4)
     assert_close(g["lse"], ref["lse"], lse_tol, what + " lse")
     return ref
 

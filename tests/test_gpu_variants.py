@@ -1,7 +1,8 @@
 """The same parity check under the other kernel selections and launch modes.
 
 CSA_INDEXER=mma selects the warp-MMA indexer (the measured baseline of the
-tcgen05 one); CSA_ATTN=tc5 selects the tcgen05 attention tile kernel + merge;
+tcgen05 one); CSA_ATTN=mma selects the warp-MMA attention kernel (the
+measured baseline of the tcgen05 tile kernel + merge);
 CSA_PDL=0 launches without programmatic dependent launch.  All are read once
 per process, so each variant runs in a child process.
 """
@@ -44,8 +45,8 @@ print("variant ok")
 
 
 @pytest.mark.parametrize("env", [{"CSA_INDEXER": "mma"}, {"CSA_PDL": "0"},
-                                 {"CSA_INDEXER": "mma", "CSA_PDL": "0"}, {"CSA_ATTN": "tc5"},
-                                 {"CSA_ATTN": "tc5", "CSA_PDL": "0"}])
+                                 {"CSA_INDEXER": "mma", "CSA_PDL": "0"}, {"CSA_ATTN": "mma"},
+                                 {"CSA_ATTN": "mma", "CSA_PDL": "0"}])
 def test_variant_parity(env):
     import torch
     if not torch.cuda.is_available():
