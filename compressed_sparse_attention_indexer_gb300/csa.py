@@ -22,7 +22,7 @@ ERROR_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 
 EXPORTS = ("csa_decode_create", "csa_decode_destroy", "csa_indexer_topk", "csa_sparse_attn",
            "csa_decode_step", "csa_indexer_scores", "csa_topk_select", "csa_check_batch",
            "csa_get_status", "csa_last_error", "csa_last_launch_count", "csa_abi_version",
-           "csa_profile_enable", "csa_profile_read")
+           "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static")
 STAGES = ("plan", "indexer", "topk", "attention")
 
 
@@ -90,9 +90,11 @@ def lib(path: str | None = None):
             L.csa_abi_version.restype = i32
             L.csa_profile_enable.argtypes = [H, i32]
             L.csa_profile_read.argtypes = [H, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)]
+            L.csa_indexer_topk_static.argtypes = [ctypes.POINTER(CConfig), ctypes.POINTER(CBatch), vp,
+                                                  vp, vp, vp]
             for name in ("csa_decode_create", "csa_indexer_topk", "csa_sparse_attn", "csa_decode_step",
                          "csa_indexer_scores", "csa_topk_select", "csa_check_batch", "csa_get_status",
-                         "csa_profile_enable", "csa_profile_read"):
+                         "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -144,6 +146,13 @@ def make_batch_struct(batch: dict, ctx_len_host=None) -> CBatch:
 def check_batch(cconfig: CConfig, cbatch: CBatch) -> int:
     """Host-side validation only (no GPU); returns the C return code."""
     return lib().csa_check_batch(ctypes.byref(cconfig), ctypes.byref(cbatch))
+
+
+def indexer_topk_static(cconfig: CConfig, cb: CBatch, topk_idx, topk_cnt, status=None, stream=None):
+    """Steps (a)+(b) without a handle or any device allocation (scratch in the
+    library's static device array; see csa_indexer_topk_static in csa.h)."""
+    _check(lib().csa_indexer_topk_static(ctypes.byref(cconfig), ctypes.byref(cb), _ptr(topk_idx),
+                                         _ptr(topk_cnt), _ptr(status), _stream(stream)))
 
 
 def _stream(stream) -> int | None:

@@ -6,6 +6,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -248,6 +249,47 @@ void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int
   }));
 }
 
+// ---- allocation-free variant of indexer + Top-K ----------------------------
+// Its scratch (status word, indexer work list, score matrix) lives in this
+// file-scope device array, loaded with the module; nothing is allocated per
+// call.  One array per device and process, so calls that overlap in time
+// (other streams or threads on the same device) share it and race.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+void* g_static_addr[kMaxStaticDevices];  // device address of g_static_scratch, per device
+int g_static_sms[kMaxStaticDevices];
+
+// The config as the kernels read it (what csa_decode_create stores in a
+// handle).
+csa::DevCfg static_devcfg(const csa_config& c) {
+  csa::DevCfg d;
+  d.H = c.heads; d.D = c.row_dim; d.V = c.v_dim; d.R = c.row_dim - c.v_dim;
+  d.Hi = c.idx_heads; d.Di = c.idx_dim; d.ratio = c.ratio; d.K = c.topk;
+  d.win = c.win; d.hca_ratio = c.hca_ratio; d.dtype = c.dtype;
+  d.scale = c.softmax_scale > 0.f ? c.softmax_scale : (float)(1.0 / sqrt((double)c.row_dim));
+  d.rope_base = c.rope_base;
+  d.max_context = c.max_context;
+  d.max_vis = c.max_context / c.ratio;
+  for (int i = 0; i < csa::kRopeTable; ++i)
+    d.rope_theta[i] = (d.R > 0 && i < d.R / 2)
+                          ? pow((double)c.rope_base, -2.0 * (double)i / (double)d.R) : 0.0;
+  return d;
+}
+
+// Bytes of scratch a batch needs: the status word, the work list, the
+// [B*S, max_context/ratio] fp32 score matrix, each 256-byte aligned.
+size_t static_scratch_need(const csa_config& c, const csa_batch* b, size_t* o_prefix,
+                           size_t* o_scores) {
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t ld = (size_t)(c.max_context / c.ratio > 0 ? c.max_context / c.ratio : 1);
+  *o_prefix = 256;
+  *o_scores = *o_prefix + al(sizeof(int) * ((size_t)b->B + 1));
+  return *o_scores + al(sizeof(float) * ld * (size_t)b->B * (size_t)b->S);
+}
+
 }  // namespace
 
 extern "C" {
@@ -415,6 +457,85 @@ int csa_topk_select(csa_handle* h, int32_t nq, const float* scores, int64_t ld, 
                             h->dc.max_vis, st, pdl);
   }));
   return finish(h, L);
+}
+
+int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* topk_idx,
+                            int32_t* topk_cnt, int32_t* status_out, void* stream) {
+  int rc = validate_cfg(cfg);
+  if (rc) return rc;
+  rc = validate_batch_cfg(*cfg, b);
+  if (rc) return rc;
+  if (!topk_idx || !topk_cnt) return fail(CSA_ERR_INVALID_ARG, "topk_idx/topk_cnt NULL");
+  size_t o_prefix = 0, o_scores = 0;
+  const size_t need = static_scratch_need(*cfg, b, &o_prefix, &o_scores);
+  if (need > kStaticScratchBytes)
+    return fail(CSA_ERR_WORKSPACE,
+                "B*S = %d queries x max_context/ratio = %d scores need %zu bytes of scratch, above "
+                "the %zu bytes of the allocation-free entry point (use csa_indexer_topk)",
+                b->B * b->S, cfg->max_context / cfg->ratio, need, kStaticScratchBytes);
+  // set-up, once per device: the scratch array's address and the SM count
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxStaticDevices)
+    return fail(CSA_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxStaticDevices - 1);
+  void* base = nullptr;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+      void* a = nullptr;
+      e = cudaGetSymbolAddress(&a, g_static_scratch);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+      e = cudaDeviceGetAttribute(&g_static_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+      g_static_addr[dev] = a;
+    }
+    base = g_static_addr[dev];
+    sms = g_static_sms[dev];
+  }
+  if (b->B == 0) return CSA_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  char* sb = static_cast<char*>(base);
+  // a handle on the stack that borrows the static scratch: the same launch
+  // sequence as csa_indexer_topk, with no workspace of its own
+  csa_handle h;
+  h.cfg = *cfg;
+  h.dc = static_devcfg(*cfg);
+  h.ws_base = nullptr;
+  h.ws_bytes = 0;
+  h.device = dev;
+  h.num_sms = sms;
+  h.last_launches = 0;
+  csa::Workspace& w = h.ws;
+  w.status = reinterpret_cast<int*>(sb);
+  w.item_prefix = reinterpret_cast<int*>(sb + o_prefix);
+  w.scores = reinterpret_cast<float*>(sb + o_scores);
+  w.topk_idx = nullptr;
+  w.topk_cnt = nullptr;
+  w.job_prefix = nullptr;
+  w.part_o = nullptr;
+  w.part_lse = nullptr;
+  w.max_T = b->B * b->S;
+  w.max_batch = b->B;
+  w.scores_ld = h.dc.max_vis > 0 ? h.dc.max_vis : 1;
+  // the status word must read zero when the kernels start; the work list and
+  // the scores are fully written before they are read
+  e = cudaMemsetAsync(w.status, 0, sizeof(int), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status)");
+  const csa::DevBatch db = dev_batch(b);
+  const bool pdl = use_pdl();
+  Launches L;
+  run_indexer(&h, b, db, 0, w.scores, w.scores_ld, st, L);
+  L.add(csa::launch_topk(h.dc, &db, b->B * b->S, w.scores, w.scores_ld, nullptr, topk_idx, topk_cnt,
+                         w.status, h.dc.max_vis, st, pdl));
+  rc = finish(&h, L);
+  if (rc) return rc;
+  if (status_out) {
+    e = cudaMemcpyAsync(status_out, w.status, sizeof(int), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(status)");
+  }
+  return CSA_OK;
 }
 
 int csa_profile_enable(csa_handle* h, int32_t enable) {

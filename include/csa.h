@@ -165,6 +165,34 @@ CSA_API int csa_indexer_scores(csa_handle *h, const csa_batch *b, float *scores,
 CSA_API int csa_topk_select(csa_handle *h, int32_t nq, const float *scores, int64_t ld,
                     const int32_t *n, int32_t *topk_idx, int32_t *topk_cnt, void *stream);
 
+/* Steps (a)+(b) like csa_indexer_topk, without a handle and without
+ * allocating device memory.  The published method has no counterpart of this
+ * entry point: it serves callers that may not allocate during a decode step, such
+ * as a serving loop whose device memory is planned up front (a library
+ * allocation would go around its pool) or whose step must not block (cudaMalloc
+ * and cudaFree may synchronise the device).
+ *
+ * Scratch (a status word, the indexer work list and the fp32 score matrix
+ * [B*S, max_context/ratio]) is an 8 MiB array of this library's device
+ * module; a batch needing more is rejected with CSA_ERR_WORKSPACE and a
+ * message giving the size (csa_indexer_topk has no such limit).  cfg's
+ * max_batch / max_queries_per_req bound B and S as for a handle.
+ *
+ * The first call on each device looks up the array's address (and the SM
+ * count) and keeps them; make that first call, for example with B = 0,
+ * outside stream capture.  Each call clears the status word on `stream`
+ * before its kernels run.  The array is shared by every call in the process
+ * on that device: calls whose execution overlaps (other streams or host
+ * threads) race on it and must be ordered by the caller.
+ *
+ * topk_idx / topk_cnt as csa_indexer_topk.  status_out: NULL or a device
+ * int32 that receives the status word after the kernels: 0, or bit 1 (a
+ * length or row index out of range, what csa_get_status reports as
+ * CSA_ERR_BAD_INDEX) and bit 2 (a device wait gave up, CSA_ERR_TIMEOUT).
+ * Launches on `stream`; does not synchronise. */
+CSA_API int csa_indexer_topk_static(const csa_config *cfg, const csa_batch *b, int32_t *topk_idx,
+                            int32_t *topk_cnt, int32_t *status_out, void *stream);
+
 /* Host-side checks of a batch against a config, exactly those every entry
  * point runs before launching (null / misaligned pointers, strides, sizes
  * against the maxima, ctx_len_host values).  Touches no device memory and
