@@ -244,6 +244,17 @@ def src_sha(files):
     return h.hexdigest()[:16]
 
 
+# sources of the kernels each stage runs by default (a recorded traffic figure
+# is dropped once any of them changes)
+_C = "compressed_sparse_attention_indexer_gb300/csrc/"
+KERNEL_SOURCES = {
+    "indexer": [_C + "indexer_tc5.cu", _C + "tc5.cuh", _C + "csa_internal.cuh"],
+    "attention": [_C + "attention_tc5.cu", _C + "tc5.cuh", _C + "csa_internal.cuh"],
+    "topk": [_C + "topk.cu", _C + "csa_internal.cuh"],
+    "plan": [_C + "plan.cu", _C + "csa_internal.cuh"],
+}
+
+
 def load_traffic(kernel: str, workload: str):
     """ncu-measured DRAM bytes per launch, if recorded for the current kernel source."""
     p = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
@@ -251,17 +262,9 @@ def load_traffic(kernel: str, workload: str):
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("source_sha") != src_sha(d.get("sources", [])):
+    if d.get("source_sha") != src_sha(KERNEL_SOURCES.get(kernel, d.get("sources", []))):
         return None
     return d.get("dram_bytes_per_launch")
-
-
-KERNEL_SOURCES = {
-    "indexer": ["compressed_sparse_attention_indexer_gb300/csrc/indexer.cu"],
-    "attention": ["compressed_sparse_attention_indexer_gb300/csrc/attention.cu"],
-    "topk": ["compressed_sparse_attention_indexer_gb300/csrc/topk.cu"],
-    "plan": ["compressed_sparse_attention_indexer_gb300/csrc/plan.cu"],
-}
 
 
 def run_ours(args):
