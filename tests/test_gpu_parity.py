@@ -80,6 +80,10 @@ def test_workload_decode_step(name):
     hb = make_batch(wl)
     g = run_step(wl, hb, max_context=65536 if name == "long_ragged_b64" else None)
     ref = check_against_oracle(wl, hb, g, what=name)
+    # the launch configuration bench.py times: lengths known on the host
+    # (host-built work lists, no prep kernels)
+    gh = run_step(wl, hb, max_context=65536 if name == "long_ragged_b64" else None, host_lens=True)
+    check_against_oracle(wl, hb, gh, ref=ref, what=name + " host-lengths")
     # attention alone on the oracle's own selection isolates steps (c)-(d)
     cfg = wl.cfg
     B, S = hb["B"], hb["S"]
