@@ -584,15 +584,17 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 // Per (query, 64 output dims): LSE merge of the query's segment partials in
 // job order, inverse RoPE on the last R dims, bf16 store.  The segments are
 // the query's job range cut at the tile kernel's CTA boundaries (CTA i takes
-// jobs [iN/G, (i+1)N/G)).  Thread t owns head t >> 2 and 16 consecutive dims
-// (t & 3) of the block's 64: a 32-byte load per partial, a 32-byte store.
+// jobs [iN/G, (i+1)N/G)); with N >= G the starts are strictly increasing, so
+// segment k > 0 starts at (i0 + k)N/G directly.  Thread t owns head t >> 2 and
+// 16 consecutive dims (t & 3) of the block's 64: it loads its head's LSE and
+// a 32-byte piece of the partials, four segments per batch, derives the
+// weights itself (running max across batches), and stores 32 bytes.
+constexpr int kMergeUnroll = 4;  // partials whose loads are in flight together
 __global__ void __launch_bounds__(256, 4)
     attn_merge_kernel(const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
                       int G, __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   __shared__ int seg[kMergeMaxJobs + 1];
   __shared__ int nseg_s;
-  __shared__ float wgt[kMergeMaxJobs][kTcH];
-  __shared__ float tot[kTcH], Mh[kTcH], itot[kTcH];
   __shared__ float2 rope[kRopeTable];  // cos, sin of the block's rotary pairs
   pdl_wait();
   pdl_trigger();
@@ -601,85 +603,85 @@ __global__ void __launch_bounds__(256, 4)
   const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
   const int N = prefix[T], j0 = prefix[q], j1 = prefix[q + 1];
   const int rope0 = kTcV - c.R;  // first rotary dim
-  if (t == 0) nseg_s = 0;
-  __syncthreads();
-  // segment starts, in parallel: j0 and every CTA start inside (j0, j1)
-  if (j1 > j0) {
-    const int i0 = (int)((int64_t)j0 * G / N);  // the CTA holding j0
-    for (int i = i0 + t; i < G; i += blockDim.x) {
-      const int l = (int)((int64_t)i * N / G);
-      if (l >= j1) break;
-      const int lprev = i > i0 ? (int)((int64_t)(i - 1) * N / G) : -1;
-      // the first CTA start >= j0 of a run of equal starts opens a segment;
-      // j0 itself opens one whether or not a CTA starts there
-      if (i == i0 || (l > j0 && l > lprev)) {
-        const int k = atomicAdd(&nseg_s, 1);
-        if (k < kMergeMaxJobs) seg[k] = i == i0 ? j0 : l;
-      }
-    }
-  }
   if (dg * kMergeDims + kMergeDims > rope0 && t >= 64 && t < 64 + c.R / 2 && t - 64 < kRopeTable) {
     const int bi = q / b.S;
     const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
     const int i = t - 64;
     rope[i] = (p.flags & kPlanBad) ? make_float2(1.f, 0.f) : rope_cos_sin((double)p.pos, c.rope_theta[i]);
   }
+  // CTA i starts at job (i N) / G; 32-bit arithmetic while i N fits
+  const bool small = (uint64_t)N * (uint64_t)G < (1ull << 32);
+  auto cta_start = [&](int i) -> int {
+    return small ? (int)((uint32_t)i * (uint32_t)N / (uint32_t)G) : (int)((int64_t)i * N / G);
+  };
+  if (j1 <= j0) {
+    if (t == 0) nseg_s = 0;
+  } else if (N >= G) {
+    // starts strictly increase: with i0 the CTA holding j0, segment t > 0
+    // starts at (i0 + t)N/G while that is < j1
+    if (t < kMergeMaxJobs) {
+      int i0 = small ? (int)((uint32_t)j0 * (uint32_t)G / (uint32_t)N) : (int)((int64_t)j0 * G / N);
+      if (i0 + 1 < G && cta_start(i0 + 1) <= j0) ++i0;
+      const int i = i0 + t;
+      const int l = t == 0 ? j0 : (i < G ? cta_start(i) : j1);
+      if (l < j1) seg[t] = l;
+      const int lnext = i + 1 < G ? cta_start(i + 1) : j1;
+      if (l < j1 && lnext >= j1) nseg_s = t + 1;  // the last segment
+    }
+  } else if (t == 0) {
+    // more CTAs than jobs: runs of equal starts, walked in order
+    int k = 0, last = j0;
+    seg[k++] = j0;
+    for (int i = (int)((int64_t)j0 * G / N) + 1; i < G && k < kMergeMaxJobs; ++i) {
+      const int l = cta_start(i);
+      if (l >= j1) break;
+      if (l > last) {
+        seg[k++] = l;
+        last = l;
+      }
+    }
+    nseg_s = k;
+  }
   __syncthreads();
   const int nseg = min(nseg_s, kMergeMaxJobs);
-  if (t == 0) {
-    // order the starts (the atomic slots are unordered): insertion sort
-    for (int a = 1; a < nseg; ++a) {
-      const int x = seg[a];
-      int k = a - 1;
-      while (k >= 0 && seg[k] > x) {
-        seg[k + 1] = seg[k];
-        --k;
-      }
-      seg[k + 1] = x;
-    }
-  }
-  __syncthreads();
-  for (int e = t; e < nseg * kTcH; e += blockDim.x) {
-    const int k = e >> 6, h = e & 63;
-    wgt[k][h] = ws.part_lse[(int64_t)seg[k] * kTcH + h];
-  }
-  __syncthreads();
-  if (t < kTcH) {
-    float M = -INFINITY;
-    for (int k = 0; k < nseg; ++k) M = fmaxf(M, wgt[k][t]);
-    float sum = 0.f;
-    for (int k = 0; k < nseg; ++k) {
-      const float wk = M == -INFINITY ? 0.f : exp2f(wgt[k][t] - M);
-      wgt[k][t] = wk;
-      sum += wk;
-    }
-    Mh[t] = M;
-    tot[t] = sum;
-    itot[t] = sum > 0.f ? 1.f / sum : 0.f;
-  }
-  __syncthreads();
   const int h = t >> 2;
   const int v0 = dg * kMergeDims + 16 * (t & 3);
+  // partials and LSEs in batches of kMergeUnroll, loaded together; a running
+  // max over the batches rescales what is summed so far
+  float M = -INFINITY, tot = 0.f;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  // partials four at a time, all loads of a group issued before use
-  for (int k0 = 0; k0 < nseg; k0 += 4) {
-    uint4 u[4][2];
+  for (int k0 = 0; k0 < nseg; k0 += kMergeUnroll) {
+    uint4 u[kMergeUnroll][2];
+    float lk[kMergeUnroll];
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
+    for (int kk = 0; kk < kMergeUnroll; ++kk) {
       if (k0 + kk < nseg) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(ws.part_o + ((int64_t)seg[k0 + kk] * kTcH + h) * kTcV + v0);
+        const int64_t sb = (int64_t)seg[k0 + kk] * kTcH + h;
+        const uint4* src = reinterpret_cast<const uint4*>(ws.part_o + sb * kTcV + v0);
         u[kk][0] = src[0];
         u[kk][1] = src[1];
+        lk[kk] = ws.part_lse[sb];
       } else {
         u[kk][0] = u[kk][1] = make_uint4(0u, 0u, 0u, 0u);
+        lk[kk] = -INFINITY;
       }
     }
+    float Mn = M;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const float w = k0 + kk < nseg ? wgt[k0 + kk][h] : 0.f;
+    for (int kk = 0; kk < kMergeUnroll; ++kk) Mn = fmaxf(Mn, lk[kk]);
+    if (Mn > M && M != -INFINITY) {
+      const float sc = exp2f(M - Mn);
+      tot *= sc;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc[i] *= sc;
+    }
+    M = Mn;
+#pragma unroll
+    for (int kk = 0; kk < kMergeUnroll; ++kk) {
+      const float w = (M == -INFINITY || lk[kk] == -INFINITY) ? 0.f : exp2f(lk[kk] - M);
+      tot += w;
       const __half2* a = reinterpret_cast<const __half2*>(&u[kk][0]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -688,7 +690,7 @@ __global__ void __launch_bounds__(256, 4)
       }
     }
   }
-  const float it = itot[h];
+  const float it = tot > 0.f ? 1.f / tot : 0.f;
   uint32_t pk[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
@@ -705,9 +707,8 @@ __global__ void __launch_bounds__(256, 4)
   uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)q * kTcH + h) * kTcV + v0);
   dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  if (lse_out && dg == 0 && t < kTcH)
-    lse_out[(int64_t)q * kTcH + t] =
-        Mh[t] == -INFINITY ? -INFINITY : (Mh[t] + log2f(tot[t])) * 0.6931471805599453f;
+  if (lse_out && dg == 0 && (t & 3) == 0)
+    lse_out[(int64_t)q * kTcH + h] = M == -INFINITY ? -INFINITY : (M + log2f(tot)) * 0.6931471805599453f;
 }
 
 // Counts each query's jobs into ws.job_prefix when the host has no lengths.
