@@ -357,14 +357,17 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   if (NB > 8) NB = 8;
   if (NB < 2) return -2;
   const int per_cta = 228 * 1024 / ctas_per_sm - 1024;  // per-SM shared memory / CTAs
-  int NQB = 2, NST = 0;
+  // key stages first: a CTA spans few requests, so a second q_idx buffer
+  // (prefetching the next request's queries) is kept only when it costs no
+  // key stage
   const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
-  for (NQB = 2; NQB >= 1; --NQB) {
-    NST = (budget - NQB * qbytes) / kStageBytes;
-    if (NST > max_stages) NST = max_stages;
-    if (NST >= 3 || (ctas_per_sm >= 2 && NST >= 2)) break;
-  }
-  if (NQB < 1 || NST < 2) return -2;
+  auto stages = [&](int nqb) {
+    const int n = (budget - nqb * qbytes) / kStageBytes;
+    return n > max_stages ? max_stages : n;
+  };
+  const int NQB = stages(2) >= stages(1) ? 2 : 1;
+  const int NST = stages(NQB);
+  if (NST < 2) return -2;
   CUtensorMap kmap, qmap;
   if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk)) return -1;
   if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
