@@ -405,6 +405,9 @@ def run_ours(args):
         ev1.record(stream)
         torch.cuda.synchronize()
     ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, dist if ws > 1 else None, dev)
+    st = dec.status()
+    if st != csa.CSA_OK:
+        raise RuntimeError(f"device status {st} after the timed steps: {csa.last_error()}")
     if ws > 1:
         dist.barrier()
 

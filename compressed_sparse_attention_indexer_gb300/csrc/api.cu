@@ -207,12 +207,14 @@ bool use_pdl() {
 // attention: the tcgen05 tile kernel + merge for the tensor-core shape
 // (unless CSA_ATTN=mma or the batch does not fit it), else the warp-MMA or
 // SIMT kernel
+// early: the Top-K kernel of the same call runs right before (see
+// launch_attention_tc5)
 int run_attention(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, const int* idx,
-                  const int* cnt, void* out, float* lse, cudaStream_t st, bool pdl) {
+                  const int* cnt, void* out, float* lse, cudaStream_t st, bool pdl, bool early) {
   if (csa::tensor_core_shape(h->dc) && csa::attention_impl() == csa::kAttnTc5) {
     csa::host_jobs(h->dc, b->B, b->S, b->ctx_len_host, &h->jobs);
     const int r = csa::launch_attention_tc5(h->dc, db, h->ws, h->jobs, idx, cnt, out, lse,
-                                            h->num_sms, st, pdl);
+                                            h->num_sms, st, pdl, early);
     if (r != -2) return r;
   }
   return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse, h->num_sms, st, pdl);
@@ -399,7 +401,7 @@ int csa_sparse_attn(csa_handle* h, const csa_batch* b, const int32_t* topk_idx,
   const bool pdl = use_pdl();
   Launches L;
   L.add(staged(h, kStageAttention, st, [&] {
-    return run_attention(h, b, db, topk_idx, topk_cnt, out, lse_out, st, pdl);
+    return run_attention(h, b, db, topk_idx, topk_cnt, out, lse_out, st, pdl, false);
   }));
   return finish(h, L);
 }
@@ -423,7 +425,7 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
                             cnt, h->ws.status, h->dc.max_vis, st, pdl);
   }));
   L.add(staged(h, kStageAttention, st, [&] {
-    return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl);
+    return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl, true);
   }));
   return finish(h, L);
 }

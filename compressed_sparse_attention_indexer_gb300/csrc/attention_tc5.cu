@@ -68,7 +68,12 @@ constexpr uint32_t kTmemS = 0, kTmemO = 256;
 
 struct __align__(16) A5Smem {
   uint64_t full[2], empty[2], mfull[2], mempty[2], s_full[2], s_empty[2];
-  uint64_t p_full, pv_done, o_full, o_empty, qfull, qdone, done;
+  // p_full per job buffer: with one barrier the softmax could complete two
+  // jobs' phases before the MMA thread polls the first, and a parity wait
+  // cannot tell phase n from phase n + 2; per buffer, job n + 2's phase needs
+  // job n's PV first
+  uint64_t p_full[2];
+  uint64_t pv_done, o_full, o_empty, qfull, qdone, done;
   uint32_t tmem_base;
   int abort;
   int flag[2][4];                  // per job parity and warp: some head needs a rescale
@@ -140,24 +145,30 @@ struct JobCtx {
   int nt[3];
 };
 
-__device__ __forceinline__ JobCtx job_ctx(const DevCfg& c, const DevBatch& b, int q,
-                                          const int* __restrict__ topk_cnt) {
+// The job's query plan and its stream lengths, from the caller's inputs
+// only; the compressed count (a Top-K output) is filled in by job_topk_cnt.
+__device__ __forceinline__ JobCtx job_ctx(const DevCfg& c, const DevBatch& b, int q) {
   JobCtx x;
   x.bi = q / b.S;
   x.p = query_plan(c, b.S, b.ctx_len[x.bi], q - x.bi * b.S, 0);
-  int cnt = 0;
-  if (!(x.p.flags & kPlanBad)) {
-    cnt = topk_cnt[q];
-    cnt = cnt < 0 ? 0 : (cnt > x.p.cnt ? x.p.cnt : cnt);
-  }
   x.n[0] = x.p.nwin;
-  x.n[1] = cnt;
+  x.n[1] = 0;
   x.n[2] = x.p.vis2;
   // tiles per stream from the bound min(vis, K), as the job list counts them
   x.nt[0] = (x.p.nwin + kTile - 1) / kTile;
   x.nt[1] = (x.p.cnt + kTile - 1) / kTile;
   x.nt[2] = (x.p.vis2 + kTile - 1) / kTile;
   return x;
+}
+
+// The compressed stream's length: the Top-K count, bounded by min(vis, K).
+__device__ __forceinline__ void job_topk_cnt(JobCtx& x, int q, const int* __restrict__ topk_cnt) {
+  int cnt = 0;
+  if (!(x.p.flags & kPlanBad)) {
+    cnt = topk_cnt[q];
+    cnt = cnt < 0 ? 0 : (cnt > x.p.cnt ? x.p.cnt : cnt);
+  }
+  x.n[1] = cnt;
 }
 
 __device__ __forceinline__ void job_stream(const JobCtx& x, int local, int& sid, int& t) {
@@ -168,25 +179,25 @@ __device__ __forceinline__ void job_stream(const JobCtx& x, int local, int& sid,
 
 // Pool row of stream row i of the job, or -1 (read as zeros by the gather and
 // masked by the softmax) when the row does not exist or is out of range.
-__device__ __forceinline__ int job_row(const DevCfg& c, const DevBatch& b, const JobCtx& x, int q,
-                                       int sid, int i, const int* __restrict__ topk_idx,
-                                       int* status) {
+// `j` is the row's Top-K index for the compressed stream (loaded by the
+// caller ahead of the count it is checked against).
+__device__ __forceinline__ int job_row(const DevBatch& b, const JobCtx& x, int sid, int i, int j,
+                                       int64_t off, int* status) {
   if (i >= x.n[sid]) return -1;
   int64_t gr;
   int64_t rows;
   if (sid == 0) {
-    gr = b.raw_off[x.bi] + (x.p.pos - x.p.nwin + 1 + i);
+    gr = off + (x.p.pos - x.p.nwin + 1 + i);
     rows = b.raw_rows;
   } else if (sid == 1) {
-    const int j = topk_idx[(int64_t)q * c.K + i];
     if (j < 0 || j >= x.p.vis) {
       set_status(status, kStatusBadIndex);
       return -1;
     }
-    gr = b.cmp_off[x.bi] + j;
+    gr = off + j;
     rows = b.cmp_rows;
   } else {
-    gr = b.hca_off[x.bi] + i;
+    gr = off + i;
     rows = b.hca_rows;
   }
   if (gr < 0 || gr >= rows) {
@@ -199,7 +210,8 @@ __device__ __forceinline__ int job_row(const DevCfg& c, const DevBatch& b, const
 __global__ void __launch_bounds__(kA5Threads, 1)
     attn_tile_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
-                     const int* __restrict__ topk_idx, const int* __restrict__ topk_cnt) {
+                     const int* __restrict__ topk_idx, const int* __restrict__ topk_cnt,
+                     int early) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ A5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -209,7 +221,14 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = b.B * b.S;
-  pdl_wait();
+  // Launched right after this library's Top-K kernel of the same step
+  // (early != 0), every input but the Top-K outputs was complete before the
+  // step's first kernel passed its own wait, so only the threads that read
+  // topk_idx / topk_cnt wait for the previous grid, and setup, Q and window
+  // rows overlap its tail.  Otherwise (a caller's kernel before this one, or
+  // a job list built on the device) every thread waits first.
+  const bool wait_all = !(early && jobs.host_B >= 0);
+  if (wait_all) pdl_wait();
   const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
   const int N = prefix[T];
   const int lo = (int)((int64_t)blockIdx.x * N / gridDim.x);
@@ -231,7 +250,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       tc5::mbar_init(smem_u32(&sm.s_full[g]), 1);
       tc5::mbar_init(smem_u32(&sm.s_empty[g]), 128);
     }
-    tc5::mbar_init(smem_u32(&sm.p_full), 128);
+    for (int g = 0; g < 2; ++g) tc5::mbar_init(smem_u32(&sm.p_full[g]), 128);
     tc5::mbar_init(smem_u32(&sm.pv_done), 1);
     tc5::mbar_init(smem_u32(&sm.o_full), 1);
     tc5::mbar_init(smem_u32(&sm.o_empty), 128);
@@ -257,17 +276,36 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     JobCursor cur;
     cur.init(prefix, T, lo);
     int m = 0;
+    bool waited = wait_all;
     for (int job = lo + g; job < hi && !*abort; job += 2, ++m) {
       cur.advance(job);
       const int q = cur.q;
-      const JobCtx x = job_ctx(c, b, q, topk_cnt);
+      JobCtx x = job_ctx(c, b, q);
       int sid, t;
       job_stream(x, job - cur.first, sid, t);
       const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(
           sid == 0 ? b.raw : (sid == 1 ? b.cmp : b.hca));
       const int64_t stride = sid == 0 ? b.raw_stride : (sid == 1 ? b.cmp_stride : b.hca_stride);
-      // this lane's rows and their pool addresses (read before waiting for
-      // the buffer, so that the index loads overlap the wait)
+      const int64_t off = sid == 0 ? b.raw_off[x.bi] : (sid == 1 ? b.cmp_off[x.bi] : b.hca_off[x.bi]);
+      // this lane's rows: their Top-K indices are loaded together with the
+      // count they are checked against (read before waiting for the buffer,
+      // so that the loads overlap the wait)
+      int jr[kQuadsPerWarp];
+#pragma unroll
+      for (int i = 0; i < kQuadsPerWarp; ++i) jr[i] = -1;
+      if (sid == 1) {
+        if (!waited) {
+          pdl_wait();
+          waited = true;
+        }
+#pragma unroll
+        for (int i = 0; i < kQuadsPerWarp; ++i) {
+          const int rq = lw + kLoadWarps * i;
+          const int ri = t * kTile + 4 * rq + (lane >> 3);
+          if (rq < kTile / 4 && ri < c.K) jr[i] = topk_idx[(int64_t)q * c.K + ri];
+        }
+        job_topk_cnt(x, q, topk_cnt);
+      }
       const __nv_bfloat16* src[kQuadsPerWarp];
       uint64_t bits = 0;
 #pragma unroll
@@ -275,7 +313,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         const int rq = lw + kLoadWarps * i;
         src[i] = nullptr;
         if (rq < kTile / 4) {
-          const int gr = job_row(c, b, x, q, sid, t * kTile + 4 * rq + (lane >> 3), topk_idx, ws.status);
+          const int gr = job_row(b, x, sid, t * kTile + 4 * rq + (lane >> 3), jr[i], off, ws.status);
           if (gr >= 0) src[i] = pool + (int64_t)gr * stride;
         }
         const uint32_t v = __ballot_sync(0xffffffffu, src[i] != nullptr);
@@ -341,7 +379,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
           const bool first = job == lo || job == pc.first;
           const bool last = job + 1 == hi || job + 1 == pc.end;
           if ((!first || seg == 0 || tc5::mbar_try_wait(smem_u32(&sm.o_empty), (seg - 1) & 1)) &&
-              tc5::mbar_try_wait(smem_u32(&sm.p_full), np & 1)) {
+              tc5::mbar_try_wait(smem_u32(&sm.p_full[np & 1]), (np >> 1) & 1)) {
             // O^T += V^T . P^T (overwrite at a segment's first job)
             tc5::fence_after_sync();
             const uint32_t vo = ((np & 1) * kBuf) >> 4;           // buffer offset, 16-byte units
@@ -523,7 +561,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         tc5::tmem_wait_st();
       }
       tc5::fence_before_sync();
-      tc5::mbar_arrive(smem_u32(&sm.p_full));
+      tc5::mbar_arrive(smem_u32(&sm.p_full[g]));
 
       if (last) {
         // segment epilogue: thread (warp, lane) owns dim 128cc + 32warp + lane
@@ -799,7 +837,7 @@ int max_jobs_per_query(const DevCfg& c) {
 // batch does not fit this path (the caller then uses the warp-MMA kernel).
 int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                          const ItemList& jobs, const int* topk_idx, const int* topk_cnt, void* out,
-                         float* lse_out, int num_sms, cudaStream_t st, bool pdl) {
+                         float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early) {
   const int T = b.B * b.S;
   if (T == 0) return 0;
   if (!ws.part_o || max_jobs_per_query(c) > kMergeMaxJobs || b.raw_rows > 0x7fffffffLL ||
@@ -820,7 +858,7 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
   int grid = num_sms;
   if (jobs.host_B >= 0 && jobs.prefix[T] < grid) grid = jobs.prefix[T] > 0 ? jobs.prefix[T] : 1;
   if (launch_kernel(attn_tile_kernel, dim3(grid), dim3(kA5Threads), kA5Dyn, st, pdl, qmap, jobs, c,
-                    b, ws, topk_idx, topk_cnt) < 0)
+                    b, ws, topk_idx, topk_cnt, (pdl && early) ? 1 : 0) < 0)
     return -1;
   ++n;
   if (launch_kernel(attn_merge_kernel, dim3(T, kTcV / kMergeDims), dim3(256), 0, st, pdl, jobs, c,

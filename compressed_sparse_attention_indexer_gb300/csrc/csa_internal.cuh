@@ -172,9 +172,11 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
                      cudaStream_t st, bool pdl);
+// early: launched right after this library's Top-K kernel of the same step,
+// so the tile kernel may read the caller's inputs before its grid wait.
 int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                          const ItemList& jobs, const int* topk_idx, const int* topk_cnt, void* out,
-                         float* lse_out, int num_sms, cudaStream_t st, bool pdl);
+                         float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early);
 void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, ItemList* jobs);
 int max_jobs_per_query(const DevCfg& c);
 constexpr int kAttnMma = 0, kAttnTc5 = 1;

@@ -286,6 +286,31 @@ def test_bitwise_deterministic():
     np.testing.assert_array_equal(g1["lse"], g2["lse"])
 
 
+def test_many_consecutive_steps_keep_a_clean_status():
+    # a few thousand back-to-back steps in the bench's launch configuration
+    # (PDL chaining, host lengths): a lost barrier phase or a race between
+    # consecutive kernels shows up as CSA_ERR_TIMEOUT or a changed output
+    wl = WORKLOADS["long_ragged_b64"]
+    hb = make_batch(wl)
+    db = to_device(hb, DEV)
+    cfg = wl.cfg
+    dec = csa.Decoder(cfg, hb["B"], 1, 65536)
+    lens_host = hb["ctx_len"].clone()  # kept alive while the struct points at it
+    cb = csa.make_batch_struct(db, lens_host)
+    out = torch.empty(hb["B"], 1, cfg.H, cfg.V, dtype=cfg.torch_dtype, device=DEV)
+    idx = torch.empty(hb["B"], 1, cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(hb["B"], 1, dtype=torch.int32, device=DEV)
+    dec.decode_step(cb, out, None, idx, cnt)
+    first = out.clone()
+    for i in range(2000):
+        dec.decode_step(cb, out, None, idx, cnt)
+        if i % 4 == 3:
+            dec.sparse_attn(cb, idx, cnt, out)
+    torch.cuda.synchronize()
+    assert dec.status() == csa.CSA_OK, csa.last_error()
+    assert torch.equal(out, first)
+
+
 def test_empty_batch_is_a_noop():
     wl = WORKLOADS["bypass_b16_l256"]
     hb = make_batch(wl, lens=[256])
