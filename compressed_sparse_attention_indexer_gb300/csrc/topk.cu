@@ -6,7 +6,10 @@
 // DSpark" (a staged sort that stops at 256 picks wrong keys past 256: the
 // selection here is exact at any width).
 //
-// One 1024-thread block per query.  Scores become order-preserving 32-bit
+// One 1024-thread block per query, in one of two kernels: topk_reg_kernel
+// (below) keeps a row of up to 16384 keys in registers and resolves the last
+// candidates by ranking them; topk_kernel, for longer rows, works as follows.
+// Scores become order-preserving 32-bit
 // keys in shared memory (-0.0 folded onto +0.0, NaN below every number).  The
 // bits above the highest bit on which the keys differ are skipped; then
 // radix-select passes of up to 11 bits each build a histogram of the next
@@ -178,20 +181,289 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if (tid == 0) cnt_out[q] = K;
 }
 
+// Register-resident variant for rows of at most kRegMax keys (the common
+// case: max_context / ratio <= 16384).  Thread t holds keys t + 1024 j,
+// j < 16, in registers for the whole selection.  The result is defined by a
+// threshold pair (tkey, tidx): the K-th entry in the order (key descending,
+// index ascending); a key is selected iff it precedes or is that entry.
+//   1. radix passes as above (histogram of the next digit among keys that
+//      match the prefix), until the digit's keys are exactly the ones needed
+//      (threshold = the digit's lowest key, any index) or few enough to rank
+//      directly;
+//   2. ranking: the <= 1024 candidates left are compacted into shared memory
+//      and each candidate's rank among them is counted by one thread; rank
+//      need - 1 is the threshold;
+//   3. keys all equal and more than 1024 of them straddle the threshold: the
+//      threshold index is the need-th of them in index order, from per-row
+//      ballots and one block scan;
+//   4. output: per (row j, warp) ballots of the selection, one block scan over
+//      the 512 counts in index order, and each selected key writes its index
+//      at its position, so the output is in ascending index order.
+constexpr int kRegKeys = 16;
+constexpr int kRegMax = kRegKeys * kTopkThreads;
+constexpr int kRows = kRegKeys * 32;  // (row j, warp) pairs, in index order
+constexpr int kCand = kTopkThreads;   // candidates ranked directly
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;\n" : "=r"(m));
+  return m;
+}
+
+__global__ void __launch_bounds__(kTopkThreads, 1)
+    topk_reg_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
+                    const int* __restrict__ n_override, int* __restrict__ idx_out,
+                    int* __restrict__ cnt_out, int* __restrict__ status, int max_vis) {
+  __shared__ int hist[kBins];
+  __shared__ uint32_t cand_key[kCand];
+  __shared__ int cand_idx[kCand];
+  __shared__ uint32_t rowbits[kRows];
+  __shared__ int rowbase[kRows];
+  __shared__ int scan_tmp[33];
+  __shared__ uint32_t warp_or[32], warp_and[32];
+  __shared__ uint32_t s_tkey;
+  __shared__ int s_bin, s_above, s_ncand, s_tidx;
+
+  const int K = c.K;
+  const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
+  int n;
+  bool do_select;
+  if (n_override) {
+    n = n_override[q];
+    if (n < 0 || n > max_vis || (int64_t)n > ld) {  // never read past the caller's row
+      if (tid == 0) set_status(status, kStatusBadIndex);
+      n = 0;
+    }
+  } else {
+    const int bi = q / b.S;
+    const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
+    if ((p.flags & kPlanBad) && tid == 0) set_status(status, kStatusBadIndex);
+    n = p.vis;
+  }
+  if (n > kRegMax) {  // the launcher picks this kernel only when max_vis <= kRegMax
+    if (tid == 0) set_status(status, kStatusBadIndex);
+    n = 0;
+  }
+  do_select = n > K;  // vis > K: scored; otherwise the bypass
+  int* out = idx_out + (int64_t)q * K;
+  if (!do_select) {  // bypass: every visible row
+    for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
+    if (tid == 0) cnt_out[q] = n < K ? n : K;
+    return;
+  }
+  const float* sc = scores + (int64_t)q * ld;
+  if (tid == 0) s_ncand = 0;
+  // keys in registers (all sixteen loads in flight), and the OR / AND over
+  // the row: bits where they differ are the ones still to decide
+  uint32_t k[kRegKeys];
+  uint32_t vmask = 0u, aor = 0u, aand = ~0u;
+  {
+    float v[kRegKeys];
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      const int i = j * kTopkThreads + tid;
+      v[j] = i < n ? __ldg(sc + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      k[j] = score_key(v[j]);
+      if (j * kTopkThreads + tid < n) {
+        vmask |= 1u << j;
+        aor |= k[j];
+        aand &= k[j];
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    aor |= __shfl_xor_sync(0xffffffffu, aor, o);
+    aand &= __shfl_xor_sync(0xffffffffu, aand, o);
+  }
+  if (lane == 0) {
+    warp_or[warp] = aor;
+    warp_and[warp] = aand;
+  }
+  __syncthreads();
+  aor = warp_or[lane];
+  aand = warp_and[lane];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    aor |= __shfl_xor_sync(0xffffffffu, aor, o);
+    aand &= __shfl_xor_sync(0xffffffffu, aand, o);
+  }
+  const uint32_t diff = aor & ~aand;
+
+  int start = diff ? 32 - __clz(diff) : 0;  // bits [start, 32) are common to all keys
+  uint32_t prefix = start < 32 ? (aor >> start) : 0u;
+  int need = K, in_bin = n;
+  uint32_t tkey = 0u;
+  int tidx = 0;
+  int mode = 0;  // 1: threshold known, 2: rank the candidates, 0: equal keys
+  while (start > 0) {
+    const int wbits = start < 11 ? start : 11;
+    const int sh = start - wbits;
+    const uint32_t mask = (1u << wbits) - 1u;
+    hist[tid] = 0;
+    hist[tid + kTopkThreads] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j)
+      if (((vmask >> j) & 1u) && (start >= 32 || (k[j] >> start) == prefix))
+        atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+    __syncthreads();
+    {  // the digit holding the need-th largest key (counts of higher bins)
+      const int b0 = 2 * tid, b1 = 2 * tid + 1;
+      const int h0 = hist[b0], h1 = hist[b1];
+      const int rv = h0 + h1;
+      int tot;
+      const int ex = block_exclusive_scan(rv, scan_tmp, &tot);
+      const int above_t = tot - ex - rv;  // keys in bins above this thread's pair
+      if (above_t < need && above_t + rv >= need) {
+        if (above_t + h1 >= need) {
+          s_bin = b1;
+          s_above = above_t;
+        } else {
+          s_bin = b0;
+          s_above = above_t + h1;
+        }
+      }
+    }
+    __syncthreads();
+    const int bin = s_bin;
+    need -= s_above;
+    prefix = (start >= 32 ? 0u : (prefix << wbits)) | (uint32_t)bin;
+    start = sh;
+    in_bin = hist[bin];
+    if (in_bin == need) {  // every key of the digit is kept
+      tkey = prefix << start;
+      tidx = 0x7fffffff;
+      mode = 1;
+      break;
+    }
+    if (in_bin <= kCand) {
+      mode = 2;
+      break;
+    }
+    __syncthreads();  // hist and s_bin are rewritten by the next pass
+  }
+  if (mode == 0 && in_bin <= kCand) mode = 2;
+
+  if (mode == 2) {
+    // compact the keys that match the prefix, then rank each among them
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      const bool m = ((vmask >> j) & 1u) && (k[j] >> start) == prefix;  // start < 32 here
+      const uint32_t bal = __ballot_sync(0xffffffffu, m);
+      if (bal) {
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&s_ncand, __popc(bal));
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int slot = base + __popc(bal & lanemask_lt());
+        if (m && slot < kCand) {
+          cand_key[slot] = k[j];
+          cand_idx[slot] = j * kTopkThreads + tid;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < in_bin) {
+      const uint32_t kk = cand_key[tid];
+      const int ii = cand_idx[tid];
+      int rank = 0;
+      for (int x = 0; x < in_bin; ++x) {
+        const uint32_t kx = cand_key[x];
+        rank += (kx > kk) || (kx == kk && cand_idx[x] < ii);
+      }
+      if (rank == need - 1) {
+        s_tkey = kk;
+        s_tidx = ii;
+      }
+    }
+    __syncthreads();
+    tkey = s_tkey;
+    tidx = s_tidx;
+  } else if (mode == 0) {
+    // start == 0: more than kCand keys equal `prefix` and `need` of them are
+    // kept, the lowest indices first
+#pragma unroll
+    for (int j = 0; j < kRegKeys; ++j) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, ((vmask >> j) & 1u) && k[j] == prefix);
+      if (lane == 0) rowbits[j * 32 + warp] = bal;
+    }
+    __syncthreads();
+    const int cv = tid < kRows ? __popc(rowbits[tid]) : 0;
+    int tot;
+    const int ex = block_exclusive_scan(cv, scan_tmp, &tot);
+    if (tid < kRows && ex < need && ex + cv >= need) {
+      uint32_t bits = rowbits[tid];
+      for (int r = ex + 1; r < need; ++r) bits &= bits - 1u;  // drop the lower set bits
+      s_tidx = (tid >> 5) * kTopkThreads + (tid & 31) * 32 + (__ffs(bits) - 1);
+    }
+    __syncthreads();
+    tkey = prefix;
+    tidx = s_tidx;
+  }
+
+  // selection: keys before the threshold in (key desc, index asc) order
+#pragma unroll
+  for (int j = 0; j < kRegKeys; ++j) {
+    const int i = j * kTopkThreads + tid;
+    const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
+    const uint32_t bal = __ballot_sync(0xffffffffu, sel);
+    if (lane == 0) rowbits[j * 32 + warp] = bal;
+  }
+  __syncthreads();
+  {
+    const int cv = tid < kRows ? __popc(rowbits[tid]) : 0;
+    int tot;
+    const int ex = block_exclusive_scan(cv, scan_tmp, &tot);
+    if (tid < kRows) rowbase[tid] = ex;
+  }
+  __syncthreads();
+  const uint32_t lt = lanemask_lt();
+#pragma unroll
+  for (int j = 0; j < kRegKeys; ++j) {
+    const int i = j * kTopkThreads + tid;
+    const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
+    if (sel) {
+      const int e = j * 32 + warp;
+      const int pos = rowbase[e] + __popc(rowbits[e] & lt);
+      if (pos < K) out[pos] = i;
+    }
+  }
+  if (tid == 0) cnt_out[q] = K;
+}
+
 }  // namespace
+
+// The register kernel when every row fits it (CSA_TOPK=radix keeps the
+// shared-memory kernel, its measured baseline).
+bool topk_use_reg(int max_vis) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* e = getenv("CSA_TOPK");
+    forced = (e && e[0] == 'r') ? 1 : 0;
+  }
+  return !forced && max_vis <= kRegMax;
+}
 
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
                 cudaStream_t st, bool pdl) {
   if (nq == 0) return 0;
+  DevBatch none = {};
+  none.S = 1;
+  if (topk_use_reg(max_vis))
+    return launch_kernel(topk_reg_kernel, dim3(nq), dim3(kTopkThreads), 0, st, pdl, c,
+                         b ? *b : none, scores, ld, n_override, idx_out, cnt_out, status, max_vis);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
   static int attr_smem = 0;
   if (smem > 48 * 1024 && smem > attr_smem) {
     cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attr_smem = smem;
   }
-  DevBatch none = {};
-  none.S = 1;
   return launch_kernel(topk_kernel, dim3(nq), dim3(kTopkThreads), smem, st, pdl, c, b ? *b : none,
                        scores, ld, n_override, idx_out, cnt_out, status, max_vis);
 }

@@ -169,6 +169,10 @@ def _topk_cases(rng):
     cases.append(("neg_and_inf", np.concatenate([-np.abs(rng.standard_normal(900)).astype(np.float32),
                                                  np.full(3, -np.inf, np.float32)])))
     cases.append(("narrow_band", (100.0 + rng.standard_normal(16384) * 1e-4).astype(np.float32)))
+    # two values: the K-th key is one of > 1024 equal keys (ties by index after
+    # the radix passes), once after a higher group and once as the top group
+    cases.append(("high_then_equal", np.concatenate([np.full(300, 5.0), np.full(4000, 1.0)]).astype(np.float32)))
+    cases.append(("two_values", np.where(rng.random(16384) < 0.5, 1.0, 2.0).astype(np.float32)))
     return cases
 
 
@@ -193,6 +197,33 @@ def test_topk_select_bit_exact():
         assert gc[i] == ref.size, name
         assert gi[i, :ref.size].tolist() == ref.tolist(), f"{name} n={s.size}"
         assert (gi[i, ref.size:] == -1).all()
+
+
+def test_topk_select_bit_exact_rows_past_16384():
+    # max_context / ratio above 16384: the shared-memory Top-K kernel
+    rng = np.random.default_rng(2025)
+    cfg = BF16_CFG
+    cases = []
+    for n in (16385, 20000, 32768):
+        cases.append(("normal", rng.standard_normal(n).astype(np.float32)))
+        cases.append(("ties", (np.round(rng.standard_normal(n) * 4) / 4).astype(np.float32)))
+    cases.append(("all_equal", np.full(17000, -3.0, np.float32)))
+    dec = csa.Decoder(cfg, len(cases), 1, 131072)
+    ld = 32768
+    sc = np.full((len(cases), ld), np.nan, np.float32)
+    n = np.zeros(len(cases), np.int32)
+    for i, (_, s) in enumerate(cases):
+        sc[i, :s.size] = s
+        n[i] = s.size
+    idx = torch.empty(len(cases), cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(len(cases), dtype=torch.int32, device=DEV)
+    dec.topk_select(torch.from_numpy(sc).to(DEV), torch.from_numpy(n).to(DEV), idx, cnt)
+    assert dec.status() == csa.CSA_OK
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    for i, (name, s) in enumerate(cases):
+        ref = oracle.topk(s.astype(np.float64), cfg.topk)
+        assert gc[i] == ref.size, name
+        assert gi[i].tolist() == ref.tolist(), f"{name} n={s.size}"
 
 
 # ---------------------------------------------------------------------------

@@ -3,7 +3,9 @@
 CSA_INDEXER=mma selects the warp-MMA indexer (the measured baseline of the
 tcgen05 one); CSA_ATTN=mma selects the warp-MMA attention kernel (the
 measured baseline of the tcgen05 tile kernel + merge);
-CSA_PDL=0 launches without programmatic dependent launch.  All are read once
+CSA_TOPK=radix selects the shared-memory Top-K kernel (the measured baseline
+of the register one); CSA_PDL=0 launches without programmatic dependent
+launch.  All are read once
 per process, so each variant runs in a child process.
 """
 import os
@@ -46,7 +48,7 @@ print("variant ok")
 
 @pytest.mark.parametrize("env", [{"CSA_INDEXER": "mma"}, {"CSA_PDL": "0"},
                                  {"CSA_INDEXER": "mma", "CSA_PDL": "0"}, {"CSA_ATTN": "mma"},
-                                 {"CSA_ATTN": "mma", "CSA_PDL": "0"}])
+                                 {"CSA_ATTN": "mma", "CSA_PDL": "0"}, {"CSA_TOPK": "radix"}])
 def test_variant_parity(env):
     import torch
     if not torch.cuda.is_available():
