@@ -634,8 +634,11 @@ __global__ void __launch_bounds__(256, 4)
   __shared__ int seg[kMergeMaxJobs + 1];
   __shared__ int nseg_s;
   __shared__ float2 rope[kRopeTable];  // cos, sin of the block's rotary pairs
-  pdl_wait();
-  pdl_trigger();
+  // The segment list and the rotary table need only the job list and the
+  // lengths, which are complete before the tile kernel lets this grid
+  // launch (the tile kernel waits for the job-list kernel before it
+  // triggers, and for the caller's inputs before it or its predecessor
+  // does); only the partials wait for the tile grid.
   const int q = blockIdx.x, dg = blockIdx.y, t = threadIdx.x;
   const int T = b.B * b.S;
   const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
@@ -681,6 +684,8 @@ __global__ void __launch_bounds__(256, 4)
     nseg_s = k;
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
   const int nseg = min(nseg_s, kMergeMaxJobs);
   const int h = t >> 2;
   const int v0 = dg * kMergeDims + 16 * (t & 3);
