@@ -382,9 +382,10 @@ int csa_indexer_topk(csa_handle* h, const csa_batch* b, int32_t* topk_idx, int32
   const bool pdl = use_pdl();
   Launches L;
   run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
+  const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr,
-                            topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st, pdl);
+                            topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st, pdl, early);
   }));
   return finish(h, L);
 }
@@ -420,9 +421,10 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
   const bool pdl = use_pdl();
   Launches L;
   run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
+  const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr, idx,
-                            cnt, h->ws.status, h->dc.max_vis, st, pdl);
+                            cnt, h->ws.status, h->dc.max_vis, st, pdl, early);
   }));
   L.add(staged(h, kStageAttention, st, [&] {
     return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl, true);
@@ -456,7 +458,7 @@ int csa_topk_select(csa_handle* h, int32_t nq, const float* scores, int64_t ld, 
   Launches L;
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, nullptr, nq, scores, ld, n, topk_idx, topk_cnt, h->ws.status,
-                            h->dc.max_vis, st, pdl);
+                            h->dc.max_vis, st, pdl, false);
   }));
   return finish(h, L);
 }
@@ -529,8 +531,9 @@ int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* 
   const bool pdl = use_pdl();
   Launches L;
   run_indexer(&h, b, db, 0, w.scores, w.scores_ld, st, L);
+  const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(csa::launch_topk(h.dc, &db, b->B * b->S, w.scores, w.scores_ld, nullptr, topk_idx, topk_cnt,
-                         w.status, h.dc.max_vis, st, pdl));
+                         w.status, h.dc.max_vis, st, pdl, early));
   rc = finish(&h, L);
   if (rc) return rc;
   if (status_out) {

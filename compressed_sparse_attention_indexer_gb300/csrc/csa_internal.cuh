@@ -166,9 +166,11 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
                        int num_sms, cudaStream_t st, bool pdl);
+// early: this library's own kernel of the same call runs right before (the
+// lengths are then read before the grid dependency wait)
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st, bool pdl);
+                cudaStream_t st, bool pdl, bool early);
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
                      cudaStream_t st, bool pdl);

@@ -213,7 +213,8 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 __global__ void __launch_bounds__(kTopkThreads, 1)
     topk_reg_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
                     const int* __restrict__ n_override, int* __restrict__ idx_out,
-                    int* __restrict__ cnt_out, int* __restrict__ status, int max_vis) {
+                    int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
+                    int early) {
   __shared__ int hist[kBins];
   __shared__ uint32_t cand_key[kCand];
   __shared__ int cand_idx[kCand];
@@ -226,9 +227,21 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 
   const int K = c.K;
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // The row length from the plan.  Launched right after this library's own
+  // kernel of the same call (early != 0), which waits for its predecessor
+  // before it lets this grid launch, the lengths (the caller's inputs) are
+  // complete already, so only the scores wait.
+  int n = 0;
+  bool bad = false;
+  auto plan_len = [&] {
+    const int bi = q / b.S;
+    const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
+    bad = p.flags & kPlanBad;
+    n = p.vis;
+  };
+  if (!n_override && early) plan_len();
   pdl_wait();
   pdl_trigger();
-  int n;
   bool do_select;
   if (n_override) {
     n = n_override[q];
@@ -237,10 +250,8 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       n = 0;
     }
   } else {
-    const int bi = q / b.S;
-    const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
-    if ((p.flags & kPlanBad) && tid == 0) set_status(status, kStatusBadIndex);
-    n = p.vis;
+    if (!early) plan_len();
+    if (bad && tid == 0) set_status(status, kStatusBadIndex);
   }
   if (n > kRegMax) {  // the launcher picks this kernel only when max_vis <= kRegMax
     if (tid == 0) set_status(status, kStatusBadIndex);
@@ -451,13 +462,14 @@ bool topk_use_reg(int max_vis) {
 
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st, bool pdl) {
+                cudaStream_t st, bool pdl, bool early) {
   if (nq == 0) return 0;
   DevBatch none = {};
   none.S = 1;
   if (topk_use_reg(max_vis))
     return launch_kernel(topk_reg_kernel, dim3(nq), dim3(kTopkThreads), 0, st, pdl, c,
-                         b ? *b : none, scores, ld, n_override, idx_out, cnt_out, status, max_vis);
+                         b ? *b : none, scores, ld, n_override, idx_out, cnt_out, status, max_vis,
+                         (pdl && early) ? 1 : 0);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
   static int attr_smem = 0;
   if (smem > 48 * 1024 && smem > attr_smem) {
