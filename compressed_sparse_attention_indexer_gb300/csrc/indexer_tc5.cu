@@ -96,22 +96,8 @@ __global__ void __launch_bounds__(kT5Threads, 1)
   float* w_sm = reinterpret_cast<float*>(smem_raw + (qbuf + (uint32_t)NQB * qbytes - smem_u32(smem_raw)));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  pdl_wait();
-  const int* __restrict__ prefix = items.host_B >= 0 ? items.prefix : ws.item_prefix;
-  const int N = prefix[b.B];
-  const int lo = (int)((int64_t)blockIdx.x * N / gridDim.x);
-  const int hi = (int)((int64_t)(blockIdx.x + 1) * N / gridDim.x);
-  pdl_trigger();
-  if (lo >= hi) return;
-
-  const int G = S < kMaxG ? S : kMaxG;
-  const int ngroups = (S + G - 1) / G;
-  volatile int* abort = &sm.abort;
-
-  if (warp == 5) {
-    tc5::tmem_alloc(smem_u32(&sm.tmem_base), tmem_cols);
-    tc5::tmem_relinquish();
-  }
+  // barrier setup and the tensor-map prefetch need nothing from the previous
+  // grid, so they overlap its tail
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       tc5::mbar_init(smem_u32(&sm.full[i]), 1);
@@ -129,6 +115,26 @@ __global__ void __launch_bounds__(kT5Threads, 1)
     sm.abort = 0;
     tc5::fence_mbar_init();
   }
+  if (warp == 4 && lane == 0) {
+    tc5::prefetch_tmap(&kmap);
+    tc5::prefetch_tmap(&qmap);
+  }
+  pdl_wait();
+  const int* __restrict__ prefix = items.host_B >= 0 ? items.prefix : ws.item_prefix;
+  const int N = prefix[b.B];
+  const int lo = (int)((int64_t)blockIdx.x * N / gridDim.x);
+  const int hi = (int)((int64_t)(blockIdx.x + 1) * N / gridDim.x);
+  pdl_trigger();
+  if (lo >= hi) return;
+
+  const int G = S < kMaxG ? S : kMaxG;
+  const int ngroups = (S + G - 1) / G;
+  volatile int* abort = &sm.abort;
+
+  if (warp == 5) {
+    tc5::tmem_alloc(smem_u32(&sm.tmem_base), tmem_cols);
+    tc5::tmem_relinquish();
+  }
   tc5::fence_before_sync();
   __syncthreads();
   tc5::fence_after_sync();
@@ -137,8 +143,6 @@ __global__ void __launch_bounds__(kT5Threads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tc5::prefetch_tmap(&kmap);
-      tc5::prefetch_tmap(&qmap);
       int kc = 0, qc = 0;
       ReqCursor cur;
       cur.init(prefix, b.B, lo);

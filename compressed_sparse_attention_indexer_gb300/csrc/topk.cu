@@ -36,6 +36,16 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// The same order-preserving key in fewer instructions: adding +0.0 turns
+// -0.0 into +0.0 (IEEE round to nearest), then negative values have every
+// bit flipped and the others only the sign bit; NaN is 0.
+__device__ __forceinline__ uint32_t score_key_fast(float f) {
+  const float g = f + 0.f;
+  uint32_t u = __float_as_uint(g);
+  u ^= (uint32_t)((int32_t)u >> 31) | 0x80000000u;
+  return g != g ? 0u : u;
+}
+
 // Key i lives at keys[kpad(i)]: one pad word per 16 keys, so the final pass
 // (thread t reads keys 16t .. 16t+15) hits 32 different banks.
 __device__ __forceinline__ int kpad(int i) { return i + (i >> 4); }
@@ -279,7 +289,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     }
 #pragma unroll
     for (int j = 0; j < kRegKeys; ++j) {
-      k[j] = score_key(v[j]);
+      k[j] = score_key_fast(v[j]);
       if (j * kTopkThreads + tid < n) {
         vmask |= 1u << j;
         aor |= k[j];
@@ -312,17 +322,22 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   uint32_t tkey = 0u;
   int tidx = 0;
   int mode = 0;  // 1: threshold known, 2: rank the candidates, 0: equal keys
-  while (start > 0) {
+  for (bool first_pass = true; start > 0; first_pass = false) {
     const int wbits = start < 11 ? start : 11;
     const int sh = start - wbits;
     const uint32_t mask = (1u << wbits) - 1u;
     hist[tid] = 0;
     hist[tid + kTopkThreads] = 0;
     __syncthreads();
+    if (first_pass) {  // every key shares the common prefix
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j)
-      if (((vmask >> j) & 1u) && (start >= 32 || (k[j] >> start) == prefix))
-        atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+      for (int j = 0; j < kRegKeys; ++j)
+        if ((vmask >> j) & 1u) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+    } else {  // start < 32 after a pass
+#pragma unroll
+      for (int j = 0; j < kRegKeys; ++j)
+        if (((vmask >> j) & 1u) && (k[j] >> start) == prefix) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+    }
     __syncthreads();
     {  // the digit holding the need-th largest key (counts of higher bins)
       const int b0 = 2 * tid, b1 = 2 * tid + 1;
@@ -418,10 +433,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   }
 
   // selection: keys before the threshold in (key desc, index asc) order
+  uint32_t smask = 0u;
 #pragma unroll
   for (int j = 0; j < kRegKeys; ++j) {
     const int i = j * kTopkThreads + tid;
     const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
+    smask |= (uint32_t)sel << j;
     const uint32_t bal = __ballot_sync(0xffffffffu, sel);
     if (lane == 0) rowbits[j * 32 + warp] = bal;
   }
@@ -434,15 +451,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   }
   __syncthreads();
   const uint32_t lt = lanemask_lt();
-#pragma unroll
-  for (int j = 0; j < kRegKeys; ++j) {
-    const int i = j * kTopkThreads + tid;
-    const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
-    if (sel) {
-      const int e = j * 32 + warp;
-      const int pos = rowbase[e] + __popc(rowbits[e] & lt);
-      if (pos < K) out[pos] = i;
-    }
+  while (smask) {  // this thread's selected keys (few: K of n)
+    const int j = __ffs(smask) - 1;
+    smask &= smask - 1u;
+    const int e = j * 32 + warp;
+    const int pos = rowbase[e] + __popc(rowbits[e] & lt);
+    if (pos < K) out[pos] = j * kTopkThreads + tid;
   }
   if (tid == 0) cnt_out[q] = K;
 }
