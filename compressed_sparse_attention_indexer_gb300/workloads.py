@@ -21,6 +21,11 @@ Pool layout (the storage contract of the library):
     (``raw_off[b]`` may therefore be negative).
   ``gap_rows`` rows filled with NaN separate requests in every pool, so a read
   of a row a query may not use poisons its output.
+
+With ``idx_dtype="fp8"`` the indexer-key pool is stored as FP8 E4M3 codes
+(uint8) with one fp32 scale per row (``idx_scale``): each row is drawn like
+the bf16 rows (the same fp32 normal draws), its scale is max|row| / 448 and
+its codes are row / scale rounded to E4M3 by torch's float8_e4m3fn cast.
 """
 from __future__ import annotations
 
@@ -43,6 +48,7 @@ class CsaConfig:
     win: int = 128         # sliding window WIN
     hca_ratio: int = 0     # heavy-compression ratio (0 = no third stream)
     dtype: str = "bf16"    # "bf16" or "f32"
+    idx_dtype: str = "same"  # indexer-key pool: "same" (the layer dtype) or "fp8" (E4M3 + row scale)
     rope_base: float = 10000.0
     scale: float | None = None  # softmax scale; None -> 1/sqrt(D)
 
@@ -109,6 +115,11 @@ WORKLOADS = {
         "long_ragged_b64", BF16_CFG, B=64, S=1, L_range=(1024, 65536), seed=1003,
         description="B=64 S=1, L_b ~ U{1024..65536}: 256..16384 compressed rows per request, "
                     "K=512, WIN=128, H=64, D=576, indexer 64x128, bf16"),
+    "long_ragged_b64_fp8idx": Workload(
+        "long_ragged_b64_fp8idx", replace(BF16_CFG, idx_dtype="fp8"), B=64, S=1,
+        L_range=(1024, 65536), seed=1003,
+        description="long_ragged_b64 (same lengths and draws) with the indexer keys stored as "
+                    "FP8 E4M3 codes and one fp32 scale per row"),
     "multitoken_hca_b16_s8": Workload(
         "multitoken_hca_b16_s8", replace(BF16_CFG, hca_ratio=128), B=16, S=8, L=32768, seed=1004,
         description="B=16 S=8 L=32768 with per-query causal visibility; CSA (ratio 4, K=512, "
@@ -146,6 +157,17 @@ def _pool(gen, counts, width, std, dtype, gap_rows, first=None):
     return pool, off
 
 
+def _fp8_pool(gen, counts, width, std, gap_rows):
+    """Indexer-key pool as FP8 E4M3 codes (uint8 [rows, width]) and a per-row
+    fp32 scale: rows drawn as in _pool (NaN gap rows give NaN codes and scales)."""
+    keys, off = _pool(gen, counts, width, std, torch.float32, gap_rows)
+    amax = keys.abs().amax(dim=1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (keys / scale[:, None]).clamp(-448.0, 448.0)
+    codes = torch.where(keys.isnan(), keys, codes)
+    return codes.to(torch.float8_e4m3fn).view(torch.uint8).contiguous(), off, scale.contiguous()
+
+
 def make_batch(wl: Workload, lens=None, seed: int | None = None, gap_rows: int = 0,
                raw_keep: int | None = None, dists: Dists | None = None) -> dict:
     """Host (CPU) tensors for one batch of `wl`.
@@ -173,11 +195,15 @@ def make_batch(wl: Workload, lens=None, seed: int | None = None, gap_rows: int =
     raw_kv, raw_off = _pool(gen, [L - f for L, f in zip(Ls, first)], cfg.D, d.raw, dt, gap_rows, first)
     ncmp = [L // cfg.ratio for L in Ls]
     cmp_kv, cmp_off = _pool(gen, ncmp, cfg.D, d.cmp, dt, gap_rows)
-    idx_k, idx_off = _pool(gen, ncmp, cfg.Di, d.k_idx, dt, gap_rows)
+    idx_scale = None
+    if cfg.idx_dtype == "fp8":
+        idx_k, idx_off, idx_scale = _fp8_pool(gen, ncmp, cfg.Di, d.k_idx, gap_rows)
+    else:
+        idx_k, idx_off = _pool(gen, ncmp, cfg.Di, d.k_idx, dt, gap_rows)
     batch = dict(B=B, S=S, ctx_len=ctx, q=q, q_idx=q_idx, w=w,
                  raw_kv=raw_kv, raw_off=raw_off, raw_stride=cfg.D, raw_first=first,
                  cmp_kv=cmp_kv, cmp_off=cmp_off, cmp_stride=cfg.D,
-                 idx_k=idx_k, idx_off=idx_off, idx_stride=cfg.Di,
+                 idx_k=idx_k, idx_off=idx_off, idx_stride=cfg.Di, idx_scale=idx_scale,
                  hca_kv=None, hca_off=None, hca_stride=0)
     if cfg.hca_ratio:
         nh = [L // cfg.hca_ratio for L in Ls]
@@ -187,7 +213,7 @@ def make_batch(wl: Workload, lens=None, seed: int | None = None, gap_rows: int =
 
 
 TENSOR_KEYS = ("ctx_len", "q", "q_idx", "w", "raw_kv", "raw_off", "cmp_kv", "cmp_off",
-               "idx_k", "idx_off", "hca_kv", "hca_off")
+               "idx_k", "idx_off", "idx_scale", "hca_kv", "hca_off")
 
 
 def to_device(batch: dict, device) -> dict:

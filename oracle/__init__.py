@@ -26,14 +26,14 @@ _LIB_PATH = os.path.join(_BUILD, f"libcsa_oracle_{platform.machine()}.so")
 _lib = None
 _lock = threading.Lock()
 
-ORC_F32, ORC_BF16 = 0, 1
+ORC_F32, ORC_BF16, ORC_FP8_E4M3 = 0, 1, 2
 FORCE_SCORE = 1
 
 
 class OrcCfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in
                 ("H", "D", "V", "Hi", "Di", "ratio", "topk", "win", "hca_ratio", "dtype")] + [
-        ("scale", ctypes.c_double), ("rope_base", ctypes.c_double)]
+        ("scale", ctypes.c_double), ("rope_base", ctypes.c_double), ("idx_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -45,7 +45,8 @@ class OrcBatch(ctypes.Structure):
                 ("raw", _P), ("raw_off", _P), ("raw_stride", ctypes.c_int64),
                 ("cmp", _P), ("cmp_off", _P), ("cmp_stride", ctypes.c_int64),
                 ("idx", _P), ("idx_off", _P), ("idx_stride", ctypes.c_int64),
-                ("hca", _P), ("hca_off", _P), ("hca_stride", ctypes.c_int64)]
+                ("hca", _P), ("hca_off", _P), ("hca_stride", ctypes.c_int64),
+                ("idx_scale", _P)]
 
 
 class OrcQueryInfo(ctypes.Structure):
@@ -83,6 +84,8 @@ def lib():
             _lib.orc_query_scores.argtypes = [ctypes.POINTER(OrcCfg), ctypes.POINTER(OrcBatch),
                                               i32, i32, d]
             _lib.orc_query_scores.restype = i32
+            _lib.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            _lib.orc_e4m3_to_double.restype = ctypes.c_double
     return _lib
 
 
@@ -154,7 +157,8 @@ def make_cfg(cfg) -> OrcCfg:
     return OrcCfg(H=cfg.H, D=cfg.D, V=cfg.V, Hi=cfg.Hi, Di=cfg.Di, ratio=cfg.ratio,
                   topk=cfg.topk, win=cfg.win, hca_ratio=cfg.hca_ratio,
                   dtype=ORC_BF16 if cfg.dtype == "bf16" else ORC_F32,
-                  scale=cfg.softmax_scale, rope_base=cfg.rope_base)
+                  scale=cfg.softmax_scale, rope_base=cfg.rope_base,
+                  idx_dtype=ORC_FP8_E4M3 if getattr(cfg, "idx_dtype", "") == "fp8" else 0)
 
 
 class _HostBatch:
@@ -180,7 +184,8 @@ class _HostBatch:
             cmp=keep("cmp_kv"), cmp_off=keep("cmp_off", np.int64), cmp_stride=int(batch["cmp_stride"]),
             idx=keep("idx_k"), idx_off=keep("idx_off", np.int64), idx_stride=int(batch["idx_stride"]),
             hca=keep("hca_kv"), hca_off=keep("hca_off", np.int64),
-            hca_stride=int(batch.get("hca_stride", 0) or 0))
+            hca_stride=int(batch.get("hca_stride", 0) or 0),
+            idx_scale=keep("idx_scale", np.float32))
 
 
 def decode(cfg, batch: dict, qids=None, nthreads: int | None = None, force_score: bool = False):
@@ -209,6 +214,11 @@ def decode(cfg, batch: dict, qids=None, nthreads: int | None = None, force_score
     for f in ("pos", "vis", "nwin", "cnt", "vis2", "rows_used"):
         res[f] = np.array([getattr(info[i], f) for i in range(nq)], np.int64)
     return res
+
+
+def e4m3_value(byte: int) -> float:
+    """The value of one OCP FP8 E4M3 byte (as the indexer-key pool stores it)."""
+    return float(lib().orc_e4m3_to_double(int(byte) & 0xFF))
 
 
 def query_scores(cfg, batch: dict, b: int, s: int) -> np.ndarray:

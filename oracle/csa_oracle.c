@@ -37,6 +37,12 @@
  *  output dims [V-R, V) with interleaved pairs, theta_i = base^(-2i/R),
  *  rotation by -pos*theta_i; HCA = every ratio-r2 row visible, no Top-K.
  *
+ * Quantised indexer keys ("Fix: complete DeepSeek V4 TP CSA decode", PR
+ * description: the indexer cache is a key pool plus a per-row scale pool):
+ * with idx_dtype ORC_FP8_E4M3 a key element is one OCP FP8 E4M3 byte and the
+ * key row is scale[row] times the decoded bytes; the score formula is
+ * unchanged.  The element format is a reading (the pages name no format).
+ *
  * Parity pins live in the tests; every function below is pinned there.
  */
 #include <math.h>
@@ -47,12 +53,14 @@
 
 #define ORC_F32 0
 #define ORC_BF16 1
+#define ORC_FP8_E4M3 2
 
 typedef struct {
     int32_t H, D, V, Hi, Di;
     int32_t ratio, topk, win, hca_ratio; /* hca_ratio 0 = no HCA stream */
     int32_t dtype;                       /* ORC_F32 or ORC_BF16 */
     double scale, rope_base;
+    int32_t idx_dtype;                   /* 0: keys in dtype; ORC_FP8_E4M3: bytes + row scale */
 } orc_cfg;
 
 /* Host copies of one batch.  Pool row r of request b sits at
@@ -67,6 +75,7 @@ typedef struct {
     const void *cmp;   const int64_t *cmp_off; int64_t cmp_stride;
     const void *idx;   const int64_t *idx_off; int64_t idx_stride;
     const void *hca;   const int64_t *hca_off; int64_t hca_stride;
+    const float *idx_scale; /* [rows] scale of each FP8 key row */
 } orc_batch;
 
 /* ------------------------------------------------------------------ */
@@ -93,6 +102,35 @@ static void orc_load_vec(const void *base, int32_t dtype, int64_t first,
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = orc_load(base, dtype, first + i);
+}
+
+/* OCP FP8 E4M3 (the "fn" variant): bit 7 sign, bits 6..3 exponent e with
+ * bias 7, bits 2..0 mantissa m.  e = 0: subnormal, m/8 * 2^(1-7); e = 15 and
+ * m = 7: NaN (there is no infinity); otherwise (1 + m/8) * 2^(e-7). */
+double orc_e4m3_to_double(uint8_t v)
+{
+    const int sign = v >> 7, e = (v >> 3) & 15, m = v & 7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, 1 - 7);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Indexer key row `row` of the pool (absolute row index). */
+static void orc_load_key_row(const orc_cfg *c, const orc_batch *bt, int64_t row, double *dst)
+{
+    if (c->idx_dtype == ORC_FP8_E4M3) {
+        const uint8_t *p = (const uint8_t *)bt->idx + row * bt->idx_stride;
+        const double sc = (double)bt->idx_scale[row];
+        for (int32_t d = 0; d < c->Di; ++d)
+            dst[d] = sc * orc_e4m3_to_double(p[d]);
+    } else {
+        orc_load_vec(bt->idx, c->dtype, row * bt->idx_stride, c->Di, dst);
+    }
 }
 
 /* ------------------------------------------------------------------ */
@@ -250,8 +288,7 @@ int orc_query(const orc_cfg *c, const orc_batch *bt, int32_t b, int32_t s,
         orc_load_vec(bt->q_idx, c->dtype, qid * Hi * Di, (int64_t)Hi * Di, qi);
         for (int32_t h = 0; h < Hi; ++h) wv[h] = (double)bt->w[qid * Hi + h];
         for (int32_t j = 0; j < vis; ++j)
-            orc_load_vec(bt->idx, c->dtype, (bt->idx_off[b] + j) * bt->idx_stride,
-                         Di, kr + (int64_t)j * Di);
+            orc_load_key_row(c, bt, bt->idx_off[b] + j, kr + (int64_t)j * Di);
         orc_index_scores(Hi, Di, qi, wv, vis, kr, sc);
         cnt = orc_topk(sc, vis, K, idx);
         free(qi); free(wv); free(kr); free(sc);
@@ -308,8 +345,7 @@ int32_t orc_query_scores(const orc_cfg *c, const orc_batch *bt, int32_t b,
     orc_load_vec(bt->q_idx, c->dtype, qid * Hi * Di, (int64_t)Hi * Di, qi);
     for (int32_t h = 0; h < Hi; ++h) wv[h] = (double)bt->w[qid * Hi + h];
     for (int32_t j = 0; j < vis; ++j)
-        orc_load_vec(bt->idx, c->dtype, (bt->idx_off[b] + j) * bt->idx_stride, Di,
-                     kr + (int64_t)j * Di);
+        orc_load_key_row(c, bt, bt->idx_off[b] + j, kr + (int64_t)j * Di);
     orc_index_scores(Hi, Di, qi, wv, vis, kr, scores);
     free(qi); free(wv); free(kr);
     return vis;
