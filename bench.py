@@ -94,10 +94,13 @@ def step_bytes(cfg, lens, S, topk_idx=None):
     Per query: q (H*D*e), output (H*V*e); per request, counted once: the
     window rows and selected compressed rows it reads (union over its
     queries), the indexer keys it scores and q_idx/w of scored queries, and
-    the heavy-compression rows.  topk_idx [B*S, K] (numpy) gives the selected
+    the heavy-compression rows (FP8 keys: Di bytes + a 4-byte scale per row).
+    topk_idx [B*S, K] (numpy) gives the selected
     rows; without it every query is assumed to read min(vis, K) rows.
     """
     e = cfg.esize
+    fp8 = getattr(cfg, "idx_dtype", "same") == "fp8"
+    key_row = cfg.Di + 4 if fp8 else cfg.Di * e  # FP8 keys: one byte per dim + the row scale
     tot_q = tot_rows = idx_b = 0
     for b, L in enumerate(lens):
         win_rows, sel, hca_rows, krows = set(), set(), 0, 0
@@ -116,7 +119,7 @@ def step_bytes(cfg, lens, S, topk_idx=None):
                 idx_b += cfg.Hi * cfg.Di * e + 4 * cfg.Hi
             if cfg.hca_ratio:
                 hca_rows = max(hca_rows, (pos + 1) // cfg.hca_ratio)
-        idx_b += krows * cfg.Di * e
+        idx_b += krows * key_row
         tot_rows += len(win_rows) + len(sel) + hca_rows
         tot_q += S
     attn_b = tot_q * (cfg.H * cfg.D * e + cfg.H * cfg.V * e) + tot_rows * cfg.D * e

@@ -15,7 +15,7 @@ from . import build as _build
 
 CSA_OK, CSA_ERR_INVALID_ARG, CSA_ERR_UNSUPPORTED, CSA_ERR_WORKSPACE = 0, 1, 2, 3
 CSA_ERR_CUDA, CSA_ERR_BAD_INDEX, CSA_ERR_TIMEOUT = 4, 5, 6
-CSA_DTYPE_F32, CSA_DTYPE_BF16 = 0, 1
+CSA_DTYPE_F32, CSA_DTYPE_BF16, CSA_DTYPE_FP8_E4M3 = 0, 1, 2
 ERROR_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 3: "CSA_ERR_WORKSPACE",
                4: "CSA_ERR_CUDA", 5: "CSA_ERR_BAD_INDEX", 6: "CSA_ERR_TIMEOUT"}
 
@@ -38,7 +38,7 @@ class CConfig(ctypes.Structure):
                  "hca_ratio", "dtype")] + [
         ("softmax_scale", ctypes.c_float), ("rope_base", ctypes.c_float),
         ("max_batch", ctypes.c_int32), ("max_queries_per_req", ctypes.c_int32),
-        ("max_context", ctypes.c_int32)]
+        ("max_context", ctypes.c_int32), ("idx_dtype", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -51,7 +51,8 @@ class CBatch(ctypes.Structure):
                 ("raw_kv", _P), ("raw_off", _P), ("raw_stride", _I64), ("raw_rows", _I64),
                 ("cmp_kv", _P), ("cmp_off", _P), ("cmp_stride", _I64), ("cmp_rows", _I64),
                 ("idx_k", _P), ("idx_off", _P), ("idx_stride", _I64), ("idx_rows", _I64),
-                ("hca_kv", _P), ("hca_off", _P), ("hca_stride", _I64), ("hca_rows", _I64)]
+                ("hca_kv", _P), ("hca_off", _P), ("hca_stride", _I64), ("hca_rows", _I64),
+                ("idx_scale", _P)]
 
 
 _lib = None
@@ -115,7 +116,8 @@ def make_config(cfg, max_batch: int, max_queries: int, max_context: int) -> CCon
                    ratio=cfg.ratio, topk=cfg.topk, win=cfg.win, hca_ratio=cfg.hca_ratio,
                    dtype=CSA_DTYPE_BF16 if cfg.dtype == "bf16" else CSA_DTYPE_F32,
                    softmax_scale=cfg.softmax_scale, rope_base=cfg.rope_base,
-                   max_batch=max_batch, max_queries_per_req=max_queries, max_context=max_context)
+                   max_batch=max_batch, max_queries_per_req=max_queries, max_context=max_context,
+                   idx_dtype=CSA_DTYPE_FP8_E4M3 if getattr(cfg, "idx_dtype", "") == "fp8" else 0)
 
 
 def _ptr(t) -> int | None:
@@ -140,7 +142,8 @@ def make_batch_struct(batch: dict, ctx_len_host=None) -> CBatch:
         idx_k=_ptr(batch["idx_k"]), idx_off=_ptr(batch["idx_off"]),
         idx_stride=int(batch["idx_stride"]), idx_rows=rows(batch["idx_k"]),
         hca_kv=_ptr(batch.get("hca_kv")), hca_off=_ptr(batch.get("hca_off")),
-        hca_stride=int(batch.get("hca_stride") or 0), hca_rows=rows(batch.get("hca_kv")))
+        hca_stride=int(batch.get("hca_stride") or 0), hca_rows=rows(batch.get("hca_kv")),
+        idx_scale=_ptr(batch.get("idx_scale")))
 
 
 def check_batch(cconfig: CConfig, cbatch: CBatch) -> int:

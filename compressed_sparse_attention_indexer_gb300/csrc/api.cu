@@ -93,6 +93,12 @@ int validate_cfg(const csa_config* c) {
     return fail(CSA_ERR_INVALID_ARG, "need ratio, topk, win >= 1 and hca_ratio >= 0");
   if (c->dtype != CSA_DTYPE_F32 && c->dtype != CSA_DTYPE_BF16)
     return fail(CSA_ERR_UNSUPPORTED, "dtype must be CSA_DTYPE_F32 or CSA_DTYPE_BF16");
+  if (c->idx_dtype != 0 && c->idx_dtype != CSA_DTYPE_FP8_E4M3)
+    return fail(CSA_ERR_UNSUPPORTED, "idx_dtype must be 0 (the layer dtype) or CSA_DTYPE_FP8_E4M3");
+  if (c->idx_dtype == CSA_DTYPE_FP8_E4M3 &&
+      (c->dtype != CSA_DTYPE_BF16 || c->idx_heads != csa::kTcHi || c->idx_dim != csa::kTcDi))
+    return fail(CSA_ERR_UNSUPPORTED, "FP8 indexer keys need dtype bf16, idx_heads %d, idx_dim %d",
+                csa::kTcHi, csa::kTcDi);
   if (c->max_batch < 1 || c->max_queries_per_req < 1 || c->max_context < 1)
     return fail(CSA_ERR_INVALID_ARG, "workspace maxima must be >= 1");
   if (c->max_context / c->ratio > kMaxVisCap)
@@ -116,6 +122,7 @@ int validate_batch_cfg(const csa_config& c, const csa_batch* b) {
                 c.max_batch, c.max_queries_per_req);
   if (b->B == 0) return CSA_OK;
   const int es = c.dtype == CSA_DTYPE_BF16 ? 2 : 4;
+  const bool fp8 = c.idx_dtype == CSA_DTYPE_FP8_E4M3;
   struct P { const void* p; const char* n; } ptrs[] = {
       {b->ctx_len, "ctx_len"}, {b->q, "q"}, {b->q_idx, "q_idx"}, {b->w, "w"},
       {b->raw_kv, "raw_kv"}, {b->raw_off, "raw_off"}, {b->cmp_kv, "cmp_kv"},
@@ -133,10 +140,12 @@ int validate_batch_cfg(const csa_config& c, const csa_batch* b) {
     const Pool& x = pools[i];
     if (i == 3 && c.hca_ratio == 0) continue;
     if (x.stride < x.width) return fail(CSA_ERR_INVALID_ARG, "%s_stride below the row width", x.n);
-    if ((x.stride * es) % 16 != 0)
+    if ((x.stride * (i == 2 && fp8 ? 1 : es)) % 16 != 0)
       return fail(CSA_ERR_INVALID_ARG, "%s_stride * element size is not a multiple of 16", x.n);
     if (x.rows < 0) return fail(CSA_ERR_INVALID_ARG, "%s_rows < 0", x.n);
   }
+  if (fp8 && (!b->idx_scale || !aligned16(b->idx_scale)))
+    return fail(CSA_ERR_INVALID_ARG, "idx_scale is NULL or not 16-byte aligned with FP8 keys");
   if (c.hca_ratio > 0) {
     if (!b->hca_kv || !b->hca_off) return fail(CSA_ERR_INVALID_ARG, "hca_kv/hca_off NULL with hca_ratio > 0");
     if (!aligned16(b->hca_kv) || !aligned16(b->hca_off))
@@ -165,6 +174,7 @@ csa::DevBatch dev_batch(const csa_batch* b) {
   d.raw = b->raw_kv; d.raw_off = b->raw_off; d.raw_stride = b->raw_stride; d.raw_rows = b->raw_rows;
   d.cmp = b->cmp_kv; d.cmp_off = b->cmp_off; d.cmp_stride = b->cmp_stride; d.cmp_rows = b->cmp_rows;
   d.idx = b->idx_k; d.idx_off = b->idx_off; d.idx_stride = b->idx_stride; d.idx_rows = b->idx_rows;
+  d.idx_scale = b->idx_scale;
   d.hca = b->hca_kv; d.hca_off = b->hca_off; d.hca_stride = b->hca_stride; d.hca_rows = b->hca_rows;
   return d;
 }
@@ -271,6 +281,7 @@ csa::DevCfg static_devcfg(const csa_config& c) {
   d.H = c.heads; d.D = c.row_dim; d.V = c.v_dim; d.R = c.row_dim - c.v_dim;
   d.Hi = c.idx_heads; d.Di = c.idx_dim; d.ratio = c.ratio; d.K = c.topk;
   d.win = c.win; d.hca_ratio = c.hca_ratio; d.dtype = c.dtype;
+  d.idx_fp8 = c.idx_dtype == CSA_DTYPE_FP8_E4M3;
   d.scale = c.softmax_scale > 0.f ? c.softmax_scale : (float)(1.0 / sqrt((double)c.row_dim));
   d.rope_base = c.rope_base;
   d.max_context = c.max_context;
@@ -312,6 +323,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   d.H = cfg->heads; d.D = cfg->row_dim; d.V = cfg->v_dim; d.R = cfg->row_dim - cfg->v_dim;
   d.Hi = cfg->idx_heads; d.Di = cfg->idx_dim; d.ratio = cfg->ratio; d.K = cfg->topk;
   d.win = cfg->win; d.hca_ratio = cfg->hca_ratio; d.dtype = cfg->dtype;
+  d.idx_fp8 = cfg->idx_dtype == CSA_DTYPE_FP8_E4M3;
   d.scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : (float)(1.0 / sqrt((double)cfg->row_dim));
   d.rope_base = cfg->rope_base;
   d.max_context = cfg->max_context;

@@ -26,6 +26,7 @@ constexpr int kRopeTable = 32;  // rotary frequencies kept in the config (R <= 6
 
 struct DevCfg {
   int H, D, V, R, Hi, Di, ratio, K, win, hca_ratio, dtype;
+  int idx_fp8;  // indexer keys are FP8 E4M3 rows with a per-row fp32 scale
   float scale, rope_base;
   int max_context, max_vis;
   double rope_theta[kRopeTable];  // base^(-2i/R), i < min(R/2, kRopeTable), set on the host
@@ -55,6 +56,7 @@ struct DevBatch {
   const void* raw; const int64_t* raw_off; int64_t raw_stride, raw_rows;
   const void* cmp; const int64_t* cmp_off; int64_t cmp_stride, cmp_rows;
   const void* idx; const int64_t* idx_off; int64_t idx_stride, idx_rows;
+  const float* idx_scale;  // [idx_rows] when the keys are FP8
   const void* hca; const int64_t* hca_off; int64_t hca_stride, hca_rows;
 };
 

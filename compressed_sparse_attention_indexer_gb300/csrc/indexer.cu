@@ -268,6 +268,10 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
                    bool pdl) {
   const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;  // items, if known
   if (known == 0) return 0;
+  if (c.idx_fp8) {  // FP8 keys: the tcgen05 kernel only (its shape is checked at create)
+    const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, st, pdl);
+    return r == -2 ? -1 : r;
+  }
   if (tensor_core_shape(c) && indexer_impl() == kIndexerTc5) {
     const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, st, pdl);
     if (r != -2) return r;  // -2: shape outside the tcgen05 kernel, use warp MMA

@@ -36,16 +36,42 @@ namespace csa {
 namespace {
 
 constexpr int kT5Threads = 192;
+constexpr int kConvThreads = 256;               // FP8: eight converter warps, two per key row
+constexpr int kT5ThreadsFp8 = kT5Threads + kConvThreads;
 constexpr int kSubBytes = kIdxChunk * 64 * 2;   // 128 rows x 64 dims bf16 = 16 KB
 constexpr int kStageBytes = 2 * kSubBytes;      // 32 KB: one item of keys
+constexpr int kStage8Bytes = kIdxChunk * kTcDi; // 16 KB: one item of FP8 keys
+constexpr int kConvBufs = 2;                    // FP8: converted (bf16) items in flight
 constexpr int kQSubBytes = kTcHi * 64 * 2;      // 64 heads x 64 dims = 8 KB
 constexpr int kMaxG = 4;                        // queries per MMA group
 
 struct T5Smem {
   uint64_t full[8], empty[8], qfull[2], qempty[2], tfull[8], tempty[8], done;
+  uint64_t cfull[kConvBufs], cempty[kConvBufs];  // FP8 keys: converted items
   uint32_t tmem_base;
   int abort;
 };
+
+// Sixteen FP8 E4M3 keys (one 16-byte chunk) to sixteen bf16, exactly: every
+// E4M3 value (subnormals included, NaN stays NaN) is an f16 value, every f16
+// value an f32 value, and every such value a bf16 value.  Byte 2i of the
+// chunk is dim 2i; each pair is E4M3x2 -> f16x2 -> two f32 -> one bf16x2.
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 in, uint32_t out[8]) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const uint16_t pair = (uint16_t)(w[i] >> (16 * half));
+      uint32_t o;
+      asm("{\n .reg .b32 h2;\n .reg .b16 a, b;\n .reg .f32 fa, fb;\n"
+          " cvt.rn.f16x2.e4m3x2 h2, %1;\n mov.b32 {a, b}, h2;\n"
+          " cvt.f32.f16 fa, a;\n cvt.f32.f16 fb, b;\n cvt.rn.bf16x2.f32 %0, fb, fa;\n}\n"
+          : "=r"(o) : "h"(pair));
+      out[2 * i + half] = o;
+    }
+  }
+}
 
 // Walks the work list in item order: the request owning the current item and
 // its item range, re-read only when the request changes (the single-thread
@@ -77,22 +103,29 @@ struct ReqCursor {
   }
 };
 
-__global__ void __launch_bounds__(kT5Threads, 1)
+// kFp8: the key pool holds FP8 E4M3 rows with a per-row fp32 scale
+// (b.idx_scale).  Warps 6-13 then convert each item's FP8 tile (one TMA box)
+// into the bf16 tile layout the MMA reads, and the epilogue multiplies each
+// row's dot products by its scale before the ReLU.
+template <bool kFp8>
+__global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     indexer_tc5_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
                        int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
-                       int acc_cols, int NB) {
+                       int acc_cols, int NB, int NCB) {
   // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
   // MMAs run up to NB jobs ahead of the epilogue
   const uint32_t tmem_cols = (uint32_t)(NB * acc_cols);
   extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 below
   __shared__ T5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t kbuf = base;                                  // NST x 32 KB
+  const uint32_t kbuf = base;                                  // NST x 32 KB (FP8: 16 KB)
+  const uint32_t stage_bytes = kFp8 ? kStage8Bytes : kStageBytes;
+  const uint32_t cbuf = kbuf + (uint32_t)NST * stage_bytes;    // FP8: converted items
   const int S = b.S;
   const uint32_t qbytes = (uint32_t)S * 2u * kQSubBytes;       // one request's q_idx
-  const uint32_t qbuf = kbuf + (uint32_t)NST * kStageBytes;    // NQB x qbytes
+  const uint32_t qbuf = cbuf + (kFp8 ? (uint32_t)NCB * kStageBytes : 0u);  // NQB x qbytes
   float* w_sm = reinterpret_cast<float*>(smem_raw + (qbuf + (uint32_t)NQB * qbytes - smem_u32(smem_raw)));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -101,7 +134,11 @@ __global__ void __launch_bounds__(kT5Threads, 1)
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       tc5::mbar_init(smem_u32(&sm.full[i]), 1);
-      tc5::mbar_init(smem_u32(&sm.empty[i]), 1);
+      tc5::mbar_init(smem_u32(&sm.empty[i]), kFp8 ? kConvThreads : 1);  // FP8: the converters free a stage
+    }
+    for (int i = 0; i < NCB; ++i) {
+      tc5::mbar_init(smem_u32(&sm.cfull[i]), kConvThreads);
+      tc5::mbar_init(smem_u32(&sm.cempty[i]), 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc5::mbar_init(smem_u32(&sm.qfull[i]), 1);
@@ -164,9 +201,13 @@ __global__ void __launch_bounds__(kT5Threads, 1)
         if (kc >= NST && !tc5::mbar_wait(smem_u32(&sm.empty[st]), ((kc / NST) - 1) & 1, abort))
           break;
         const int y = (int)(off + (int64_t)(it - cur.first) * kIdxChunk);
-        tc5::mbar_expect_tx(smem_u32(&sm.full[st]), kStageBytes);
-        tc5::tma_load_2d(kbuf + st * kStageBytes, &kmap, 0, y, smem_u32(&sm.full[st]));
-        tc5::tma_load_2d(kbuf + st * kStageBytes + kSubBytes, &kmap, 64, y, smem_u32(&sm.full[st]));
+        tc5::mbar_expect_tx(smem_u32(&sm.full[st]), stage_bytes);
+        if (kFp8) {  // one box: 128 rows x 128 FP8 keys
+          tc5::tma_load_2d(kbuf + st * stage_bytes, &kmap, 0, y, smem_u32(&sm.full[st]));
+        } else {
+          tc5::tma_load_2d(kbuf + st * kStageBytes, &kmap, 0, y, smem_u32(&sm.full[st]));
+          tc5::tma_load_2d(kbuf + st * kStageBytes + kSubBytes, &kmap, 64, y, smem_u32(&sm.full[st]));
+        }
         ++kc;
       }
       // let every copy this thread started land before the block exits
@@ -188,9 +229,14 @@ __global__ void __launch_bounds__(kT5Threads, 1)
           ++qc;
         }
         const int st = kc % NST;
-        if (!tc5::mbar_wait(smem_u32(&sm.full[st]), (kc / NST) & 1, abort)) break;
+        const int cb = kc % NCB;
+        if (kFp8) {
+          if (!tc5::mbar_wait(smem_u32(&sm.cfull[cb]), (kc / NCB) & 1, abort)) break;
+        } else {
+          if (!tc5::mbar_wait(smem_u32(&sm.full[st]), (kc / NST) & 1, abort)) break;
+        }
         tc5::fence_after_sync();
-        const uint32_t ka = kbuf + st * kStageBytes;
+        const uint32_t ka = kFp8 ? cbuf + cb * kStageBytes : kbuf + st * kStageBytes;
         const uint32_t qa = qbuf + ((qc - 1) % NQB) * qbytes;
         bool ok = true;
         for (int g = 0; g < ngroups; ++g) {
@@ -214,14 +260,45 @@ __global__ void __launch_bounds__(kT5Threads, 1)
           ++job;
         }
         if (!ok) break;
-        tc5::mma_commit(smem_u32(&sm.empty[st]));
+        tc5::mma_commit(smem_u32(kFp8 ? &sm.cempty[cb] : &sm.empty[st]));
         ++kc;
       }
       // every MMA issued above has finished before TMEM is freed
       tc5::mma_commit(smem_u32(&sm.done));
       tc5::mbar_wait_drain(smem_u32(&sm.done), 0);
     }
-  } else {
+  } else if (kFp8 && warp >= 6) {
+    // ------------------------------------------------------------ converters (FP8 keys)
+    // two threads per key row r of each item: half hf converts dims
+    // 64 hf .. 64 hf + 63, four 16-byte FP8 chunks of the TMA tile (128-byte
+    // swizzle: chunk c at (c ^ (r & 7))), into bf16 sub-tile hf of a
+    // converted buffer (the same swizzle); then each thread frees the stage
+    // and publishes the buffer to the MMA issuer
+    const int r = ((warp - 6) & 3) * 32 + lane, hf = (warp - 6) >> 2;
+    int kc = 0;
+    for (int it = lo; it < hi && !*abort; ++it, ++kc) {
+      const int st = kc % NST, cb = kc % NCB;
+      if (!tc5::mbar_wait(smem_u32(&sm.full[st]), (kc / NST) & 1, abort)) break;
+      if (kc >= NCB && !tc5::mbar_wait(smem_u32(&sm.cempty[cb]), ((kc / NCB) - 1) & 1, abort))
+        break;
+      const uint8_t* src = smem_raw + (kbuf + st * kStage8Bytes - smem_u32(smem_raw)) + r * 128;
+      uint8_t* dst = smem_raw + (cbuf + cb * kStageBytes - smem_u32(smem_raw)) + r * 128;
+#pragma unroll
+      for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+        uint32_t o[8];
+        e4m3x16_to_bf16(v, o);
+        // dims 16c .. 16c+15: sub-tile c / 4, bf16 chunks 2(c % 4) and 2(c % 4) + 1
+        uint8_t* sub = dst + (c >> 2) * kSubBytes;
+        const int c0 = 2 * (c & 3);
+        *reinterpret_cast<uint4*>(sub + ((c0 ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4*>(sub + (((c0 + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+      }
+      tc5::fence_proxy_async_smem();  // the MMA reads the tile through the async proxy
+      tc5::mbar_arrive(smem_u32(&sm.empty[st]));
+      tc5::mbar_arrive(smem_u32(&sm.cfull[cb]));
+    }
+  } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;  // TMEM lane = key row within the item
     int job = 0;
@@ -242,6 +319,10 @@ __global__ void __launch_bounds__(kT5Threads, 1)
       const int c0 = (it - cur.first) * kIdxChunk;
       const int64_t gr = off + c0 + row;
       const bool in_pool = gr >= 0 && gr < b.idx_rows;
+      // FP8: the row's scale (loaded ahead of the accumulator wait); only rows
+      // the query may read are used
+      float ks = 1.f;
+      if (kFp8 && in_pool && c0 + row < L / c.ratio) ks = __ldg(b.idx_scale + gr);
       bool ok = true;
       for (int g = 0; g < ngroups; ++g) {
         const int gn = min(G, S - g * G);
@@ -269,10 +350,17 @@ __global__ void __launch_bounds__(kT5Threads, 1)
             for (int i = 0; i < 4; ++i) {
               const float4 wv = w4[k * 4 + i];
               const int h = k * 16 + i * 4;
-              acc = fmaf(wv.x, fmaxf(v[h], 0.f), acc);
-              acc = fmaf(wv.y, fmaxf(v[h + 1], 0.f), acc);
-              acc = fmaf(wv.z, fmaxf(v[h + 2], 0.f), acc);
-              acc = fmaf(wv.w, fmaxf(v[h + 3], 0.f), acc);
+              if (kFp8) {
+                acc = fmaf(wv.x, fmaxf(v[h] * ks, 0.f), acc);
+                acc = fmaf(wv.y, fmaxf(v[h + 1] * ks, 0.f), acc);
+                acc = fmaf(wv.z, fmaxf(v[h + 2] * ks, 0.f), acc);
+                acc = fmaf(wv.w, fmaxf(v[h + 3] * ks, 0.f), acc);
+              } else {
+                acc = fmaf(wv.x, fmaxf(v[h], 0.f), acc);
+                acc = fmaf(wv.y, fmaxf(v[h + 1], 0.f), acc);
+                acc = fmaf(wv.z, fmaxf(v[h + 2], 0.f), acc);
+                acc = fmaf(wv.w, fmaxf(v[h + 3], 0.f), acc);
+              }
             }
             part[k] = acc;
           }
@@ -311,19 +399,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 tensor [rows, cols] with a row stride in elements; boxes of
-// [box_rows, 64] (64 bf16 = one 128-byte swizzle row).
+// 2D tensor [rows, cols] with a row stride in elements; boxes of
+// [box_rows, 128 bytes] (one 128-byte swizzle row): 64 bf16 or 128 FP8.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t stride,
-              uint32_t box_rows) {
+              uint32_t box_rows, bool fp8 = false) {
   auto fn = encode_fn();
   if (!fn) return false;
+  const uint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {stride * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {stride * es};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -353,7 +443,10 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
     forced_ctas = f ? atoi(f) : 0;
     if (forced_ctas < 0 || forced_ctas > 4) forced_ctas = 0;
   }
-  const int ctas_per_sm = forced_ctas ? forced_ctas : (S <= 2 ? 2 : 1);
+  // FP8 keys: one CTA per SM (the converted buffers leave no room for a
+  // second CTA's ring)
+  const bool fp8 = c.idx_fp8 != 0;
+  const int ctas_per_sm = forced_ctas ? forced_ctas : ((S <= 2 && !fp8) ? 2 : 1);
   const int G = S < 4 ? S : 4;
   int acc_cols = 32;
   while (acc_cols < 64 * G) acc_cols <<= 1;  // power of two >= 32
@@ -364,28 +457,40 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   // key stages first: a CTA spans few requests, so a second q_idx buffer
   // (prefetching the next request's queries) is kept only when it costs no
   // key stage
-  const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
+  const int stage_bytes = fp8 ? kStage8Bytes : kStageBytes;
+  // FP8: two converted items (measured: a third adds nothing)
+  const int NCB = fp8 ? kConvBufs : 0;
+  const int conv_bytes = NCB * kStageBytes;
+  const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4 - conv_bytes;
   auto stages = [&](int nqb) {
-    const int n = (budget - nqb * qbytes) / kStageBytes;
+    const int n = (budget - nqb * qbytes) / stage_bytes;
     return n > max_stages ? max_stages : n;
   };
   const int NQB = stages(2) >= stages(1) ? 2 : 1;
   const int NST = stages(NQB);
   if (NST < 2) return -2;
+  if (fp8 && !b.idx_scale) return -1;
   CUtensorMap kmap, qmap;
-  if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk)) return -1;
+  if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk, fp8))
+    return -1;
   if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
-  const int smem = 1024 + NST * kStageBytes + NQB * qbytes + S * kTcHi * 4;
+  const int smem = 1024 + NST * stage_bytes + conv_bytes + NQB * qbytes + S * kTcHi * 4;
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(indexer_tc5_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(indexer_tc5_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         227 * 1024 - (int)sizeof(T5Smem));
+    cudaFuncSetAttribute(indexer_tc5_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          227 * 1024 - (int)sizeof(T5Smem));
     attr = true;
   }
   int grid = num_sms * ctas_per_sm;
   if (known > 0 && known < grid) grid = known;
-  return launch_kernel(indexer_tc5_kernel, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap, qmap,
-                       items, c, b, ws, score_all, scores, ld, NST, NQB, acc_cols, NB);
+  if (fp8)
+    return launch_kernel(indexer_tc5_kernel<true>, dim3(grid), dim3(kT5ThreadsFp8), smem, st, pdl,
+                         kmap, qmap, items, c, b, ws, score_all, scores, ld, NST, NQB, acc_cols, NB,
+                         NCB);
+  return launch_kernel(indexer_tc5_kernel<false>, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap,
+                       qmap, items, c, b, ws, score_all, scores, ld, NST, NQB, acc_cols, NB, 0);
 }
 
 }  // namespace csa

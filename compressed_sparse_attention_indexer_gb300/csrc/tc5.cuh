@@ -70,6 +70,12 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (a tcgen05.mma operand, a TMA store).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
 // Bounded wait that ignores the abort flag: used while winding down, to let
 // copies and MMAs already started finish before the block exits.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {

@@ -63,7 +63,7 @@
 extern "C" {
 #endif
 
-#define CSA_ABI_VERSION 1
+#define CSA_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define CSA_API __attribute__((visibility("default")))
@@ -82,7 +82,7 @@ enum {
     CSA_ERR_TIMEOUT = 6      /* device-side: a bounded wait gave up                   */
 };
 
-enum { CSA_DTYPE_F32 = 0, CSA_DTYPE_BF16 = 1 };
+enum { CSA_DTYPE_F32 = 0, CSA_DTYPE_BF16 = 1, CSA_DTYPE_FP8_E4M3 = 2 };
 
 /* Static shape of one attention layer; fixed at csa_decode_create. */
 typedef struct {
@@ -101,6 +101,18 @@ typedef struct {
     int32_t max_batch;   /* workspace bound on B                               */
     int32_t max_queries_per_req; /* workspace bound on S                       */
     int32_t max_context; /* workspace bound on every L_b                       */
+    /* Storage of the indexer key pool (idx_k): 0 = the layer dtype, or
+     * CSA_DTYPE_FP8_E4M3 = one byte per key element (OCP FP8 E4M3: 1 sign,
+     * 4 exponent bits with bias 7, 3 mantissa bits, subnormals, no
+     * infinities, NaN = S.1111.111) with one fp32 scale per pool row, the
+     * key being idx_scale[row] * e4m3(byte).  The pages pass the indexer
+     * cache as a key pool plus a per-row scale pool ("Fix: complete DeepSeek
+     * V4 TP CSA decode", PR description: idx_kv_cache and idx_kv_scale); the
+     * element format is this library's choice.  FP8 keys need dtype bf16,
+     * idx_heads 64 and idx_dim 128 (the tcgen05 indexer), else
+     * CSA_ERR_UNSUPPORTED.  The score is unchanged:
+     * score_j = sum_h w_h * ReLU(q_idx[h] . key_j). */
+    int32_t idx_dtype;
 } csa_config;
 
 /* One batch.  All pointers: caller-owned device memory. */
@@ -118,6 +130,9 @@ typedef struct {
     const void *cmp_kv;  const int64_t *cmp_off; int64_t cmp_stride; int64_t cmp_rows; /* ratio rows, width D */
     const void *idx_k;   const int64_t *idx_off; int64_t idx_stride; int64_t idx_rows; /* indexer keys, width Di */
     const void *hca_kv;  const int64_t *hca_off; int64_t hca_stride; int64_t hca_rows; /* heavy rows, width D; NULL if off */
+    const float *idx_scale;   /* [idx_rows] per-row scale of FP8 indexer keys (16-byte
+                                 aligned); required with idx_dtype FP8, else ignored.
+                                 idx_stride is then in bytes (a multiple of 16). */
 } csa_batch;
 
 typedef struct csa_handle csa_handle;
