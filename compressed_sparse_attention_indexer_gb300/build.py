@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build", platform.machine())
 LIB_PATH = os.path.join(HERE, "_build", f"libcsa_{platform.machine()}.so")
-SOURCES = ["api.cu", "plan.cu", "indexer.cu", "indexer_tc5.cu", "topk.cu", "attention.cu", "attention_tc5.cu"]
+SOURCES = ["api.cu", "plan.cu", "indexer.cu", "indexer_tc5.cu", "topk.cu", "attention.cu", "attention_tc5.cu",
+           "writeback.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

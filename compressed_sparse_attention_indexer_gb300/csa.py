@@ -22,7 +22,7 @@ ERROR_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 
 EXPORTS = ("csa_decode_create", "csa_decode_destroy", "csa_indexer_topk", "csa_sparse_attn",
            "csa_decode_step", "csa_indexer_scores", "csa_topk_select", "csa_check_batch",
            "csa_get_status", "csa_last_error", "csa_last_launch_count", "csa_abi_version",
-           "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static")
+           "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static", "csa_cache_writeback")
 STAGES = ("plan", "indexer", "topk", "attention")
 
 
@@ -93,9 +93,12 @@ def lib(path: str | None = None):
             L.csa_profile_read.argtypes = [H, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)]
             L.csa_indexer_topk_static.argtypes = [ctypes.POINTER(CConfig), ctypes.POINTER(CBatch), vp,
                                                   vp, vp, vp]
+            L.csa_cache_writeback.argtypes = [vp, ctypes.c_int64, vp, i32, vp, ctypes.c_int64,
+                                              ctypes.c_int64, ctypes.c_int64, vp, vp]
             for name in ("csa_decode_create", "csa_indexer_topk", "csa_sparse_attn", "csa_decode_step",
                          "csa_indexer_scores", "csa_topk_select", "csa_check_batch", "csa_get_status",
-                         "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static"):
+                         "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static",
+                         "csa_cache_writeback"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -156,6 +159,19 @@ def indexer_topk_static(cconfig: CConfig, cb: CBatch, topk_idx, topk_cnt, status
     library's static device array; see csa_indexer_topk_static in csa.h)."""
     _check(lib().csa_indexer_topk_static(ctypes.byref(cconfig), ctypes.byref(cb), _ptr(topk_idx),
                                          _ptr(topk_cnt), _ptr(status), _stream(stream)))
+
+
+def cache_writeback(rows, slot, pool, status=None, stream=None):
+    """pool[slot[t]] = rows[t] on the device (see csa_cache_writeback in csa.h).
+
+    rows [n, ...] and pool [pool_rows, ...]: device tensors whose rows are
+    contiguous and of the same byte size; slot [n] int64 (negative = skip)."""
+    n = int(rows.shape[0])
+    row_bytes = rows[0].numel() * rows.element_size() if n else 0
+    assert n == 0 or pool[0].numel() * pool.element_size() == row_bytes, "row sizes differ"
+    _check(lib().csa_cache_writeback(_ptr(rows), int(rows.stride(0)) * rows.element_size(), _ptr(slot),
+                                     n, _ptr(pool), int(pool.stride(0)) * pool.element_size(),
+                                     int(pool.shape[0]), int(row_bytes), _ptr(status), _stream(stream)))
 
 
 def _stream(stream) -> int | None:

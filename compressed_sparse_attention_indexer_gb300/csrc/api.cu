@@ -555,6 +555,22 @@ int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* 
   return CSA_OK;
 }
 
+int csa_cache_writeback(const void* rows, int64_t rows_stride, const int64_t* slot, int32_t n,
+                        void* pool, int64_t pool_stride, int64_t pool_rows, int64_t row_bytes,
+                        int32_t* status, void* stream) {
+  if (n < 0) return fail(CSA_ERR_INVALID_ARG, "n < 0");
+  if (row_bytes < 0 || pool_rows < 0) return fail(CSA_ERR_INVALID_ARG, "negative row_bytes or pool_rows");
+  if (n == 0 || row_bytes == 0) { g_err.clear(); return CSA_OK; }
+  if (!rows || !slot || !pool) return fail(CSA_ERR_INVALID_ARG, "rows/slot/pool NULL");
+  if (rows_stride < row_bytes || pool_stride < row_bytes)
+    return fail(CSA_ERR_INVALID_ARG, "a stride below row_bytes");
+  if (csa::launch_writeback(rows, rows_stride, slot, n, pool, pool_stride, pool_rows, row_bytes,
+                            status, static_cast<cudaStream_t>(stream), false) < 0)
+    return cuda_fail(cudaGetLastError(), "kernel launch");
+  g_err.clear();
+  return CSA_OK;
+}
+
 int csa_profile_enable(csa_handle* h, int32_t enable) {
   if (!h) return fail(CSA_ERR_INVALID_ARG, "handle is NULL");
   h->prof = enable != 0;

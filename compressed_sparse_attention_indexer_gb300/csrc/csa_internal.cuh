@@ -168,6 +168,11 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
                        int num_sms, cudaStream_t st, bool pdl);
+// The cache update before a step: pool[slot[t]] = src[t] (row_bytes each) for
+// t < n; strides in bytes; status may be NULL.
+int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, int n, void* pool,
+                     int64_t pool_stride, int64_t pool_rows, int64_t row_bytes, int* status,
+                     cudaStream_t st, bool pdl);
 // early: this library's own kernel of the same call runs right before (the
 // lengths are then read before the grid dependency wait)
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,

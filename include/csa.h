@@ -208,6 +208,24 @@ CSA_API int csa_topk_select(csa_handle *h, int32_t nq, const float *scores, int6
 CSA_API int csa_indexer_topk_static(const csa_config *cfg, const csa_batch *b, int32_t *topk_idx,
                             int32_t *topk_cnt, int32_t *status_out, void *stream);
 
+/* The cache update that precedes a step: pool row slot[t] receives row t of
+ * `rows` for t < n, each row_bytes bytes (any element type: bf16 KV rows,
+ * FP8 key rows, fp32 scale rows).  rows_stride / pool_stride are in BYTES
+ * (>= row_bytes); rows, slot and pool are device memory.  slot [n] int64:
+ * a negative slot is a padding token and is skipped; a slot >= pool_rows is
+ * skipped and sets bit 1 in *status (a device int32, may be NULL).  Slots
+ * are expected to be collision-free (each pool row written by at most one
+ * token, as an allocator hands them out); with a repeated slot the row holds
+ * one of the rows written to it.  ("Perf: parallelize the DSpark TP-4 SWA
+ * decode hot tasks", PR description: the SWA KV scatter by slot mapping
+ * must commit every mapping entry, whatever the row count.)  n = 0 is a
+ * no-op.  Returns CSA_ERR_INVALID_ARG for a NULL pointer with n > 0, n < 0,
+ * a stride below row_bytes or negative sizes; launches on `stream`, does
+ * not synchronise. */
+CSA_API int csa_cache_writeback(const void *rows, int64_t rows_stride, const int64_t *slot,
+                                int32_t n, void *pool, int64_t pool_stride, int64_t pool_rows,
+                                int64_t row_bytes, int32_t *status, void *stream);
+
 /* Host-side checks of a batch against a config, exactly those every entry
  * point runs before launching (null / misaligned pointers, strides, sizes
  * against the maxima, ctx_len_host values).  Touches no device memory and

@@ -216,6 +216,25 @@ def decode(cfg, batch: dict, qids=None, nthreads: int | None = None, force_score
     return res
 
 
+def cache_writeback(pool: np.ndarray, rows: np.ndarray, slot) -> tuple[np.ndarray, bool]:
+    """The cache update before a step ("Perf: parallelize the DSpark TP-4 SWA
+    decode hot tasks", PR description: the KV scatter by slot mapping commits
+    every mapping entry): a copy of `pool` in which row slot[t] holds rows[t]
+    for every t with 0 <= slot[t] < len(pool), token order.  A negative slot
+    is a padding token; a slot past the pool is skipped and reported (the
+    returned flag).  Works on raw bytes, so any element type behaves alike."""
+    out = np.array(pool, copy=True)
+    bad = False
+    for t, s in enumerate(np.asarray(slot).tolist()):
+        if s < 0:
+            continue
+        if s >= out.shape[0]:
+            bad = True
+            continue
+        out[s] = rows[t]
+    return out, bad
+
+
 def e4m3_value(byte: int) -> float:
     """The value of one OCP FP8 E4M3 byte (as the indexer-key pool stores it)."""
     return float(lib().orc_e4m3_to_double(int(byte) & 0xFF))
