@@ -52,7 +52,11 @@ class CBatch(ctypes.Structure):
                 ("cmp_kv", _P), ("cmp_off", _P), ("cmp_stride", _I64), ("cmp_rows", _I64),
                 ("idx_k", _P), ("idx_off", _P), ("idx_stride", _I64), ("idx_rows", _I64),
                 ("hca_kv", _P), ("hca_off", _P), ("hca_stride", _I64), ("hca_rows", _I64),
-                ("idx_scale", _P)]
+                ("idx_scale", _P),
+                ("raw_table", _P), ("cmp_table", _P), ("idx_table", _P), ("hca_table", _P),
+                ("raw_block", ctypes.c_int32), ("cmp_block", ctypes.c_int32),
+                ("idx_block", ctypes.c_int32), ("hca_block", ctypes.c_int32),
+                ("table_stride", ctypes.c_int32)]
 
 
 _lib = None
@@ -138,15 +142,20 @@ def make_batch_struct(batch: dict, ctx_len_host=None) -> CBatch:
         B=int(batch["B"]), S=int(batch["S"]), ctx_len=_ptr(batch["ctx_len"]),
         ctx_len_host=_ptr(ctx_len_host),
         q=_ptr(batch["q"]), q_idx=_ptr(batch["q_idx"]), w=_ptr(batch["w"]),
-        raw_kv=_ptr(batch["raw_kv"]), raw_off=_ptr(batch["raw_off"]),
+        raw_kv=_ptr(batch["raw_kv"]), raw_off=_ptr(batch.get("raw_off")),
         raw_stride=int(batch["raw_stride"]), raw_rows=rows(batch["raw_kv"]),
-        cmp_kv=_ptr(batch["cmp_kv"]), cmp_off=_ptr(batch["cmp_off"]),
+        cmp_kv=_ptr(batch["cmp_kv"]), cmp_off=_ptr(batch.get("cmp_off")),
         cmp_stride=int(batch["cmp_stride"]), cmp_rows=rows(batch["cmp_kv"]),
-        idx_k=_ptr(batch["idx_k"]), idx_off=_ptr(batch["idx_off"]),
+        idx_k=_ptr(batch["idx_k"]), idx_off=_ptr(batch.get("idx_off")),
         idx_stride=int(batch["idx_stride"]), idx_rows=rows(batch["idx_k"]),
         hca_kv=_ptr(batch.get("hca_kv")), hca_off=_ptr(batch.get("hca_off")),
         hca_stride=int(batch.get("hca_stride") or 0), hca_rows=rows(batch.get("hca_kv")),
-        idx_scale=_ptr(batch.get("idx_scale")))
+        idx_scale=_ptr(batch.get("idx_scale")),
+        raw_table=_ptr(batch.get("raw_table")), cmp_table=_ptr(batch.get("cmp_table")),
+        idx_table=_ptr(batch.get("idx_table")), hca_table=_ptr(batch.get("hca_table")),
+        raw_block=int(batch.get("raw_block") or 0), cmp_block=int(batch.get("cmp_block") or 0),
+        idx_block=int(batch.get("idx_block") or 0), hca_block=int(batch.get("hca_block") or 0),
+        table_stride=int(batch.get("table_stride") or 0))
 
 
 def check_batch(cconfig: CConfig, cbatch: CBatch) -> int:

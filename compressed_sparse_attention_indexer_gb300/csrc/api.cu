@@ -123,10 +123,13 @@ int validate_batch_cfg(const csa_config& c, const csa_batch* b) {
   if (b->B == 0) return CSA_OK;
   const int es = c.dtype == CSA_DTYPE_BF16 ? 2 : 4;
   const bool fp8 = c.idx_dtype == CSA_DTYPE_FP8_E4M3;
+  // a paged pool's offsets are not read
+  const void* dummy = b->q;
   struct P { const void* p; const char* n; } ptrs[] = {
       {b->ctx_len, "ctx_len"}, {b->q, "q"}, {b->q_idx, "q_idx"}, {b->w, "w"},
-      {b->raw_kv, "raw_kv"}, {b->raw_off, "raw_off"}, {b->cmp_kv, "cmp_kv"},
-      {b->cmp_off, "cmp_off"}, {b->idx_k, "idx_k"}, {b->idx_off, "idx_off"}};
+      {b->raw_kv, "raw_kv"}, {b->raw_table ? dummy : b->raw_off, "raw_off"}, {b->cmp_kv, "cmp_kv"},
+      {b->cmp_table ? dummy : b->cmp_off, "cmp_off"}, {b->idx_k, "idx_k"},
+      {b->idx_table ? dummy : b->idx_off, "idx_off"}};
   for (const P& x : ptrs)
     if (!x.p) return fail(CSA_ERR_INVALID_ARG, "%s is NULL", x.n);
   for (const P& x : ptrs)
@@ -147,10 +150,25 @@ int validate_batch_cfg(const csa_config& c, const csa_batch* b) {
   if (fp8 && (!b->idx_scale || !aligned16(b->idx_scale)))
     return fail(CSA_ERR_INVALID_ARG, "idx_scale is NULL or not 16-byte aligned with FP8 keys");
   if (c.hca_ratio > 0) {
-    if (!b->hca_kv || !b->hca_off) return fail(CSA_ERR_INVALID_ARG, "hca_kv/hca_off NULL with hca_ratio > 0");
-    if (!aligned16(b->hca_kv) || !aligned16(b->hca_off))
+    const void* hoff = b->hca_table ? b->hca_kv : b->hca_off;
+    if (!b->hca_kv || !hoff) return fail(CSA_ERR_INVALID_ARG, "hca_kv/hca_off NULL with hca_ratio > 0");
+    if (!aligned16(b->hca_kv) || !aligned16(hoff))
       return fail(CSA_ERR_INVALID_ARG, "hca_kv/hca_off not 16-byte aligned");
   }
+  struct T { const int32_t* t; int32_t blk; const char* n; } tabs[] = {
+      {b->raw_table, b->raw_block, "raw"}, {b->cmp_table, b->cmp_block, "cmp"},
+      {b->idx_table, b->idx_block, "idx"}, {b->hca_table, b->hca_block, "hca"}};
+  bool paged = false;
+  for (const T& x : tabs) {
+    if (!x.t) continue;
+    paged = true;
+    if ((reinterpret_cast<uintptr_t>(x.t) & 3u) != 0)
+      return fail(CSA_ERR_INVALID_ARG, "%s_table is not 4-byte aligned", x.n);
+    if (x.blk < 1) return fail(CSA_ERR_INVALID_ARG, "%s_block < 1 with a %s_table", x.n, x.n);
+  }
+  if (paged && b->table_stride < 1) return fail(CSA_ERR_INVALID_ARG, "table_stride < 1 with a block table");
+  if (b->idx_table && b->idx_block % 128 != 0)
+    return fail(CSA_ERR_INVALID_ARG, "idx_block = %d is not a multiple of 128", b->idx_block);
   if (b->ctx_len_host) {
     for (int i = 0; i < b->B; ++i) {
       const int L = b->ctx_len_host[i];
@@ -175,6 +193,11 @@ csa::DevBatch dev_batch(const csa_batch* b) {
   d.cmp = b->cmp_kv; d.cmp_off = b->cmp_off; d.cmp_stride = b->cmp_stride; d.cmp_rows = b->cmp_rows;
   d.idx = b->idx_k; d.idx_off = b->idx_off; d.idx_stride = b->idx_stride; d.idx_rows = b->idx_rows;
   d.idx_scale = b->idx_scale;
+  d.raw_table = b->raw_table; d.cmp_table = b->cmp_table;
+  d.idx_table = b->idx_table; d.hca_table = b->hca_table;
+  d.raw_block = b->raw_block; d.cmp_block = b->cmp_block;
+  d.idx_block = b->idx_block; d.hca_block = b->hca_block;
+  d.table_stride = b->table_stride;
   d.hca = b->hca_kv; d.hca_off = b->hca_off; d.hca_stride = b->hca_stride; d.hca_rows = b->hca_rows;
   return d;
 }

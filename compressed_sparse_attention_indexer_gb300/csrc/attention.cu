@@ -64,7 +64,7 @@ __device__ __forceinline__ const __nv_bfloat16* row_pointer(const DevBatch& b, c
   const __nv_bfloat16* base;
   int64_t stride, rows;
   if (sid == 0) {
-    gr = b.raw_off[bi] + (p.pos - p.nwin + 1 + i);
+    gr = raw_row(b, bi, p.pos - p.nwin + 1 + i);
     base = static_cast<const __nv_bfloat16*>(b.raw); stride = b.raw_stride; rows = b.raw_rows;
   } else if (sid == 1) {
     const int j = topk_idx[(int64_t)q * K + i];
@@ -72,10 +72,10 @@ __device__ __forceinline__ const __nv_bfloat16* row_pointer(const DevBatch& b, c
       set_status(status, kStatusBadIndex);
       return nullptr;
     }
-    gr = b.cmp_off[bi] + j;
+    gr = cmp_row(b, bi, j);
     base = static_cast<const __nv_bfloat16*>(b.cmp); stride = b.cmp_stride; rows = b.cmp_rows;
   } else {
-    gr = b.hca_off[bi] + i;
+    gr = hca_row(b, bi, i);
     base = static_cast<const __nv_bfloat16*>(b.hca); stride = b.hca_stride; rows = b.hca_rows;
   }
   if (gr < 0 || gr >= rows) {
@@ -417,15 +417,15 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(DevCfg c, DevBatch b, Wo
           int64_t stride, rows;
           bool ok = true;
           if (sid == 0) {
-            gr = b.raw_off[bi] + (p.pos - p.nwin + 1 + i);
+            gr = raw_row(b, bi, p.pos - p.nwin + 1 + i);
             base = static_cast<const T*>(b.raw); stride = b.raw_stride; rows = b.raw_rows;
           } else if (sid == 1) {
             const int j = topk_idx[(int64_t)q * c.K + i];
             ok = j >= 0 && j < p.vis;
-            gr = b.cmp_off[bi] + j;
+            gr = cmp_row(b, bi, j);
             base = static_cast<const T*>(b.cmp); stride = b.cmp_stride; rows = b.cmp_rows;
           } else {
-            gr = b.hca_off[bi] + i;
+            gr = hca_row(b, bi, i);
             base = static_cast<const T*>(b.hca); stride = b.hca_stride; rows = b.hca_rows;
           }
           ok = ok && gr >= 0 && gr < rows;

@@ -180,24 +180,28 @@ __device__ __forceinline__ void job_stream(const JobCtx& x, int local, int& sid,
 // Pool row of stream row i of the job, or -1 (read as zeros by the gather and
 // masked by the softmax) when the row does not exist or is out of range.
 // `j` is the row's Top-K index for the compressed stream (loaded by the
-// caller ahead of the count it is checked against).
+// caller ahead of the count it is checked against).  `off` is the request's
+// first pool row of the stream, or -1 when that pool is paged (then the
+// pool's block table gives the row).
+template <bool kPaged>
 __device__ __forceinline__ int job_row(const DevBatch& b, const JobCtx& x, int sid, int i, int j,
                                        int64_t off, int* status) {
   if (i >= x.n[sid]) return -1;
   int64_t gr;
   int64_t rows;
   if (sid == 0) {
-    gr = off + (x.p.pos - x.p.nwin + 1 + i);
+    const int64_t r = x.p.pos - x.p.nwin + 1 + i;
+    gr = (kPaged && b.raw_table) ? raw_row(b, x.bi, r) : off + r;
     rows = b.raw_rows;
   } else if (sid == 1) {
     if (j < 0 || j >= x.p.vis) {
       set_status(status, kStatusBadIndex);
       return -1;
     }
-    gr = off + j;
+    gr = (kPaged && b.cmp_table) ? cmp_row(b, x.bi, j) : off + j;
     rows = b.cmp_rows;
   } else {
-    gr = off + i;
+    gr = (kPaged && b.hca_table) ? hca_row(b, x.bi, i) : off + i;
     rows = b.hca_rows;
   }
   if (gr < 0 || gr >= rows) {
@@ -207,6 +211,9 @@ __device__ __forceinline__ int job_row(const DevBatch& b, const JobCtx& x, int s
   return (int)gr;
 }
 
+// kPaged: some pool has a block table (else every pool is contiguous and the
+// row lookups are one add)
+template <bool kPaged>
 __global__ void __launch_bounds__(kA5Threads, 1)
     attn_tile_kernel(const __grid_constant__ CUtensorMap qmap,
                      const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
@@ -286,7 +293,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(
           sid == 0 ? b.raw : (sid == 1 ? b.cmp : b.hca));
       const int64_t stride = sid == 0 ? b.raw_stride : (sid == 1 ? b.cmp_stride : b.hca_stride);
-      const int64_t off = sid == 0 ? b.raw_off[x.bi] : (sid == 1 ? b.cmp_off[x.bi] : b.hca_off[x.bi]);
+      const int* tbl = kPaged ? (sid == 0 ? b.raw_table : (sid == 1 ? b.cmp_table : b.hca_table)) : nullptr;
+      const int64_t off = tbl ? -1 : (sid == 0 ? b.raw_off[x.bi] : (sid == 1 ? b.cmp_off[x.bi] : b.hca_off[x.bi]));
       // this lane's rows: their Top-K indices are loaded together with the
       // count they are checked against (read before waiting for the buffer,
       // so that the loads overlap the wait)
@@ -313,7 +321,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         const int rq = lw + kLoadWarps * i;
         src[i] = nullptr;
         if (rq < kTile / 4) {
-          const int gr = job_row(b, x, sid, t * kTile + 4 * rq + (lane >> 3), jr[i], off, ws.status);
+          const int gr = job_row<kPaged>(b, x, sid, t * kTile + 4 * rq + (lane >> 3), jr[i], off, ws.status);
           if (gr >= 0) src[i] = pool + (int64_t)gr * stride;
         }
         const uint32_t v = __ballot_sync(0xffffffffu, src[i] != nullptr);
@@ -852,9 +860,11 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
   if (!make_map(&qmap, b.q, (uint64_t)T * kTcH, kTcD, kTcH)) return -1;
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(attn_tile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kA5Dyn);
+    cudaFuncSetAttribute(attn_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kA5Dyn);
+    cudaFuncSetAttribute(attn_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kA5Dyn);
     attr = true;
   }
+  const bool paged = b.raw_table || b.cmp_table || b.hca_table;
   int n = 0;
   if (jobs.host_B < 0) {
     if (launch_kernel(job_prep_kernel, dim3(1), dim3(1024), 0, st, pdl, c, b, ws) < 0) return -1;
@@ -862,8 +872,9 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
   }
   int grid = num_sms;
   if (jobs.host_B >= 0 && jobs.prefix[T] < grid) grid = jobs.prefix[T] > 0 ? jobs.prefix[T] : 1;
-  if (launch_kernel(attn_tile_kernel, dim3(grid), dim3(kA5Threads), kA5Dyn, st, pdl, qmap, jobs, c,
-                    b, ws, topk_idx, topk_cnt, (pdl && early) ? 1 : 0) < 0)
+  if (launch_kernel(paged ? attn_tile_kernel<true> : attn_tile_kernel<false>, dim3(grid),
+                    dim3(kA5Threads), kA5Dyn, st, pdl, qmap, jobs, c, b, ws, topk_idx, topk_cnt,
+                    (pdl && early) ? 1 : 0) < 0)
     return -1;
   ++n;
   if (launch_kernel(attn_merge_kernel, dim3(T, kTcV / kMergeDims), dim3(256), 0, st, pdl, jobs, c,

@@ -58,7 +58,41 @@ struct DevBatch {
   const void* idx; const int64_t* idx_off; int64_t idx_stride, idx_rows;
   const float* idx_scale;  // [idx_rows] when the keys are FP8
   const void* hca; const int64_t* hca_off; int64_t hca_stride, hca_rows;
+  // paged pools: a non-null table maps request bi's logical block k to pool
+  // block table[bi * table_stride + k] of `block` rows (negative: unmapped)
+  const int* raw_table; const int* cmp_table; const int* idx_table; const int* hca_table;
+  int raw_block, cmp_block, idx_block, hca_block, table_stride;
 };
+
+// Pool row of logical row r of request bi: through the pool's block table when
+// it is paged, else the request's first row plus r.  -1 for a row in an
+// unmapped block or past the table (the callers' range checks then report it).
+// (The paged lookup is a call, so that the contiguous path inlined into the
+// hot loops stays small; logical rows are below 2^31.)
+static __device__ __noinline__ int64_t paged_row(const int* table, int block, int tstride, int bi, int64_t r) {
+  if (r < 0 || r > 0x7fffffffLL) return -1;
+  const int k = (int)r / block;
+  if (k >= tstride) return -1;
+  const int pb = table[(int64_t)bi * tstride + k];
+  return pb < 0 ? -1 : (int64_t)pb * block + ((int)r - k * block);
+}
+__device__ __forceinline__ int64_t pool_row(const int* table, int block, int tstride,
+                                            const int64_t* off, int bi, int64_t r) {
+  if (!table) return off[bi] + r;
+  return paged_row(table, block, tstride, bi, r);
+}
+__device__ __forceinline__ int64_t raw_row(const DevBatch& b, int bi, int64_t r) {
+  return pool_row(b.raw_table, b.raw_block, b.table_stride, b.raw_off, bi, r);
+}
+__device__ __forceinline__ int64_t cmp_row(const DevBatch& b, int bi, int64_t r) {
+  return pool_row(b.cmp_table, b.cmp_block, b.table_stride, b.cmp_off, bi, r);
+}
+__device__ __forceinline__ int64_t idx_row(const DevBatch& b, int bi, int64_t r) {
+  return pool_row(b.idx_table, b.idx_block, b.table_stride, b.idx_off, bi, r);
+}
+__device__ __forceinline__ int64_t hca_row(const DevBatch& b, int bi, int64_t r) {
+  return pool_row(b.hca_table, b.hca_block, b.table_stride, b.hca_off, bi, r);
+}
 
 // Per-query quantities of the step (visibility, window, bypass).
 struct QueryPlan {

@@ -72,14 +72,12 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   // issue cursor, with the request's values cached
   int ib = b0, ib_end = prefix[b0 + 1], ib_first = prefix[b0];
   int ib_rows = request_rows(c, b.S, b.ctx_len[b0], score_all);
-  int64_t ib_off = b.idx_off[b0];
   auto issue = [&](int item) {
     while (item >= ib_end) {
       ++ib;
       ib_first = ib_end;
       ib_end = prefix[ib + 1];
       ib_rows = request_rows(c, b.S, b.ctx_len[ib], score_all);
-      ib_off = b.idx_off[ib];
     }
     const int c0 = (item - ib_first) * kIdxChunk;
     uint8_t* dst0 = Ks + (item % NST) * kKStageBytes;
@@ -88,7 +86,7 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       const int id = tid + i * kIdxThreads;
       const int row = id >> 4, ch = id & 15;
       const int r = c0 + row;
-      const int64_t gr = ib_off + r;
+      const int64_t gr = r < ib_rows ? idx_row(b, ib, r) : -1;
       const bool inb = gr >= 0 && gr < b.idx_rows;
       const bool want = r < ib_rows;
       if (want && !inb && ch == 0) set_status(ws.status, kStatusBadIndex);
@@ -224,7 +222,7 @@ __global__ void __launch_bounds__(256) indexer_simt_kernel(DevCfg c, DevBatch b,
   const float* wq = b.w + (int64_t)q * c.Hi;
   const T* kp = static_cast<const T*>(b.idx);
   for (int j = blockIdx.y * 8 + warp; j < p.vis; j += gridDim.y * 8) {
-    const int64_t gr = b.idx_off[bi] + j;
+    const int64_t gr = idx_row(b, bi, j);
     float acc;
     if (gr < 0 || gr >= b.idx_rows) {
       if (lane == 0) set_status(ws.status, kStatusBadIndex);

@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       int64_t off = 0;
       for (int it = lo; it < hi && !*abort; ++it) {
         if (cur.advance(it) || it == lo) {
-          off = b.idx_off[cur.bi];
+          off = b.idx_table ? 0 : b.idx_off[cur.bi];
           const int qb = qc % NQB;
           if (qc >= NQB && !tc5::mbar_wait(smem_u32(&sm.qempty[qb]), ((qc / NQB) - 1) & 1, abort))
             break;
@@ -200,7 +200,13 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
         const int st = kc % NST;
         if (kc >= NST && !tc5::mbar_wait(smem_u32(&sm.empty[st]), ((kc / NST) - 1) & 1, abort))
           break;
-        const int y = (int)(off + (int64_t)(it - cur.first) * kIdxChunk);
+        // the item's first pool row; a paged pool's blocks hold whole items
+        // (block a multiple of 128 rows), an unmapped block reads as zeros
+        // past the pool (its rows are reported by the epilogue)
+        const int64_t c0 = (int64_t)(it - cur.first) * kIdxChunk;
+        int64_t y0 = b.idx_table ? idx_row(b, cur.bi, c0) : off + c0;
+        if (y0 < 0) y0 = b.idx_rows;
+        const int y = (int)y0;
         tc5::mbar_expect_tx(smem_u32(&sm.full[st]), stage_bytes);
         if (kFp8) {  // one box: 128 rows x 128 FP8 keys
           tc5::tma_load_2d(kbuf + st * stage_bytes, &kmap, 0, y, smem_u32(&sm.full[st]));
@@ -309,7 +315,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     for (int it = lo; it < hi && !*abort; ++it) {
       if (cur.advance(it) || it == lo) {
         L = b.ctx_len[cur.bi];
-        off = b.idx_off[cur.bi];
+        off = b.idx_table ? 0 : b.idx_off[cur.bi];
         // the request's w (S x 64) into shared memory, shared by its items
         named_barrier_sync(1, 128);
         for (int v = row; v < S * kTcHi; v += 128) w_sm[v] = __ldg(b.w + (int64_t)cur.bi * S * kTcHi + v);
@@ -317,7 +323,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       }
       const int bi = cur.bi;
       const int c0 = (it - cur.first) * kIdxChunk;
-      const int64_t gr = off + c0 + row;
+      const int64_t gr = b.idx_table ? idx_row(b, bi, c0 + row) : off + c0 + row;
       const bool in_pool = gr >= 0 && gr < b.idx_rows;
       // FP8: the row's scale (loaded ahead of the accumulator wait); only rows
       // the query may read are used

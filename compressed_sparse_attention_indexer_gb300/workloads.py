@@ -200,7 +200,7 @@ def make_batch(wl: Workload, lens=None, seed: int | None = None, gap_rows: int =
         idx_k, idx_off, idx_scale = _fp8_pool(gen, ncmp, cfg.Di, d.k_idx, gap_rows)
     else:
         idx_k, idx_off = _pool(gen, ncmp, cfg.Di, d.k_idx, dt, gap_rows)
-    batch = dict(B=B, S=S, ctx_len=ctx, q=q, q_idx=q_idx, w=w,
+    batch = dict(B=B, S=S, ctx_len=ctx, q=q, q_idx=q_idx, w=w, _rows_cmp=ncmp, _rows_idx=ncmp,
                  raw_kv=raw_kv, raw_off=raw_off, raw_stride=cfg.D, raw_first=first,
                  cmp_kv=cmp_kv, cmp_off=cmp_off, cmp_stride=cfg.D,
                  idx_k=idx_k, idx_off=idx_off, idx_stride=cfg.Di, idx_scale=idx_scale,
@@ -208,12 +208,74 @@ def make_batch(wl: Workload, lens=None, seed: int | None = None, gap_rows: int =
     if cfg.hca_ratio:
         nh = [L // cfg.hca_ratio for L in Ls]
         hca_kv, hca_off = _pool(gen, nh, cfg.D, d.hca, dt, gap_rows)
-        batch.update(hca_kv=hca_kv, hca_off=hca_off, hca_stride=cfg.D)
+        batch.update(hca_kv=hca_kv, hca_off=hca_off, hca_stride=cfg.D, _rows_hca=nh)
     return batch
 
 
+def paginate(batch: dict, blocks: dict, seed: int = 0, spare_blocks: int = 2) -> dict:
+    """The same batch with paged pools: for each pool named in `blocks`
+    ("raw", "cmp", "idx", "hca" -> rows per block), the request's rows are
+    cut into logical blocks placed at shuffled pool blocks, and a block table
+    per pool maps request b's logical block k to its pool block
+    (table[b, k], -1 = unmapped).  Pool rows that hold no request row (the
+    tail of a request's last block, spare blocks, raw rows before the window
+    a request keeps) are NaN (FP8 keys: the NaN code, scale NaN), so a read
+    of a row the step may not use poisons its output.  Layout only: the row
+    values are the batch's own."""
+    out = dict(batch)
+    B = int(batch["B"])
+    Ls = [int(x) for x in batch["ctx_len"]]
+    gen = torch.Generator().manual_seed(seed)
+    keys = {"raw": "raw_kv", "cmp": "cmp_kv", "idx": "idx_k", "hca": "hca_kv"}
+    plans = {}
+    tstride = 1
+    for name, bs in blocks.items():
+        if batch.get(keys[name]) is None:
+            continue
+        if name == "raw":  # rows are positions; a request keeps [first, L)
+            rng = [(int(batch["raw_first"][b]), Ls[b]) for b in range(B)]
+        else:
+            rng = [(0, int(n)) for n in batch["_rows_" + name]]
+        nblk = [(hi + bs - 1) // bs for (_, hi) in rng]
+        tstride = max(tstride, max(nblk))
+        plans[name] = (bs, rng, nblk)
+    for name, (bs, rng, nblk) in plans.items():
+        key = keys[name]
+        src, off = batch[key], batch[name + "_off"]
+        # logical blocks that hold at least one existing row get a pool block
+        owned = [(b, k) for b in range(B) for k in range(nblk[b]) if (k + 1) * bs > rng[b][0]]
+        total = len(owned) + spare_blocks
+        perm = torch.randperm(total, generator=gen).tolist()
+        if src.dtype == torch.uint8:
+            pool = torch.full((total * bs, src.shape[1]), 0x7F, dtype=torch.uint8)
+        else:
+            pool = torch.full((total * bs, src.shape[1]), float("nan"), dtype=src.dtype)
+        scale = None
+        if name == "idx" and batch.get("idx_scale") is not None:
+            scale = torch.full((total * bs,), float("nan"), dtype=torch.float32)
+        table = torch.full((B, tstride), -1, dtype=torch.int32)
+        for i, (b, k) in enumerate(owned):
+            pb = perm[i]
+            table[b, k] = pb
+            lo, hi = max(k * bs, rng[b][0]), min((k + 1) * bs, rng[b][1])
+            rows = slice(int(off[b]) + lo, int(off[b]) + hi)
+            dst = slice(pb * bs + (lo - k * bs), pb * bs + (hi - k * bs))
+            pool[dst] = src[rows]
+            if scale is not None:
+                scale[dst] = batch["idx_scale"][rows]
+        out[key] = pool
+        out[name + "_table"] = table
+        out[name + "_block"] = bs
+        out[name + "_off"] = None
+        if scale is not None:
+            out["idx_scale"] = scale
+    out["table_stride"] = tstride
+    return out
+
+
 TENSOR_KEYS = ("ctx_len", "q", "q_idx", "w", "raw_kv", "raw_off", "cmp_kv", "cmp_off",
-               "idx_k", "idx_off", "idx_scale", "hca_kv", "hca_off")
+               "idx_k", "idx_off", "idx_scale", "hca_kv", "hca_off",
+               "raw_table", "cmp_table", "idx_table", "hca_table")
 
 
 def to_device(batch: dict, device) -> dict:

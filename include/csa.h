@@ -41,7 +41,8 @@
  *  - Element types: CSA_DTYPE_BF16 (bf16 storage, fp32 arithmetic) or
  *    CSA_DTYPE_F32.  Strides are in ELEMENTS; every row must start on a
  *    16-byte boundary (pointer and stride*element_size multiples of 16).
- *  - Row r of pool X for request b is at X + (X_off[b] + r) * X_stride.
+ *  - Row r of pool X for request b is at X + (X_off[b] + r) * X_stride, or
+ *    where the pool's block table puts it (paged pools, see csa_batch).
  *    X_rows is the number of rows the pool holds; a row index outside
  *    [0, X_rows) is never dereferenced: it sets CSA_ERR_BAD_INDEX in the
  *    handle's status word and the row is skipped.
@@ -63,7 +64,7 @@
 extern "C" {
 #endif
 
-#define CSA_ABI_VERSION 2
+#define CSA_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define CSA_API __attribute__((visibility("default")))
@@ -133,6 +134,19 @@ typedef struct {
     const float *idx_scale;   /* [idx_rows] per-row scale of FP8 indexer keys (16-byte
                                  aligned); required with idx_dtype FP8, else ignored.
                                  idx_stride is then in bytes (a multiple of 16). */
+    /* Paged pools (optional; NULL tables = the contiguous layout above).  With
+     * X_table given, logical row r of request b in pool X is pool row
+     * X_table[b * table_stride + r / X_block] * X_block + r % X_block, and
+     * X_off is not read (it may be NULL).  A negative table entry is an
+     * unmapped block: a row the step needs there is skipped and reported as
+     * CSA_ERR_BAD_INDEX.  Raw rows are indexed by position (r in [0, L_b));
+     * compressed, indexer-key and heavy rows by their index in the request.
+     * idx_block must be a multiple of 128 (the indexer reads 128 keys at a
+     * time); FP8 key scales follow the key rows.  Tables are device int32
+     * arrays of B * table_stride entries. */
+    const int32_t *raw_table, *cmp_table, *idx_table, *hca_table;
+    int32_t raw_block, cmp_block, idx_block, hca_block;
+    int32_t table_stride;
 } csa_batch;
 
 typedef struct csa_handle csa_handle;

@@ -46,7 +46,11 @@ class OrcBatch(ctypes.Structure):
                 ("cmp", _P), ("cmp_off", _P), ("cmp_stride", ctypes.c_int64),
                 ("idx", _P), ("idx_off", _P), ("idx_stride", ctypes.c_int64),
                 ("hca", _P), ("hca_off", _P), ("hca_stride", ctypes.c_int64),
-                ("idx_scale", _P)]
+                ("idx_scale", _P),
+                ("raw_table", _P), ("cmp_table", _P), ("idx_table", _P), ("hca_table", _P),
+                ("raw_block", ctypes.c_int32), ("cmp_block", ctypes.c_int32),
+                ("idx_block", ctypes.c_int32), ("hca_block", ctypes.c_int32),
+                ("table_stride", ctypes.c_int32)]
 
 
 class OrcQueryInfo(ctypes.Structure):
@@ -185,7 +189,12 @@ class _HostBatch:
             idx=keep("idx_k"), idx_off=keep("idx_off", np.int64), idx_stride=int(batch["idx_stride"]),
             hca=keep("hca_kv"), hca_off=keep("hca_off", np.int64),
             hca_stride=int(batch.get("hca_stride", 0) or 0),
-            idx_scale=keep("idx_scale", np.float32))
+            idx_scale=keep("idx_scale", np.float32),
+            raw_table=keep("raw_table", np.int32), cmp_table=keep("cmp_table", np.int32),
+            idx_table=keep("idx_table", np.int32), hca_table=keep("hca_table", np.int32),
+            raw_block=int(batch.get("raw_block") or 0), cmp_block=int(batch.get("cmp_block") or 0),
+            idx_block=int(batch.get("idx_block") or 0), hca_block=int(batch.get("hca_block") or 0),
+            table_stride=int(batch.get("table_stride") or 0))
 
 
 def decode(cfg, batch: dict, qids=None, nthreads: int | None = None, force_score: bool = False):
@@ -208,6 +217,8 @@ def decode(cfg, batch: dict, qids=None, nthreads: int | None = None, force_score
                           q.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), nq,
                           FORCE_SCORE if force_score else 0, nthreads, _dp(out), _dp(lse),
                           idx.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), info)
+    if rc == -2:
+        raise ValueError("oracle: a row a query needs lies in an unmapped block of a paged pool")
     if rc != 0:
         raise ValueError("oracle: a query has pos < 0 (ctx_len < S)")
     res = {"out": out, "lse": lse, "topk_idx": idx, "qids": q}
@@ -248,4 +259,6 @@ def query_scores(cfg, batch: dict, b: int, s: int) -> np.ndarray:
     vis = (pos + 1) // cfg.ratio
     out = np.zeros(max(vis, 1), np.float64)
     n = lib().orc_query_scores(ctypes.byref(c), ctypes.byref(hb.c), b, s, _dp(out))
+    if n < 0:
+        raise ValueError("oracle: a key row lies in an unmapped block of a paged pool")
     return out[:n]

@@ -76,6 +76,9 @@ typedef struct {
     const void *idx;   const int64_t *idx_off; int64_t idx_stride;
     const void *hca;   const int64_t *hca_off; int64_t hca_stride;
     const float *idx_scale; /* [rows] scale of each FP8 key row */
+    /* paged pools: NULL tables = the contiguous layout above */
+    const int32_t *raw_table, *cmp_table, *idx_table, *hca_table;
+    int32_t raw_block, cmp_block, idx_block, hca_block, table_stride;
 } orc_batch;
 
 /* ------------------------------------------------------------------ */
@@ -118,6 +121,33 @@ double orc_e4m3_to_double(uint8_t v)
     else
         mag = ldexp(1.0 + (double)m / 8.0, e - 7);
     return sign ? -mag : mag;
+}
+
+/* Pool row of row r of request b: with a block table (a paged pool), entry
+ * r / block of the request's table names the pool block that holds it, at
+ * offset r % block; without one, the request's rows are consecutive from
+ * off[b].  -1 when the block is unmapped (a negative entry) or past the
+ * table.  (Paged pools: the pages' allocator-mapped cache pools, "Fix:
+ * complete DeepSeek V4 TP CSA decode", PR description.) */
+static int64_t orc_pool_row(const int32_t *table, int32_t block, int32_t tstride,
+                            const int64_t *off, int32_t b, int64_t r)
+{
+    if (!table) return off[b] + r;
+    if (r < 0 || r / block >= tstride) return -1;
+    const int32_t pb = table[(int64_t)b * tstride + r / block];
+    return pb < 0 ? -1 : (int64_t)pb * block + r % block;
+}
+
+/* Loads row `row` of a pool of width n, or zeros and *bad = 1 if row < 0. */
+static void orc_load_row(const void *base, int32_t dtype, int64_t row, int64_t stride,
+                         int64_t n, double *dst, int *bad)
+{
+    if (row < 0) {
+        for (int64_t i = 0; i < n; ++i) dst[i] = 0.0;
+        *bad = 1;
+        return;
+    }
+    orc_load_vec(base, dtype, row * stride, n, dst);
 }
 
 /* Indexer key row `row` of the pool (absolute row index). */
@@ -276,6 +306,7 @@ int orc_query(const orc_cfg *c, const orc_batch *bt, int32_t b, int32_t s,
     const int32_t vis = (pos + 1) / c->ratio;
     const int32_t nwin = (c->win < pos + 1) ? c->win : pos + 1;
     const int32_t vis2 = c->hca_ratio > 0 ? (pos + 1) / c->hca_ratio : 0;
+    int bad = 0; /* a row the query needs lies in an unmapped block */
 
     /* (a)+(b): indexer score and Top-K, or the bypass */
     int32_t cnt;
@@ -287,8 +318,16 @@ int orc_query(const orc_cfg *c, const orc_batch *bt, int32_t b, int32_t s,
         double *sc = (double *)malloc(sizeof(double) * (size_t)(vis > 0 ? vis : 1));
         orc_load_vec(bt->q_idx, c->dtype, qid * Hi * Di, (int64_t)Hi * Di, qi);
         for (int32_t h = 0; h < Hi; ++h) wv[h] = (double)bt->w[qid * Hi + h];
-        for (int32_t j = 0; j < vis; ++j)
-            orc_load_key_row(c, bt, bt->idx_off[b] + j, kr + (int64_t)j * Di);
+        for (int32_t j = 0; j < vis; ++j) {
+            const int64_t row = orc_pool_row(bt->idx_table, bt->idx_block, bt->table_stride,
+                                             bt->idx_off, b, j);
+            if (row < 0) {
+                bad = 1;
+                for (int32_t d = 0; d < Di; ++d) kr[(int64_t)j * Di + d] = 0.0;
+            } else {
+                orc_load_key_row(c, bt, row, kr + (int64_t)j * Di);
+            }
+        }
         orc_index_scores(Hi, Di, qi, wv, vis, kr, sc);
         cnt = orc_topk(sc, vis, K, idx);
         free(qi); free(wv); free(kr); free(sc);
@@ -303,14 +342,17 @@ int orc_query(const orc_cfg *c, const orc_batch *bt, int32_t b, int32_t s,
     double *rows = (double *)malloc(sizeof(double) * (size_t)(nrows > 0 ? nrows : 1) * D);
     int32_t u = 0;
     for (int32_t r = pos - nwin + 1; r <= pos; ++r, ++u)
-        orc_load_vec(bt->raw, c->dtype, (bt->raw_off[b] + r) * bt->raw_stride, D,
-                     rows + (int64_t)u * D);
+        orc_load_row(bt->raw, c->dtype,
+                     orc_pool_row(bt->raw_table, bt->raw_block, bt->table_stride, bt->raw_off, b, r),
+                     bt->raw_stride, D, rows + (int64_t)u * D, &bad);
     for (int32_t i = 0; i < cnt; ++i, ++u)
-        orc_load_vec(bt->cmp, c->dtype, (bt->cmp_off[b] + idx[i]) * bt->cmp_stride,
-                     D, rows + (int64_t)u * D);
+        orc_load_row(bt->cmp, c->dtype,
+                     orc_pool_row(bt->cmp_table, bt->cmp_block, bt->table_stride, bt->cmp_off, b, idx[i]),
+                     bt->cmp_stride, D, rows + (int64_t)u * D, &bad);
     for (int32_t r = 0; r < vis2; ++r, ++u)
-        orc_load_vec(bt->hca, c->dtype, (bt->hca_off[b] + r) * bt->hca_stride, D,
-                     rows + (int64_t)u * D);
+        orc_load_row(bt->hca, c->dtype,
+                     orc_pool_row(bt->hca_table, bt->hca_block, bt->table_stride, bt->hca_off, b, r),
+                     bt->hca_stride, D, rows + (int64_t)u * D, &bad);
 
     /* (d): one softmax over the union, then inverse RoPE */
     double *qv = (double *)malloc(sizeof(double) * (size_t)H * D);
@@ -328,7 +370,7 @@ int orc_query(const orc_cfg *c, const orc_batch *bt, int32_t b, int32_t s,
         info->vis2 = vis2;
         info->rows_used = nrows;
     }
-    return 0;
+    return bad ? -2 : 0;
 }
 
 /* Scores of every visible row of query (b, s); returns vis. */
@@ -344,11 +386,18 @@ int32_t orc_query_scores(const orc_cfg *c, const orc_batch *bt, int32_t b,
     double *kr = (double *)malloc(sizeof(double) * (size_t)(vis > 0 ? vis : 1) * Di);
     orc_load_vec(bt->q_idx, c->dtype, qid * Hi * Di, (int64_t)Hi * Di, qi);
     for (int32_t h = 0; h < Hi; ++h) wv[h] = (double)bt->w[qid * Hi + h];
-    for (int32_t j = 0; j < vis; ++j)
-        orc_load_key_row(c, bt, bt->idx_off[b] + j, kr + (int64_t)j * Di);
-    orc_index_scores(Hi, Di, qi, wv, vis, kr, scores);
+    int bad = 0;
+    for (int32_t j = 0; j < vis; ++j) {
+        const int64_t row = orc_pool_row(bt->idx_table, bt->idx_block, bt->table_stride,
+                                         bt->idx_off, b, j);
+        if (row < 0)
+            bad = 1;
+        else
+            orc_load_key_row(c, bt, row, kr + (int64_t)j * Di);
+    }
+    if (!bad) orc_index_scores(Hi, Di, qi, wv, vis, kr, scores);
     free(qi); free(wv); free(kr);
-    return vis;
+    return bad ? -1 : vis;
 }
 
 /* ------------------------------------------------------------------ */
@@ -383,7 +432,8 @@ static void *orc_worker(void *arg)
 }
 
 /* Runs the queries qids[0..nq) (flattened b*S+s) on nthreads threads.
- * Output slot t belongs to qids[t].  Returns 0, or -1 on a bad query. */
+ * Output slot t belongs to qids[t].  Returns 0, -1 on a bad query, or -2 if
+ * a row a query needs lies in an unmapped block of a paged pool. */
 int orc_decode(const orc_cfg *c, const orc_batch *bt, const int32_t *qids,
                int32_t nq, int32_t flags, int32_t nthreads, double *out,
                double *lse, int32_t *idx, orc_query_info *info)

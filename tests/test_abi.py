@@ -31,7 +31,7 @@ def test_exports_every_declared_symbol(L):
     for n in names:
         assert hasattr(L, n), f"{n} declared in csa.h but not exported"
     assert set(names) == set(csa.EXPORTS)
-    assert L.csa_abi_version() == 2
+    assert L.csa_abi_version() == 3
 
 
 def _cfg(**kw):
