@@ -99,6 +99,9 @@ int validate_cfg(const csa_config* c) {
       (c->dtype != CSA_DTYPE_BF16 || c->idx_heads != csa::kTcHi || c->idx_dim != csa::kTcDi))
     return fail(CSA_ERR_UNSUPPORTED, "FP8 indexer keys need dtype bf16, idx_heads %d, idx_dim %d",
                 csa::kTcHi, csa::kTcDi);
+  if (c->idx_dtype == CSA_DTYPE_FP8_E4M3 && c->max_queries_per_req > csa::indexer_fp8_max_queries())
+    return fail(CSA_ERR_UNSUPPORTED, "FP8 indexer keys support at most %d queries per request",
+                csa::indexer_fp8_max_queries());
   if (c->max_batch < 1 || c->max_queries_per_req < 1 || c->max_context < 1)
     return fail(CSA_ERR_INVALID_ARG, "workspace maxima must be >= 1");
   if (c->max_context / c->ratio > kMaxVisCap)
@@ -218,7 +221,10 @@ void host_items(const csa_handle* h, const csa_batch* b, int score_all, csa::Ite
       const int vis = (L - b->S + s + 1) / c.ratio;
       if (vis > c.topk || (score_all && vis > 0)) rows = vis > rows ? vis : rows;
     }
-    acc += (rows + csa::kIdxChunk - 1) / csa::kIdxChunk;
+    int n = (rows + csa::kIdxChunk - 1) / csa::kIdxChunk;
+    const int qs = csa::indexer_qsplit(h->dc, b->S);
+    if (qs) n *= (b->S + qs - 1) / qs;  // (query group, key chunk) items
+    acc += n;
   }
   it->prefix[b->B] = acc;
   it->host_B = b->B;
@@ -278,7 +284,10 @@ void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int
   const bool pdl = use_pdl();
   if (items.host_B < 0)
     L.add(staged(h, kStagePlan, st,
-                 [&] { return csa::launch_prep(h->dc, db, h->ws, score_all, st, pdl); }));
+                 [&] {
+                   return csa::launch_prep(h->dc, db, h->ws, score_all,
+                                           csa::indexer_qsplit(h->dc, b->S), st, pdl);
+                 }));
   L.add(staged(h, kStageIndexer, st, [&] {
     return csa::launch_indexer(h->dc, db, h->ws, items, score_all, scores, ld, h->num_sms, st, pdl);
   }));

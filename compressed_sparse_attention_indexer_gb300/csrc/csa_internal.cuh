@@ -194,11 +194,17 @@ int launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
 // ---- launch wrappers (defined in the kernel files) -------------------------
 // Each returns the number of kernels launched (>= 0) or -1 on a launch error.
 // `pdl`: launch as a programmatic dependent of the previous kernel.
-int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all,
+int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all, int qsplit,
                 cudaStream_t st, bool pdl);
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
                    int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
                    bool pdl);
+int indexer_fp8_max_queries();
+bool indexer_tc5_fits(const DevCfg& c, int S);
+// warp-MMA indexer: queries per q_idx group; above it a request's work is
+// split by query group (see indexer_qsplit)
+constexpr int kMmaGroup = 8;
+int indexer_qsplit(const DevCfg& c, int S);
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
                        int num_sms, cudaStream_t st, bool pdl);

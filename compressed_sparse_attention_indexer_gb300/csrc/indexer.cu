@@ -49,7 +49,8 @@ __device__ __forceinline__ int request_of(const int* prefix, int B, int item) {
 
 __global__ void __launch_bounds__(kIdxThreads, 1)
     indexer_mma_kernel(const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
-                       int score_all, float* __restrict__ scores, int64_t ld, int SG, int NST) {
+                       int score_all, float* __restrict__ scores, int64_t ld, int SG, int NST,
+                       int qsplit) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* Qs = smem;
   uint8_t* Ks = Qs + SG * kQBytes;
@@ -72,6 +73,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
   // issue cursor, with the request's values cached
   int ib = b0, ib_end = prefix[b0 + 1], ib_first = prefix[b0];
   int ib_rows = request_rows(c, b.S, b.ctx_len[b0], score_all);
+  // with qsplit, a request's items are (query group, key chunk) pairs, group
+  // major: item i of the request is chunk i % chunks of group i / chunks
   auto issue = [&](int item) {
     while (item >= ib_end) {
       ++ib;
@@ -79,7 +82,9 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       ib_end = prefix[ib + 1];
       ib_rows = request_rows(c, b.S, b.ctx_len[ib], score_all);
     }
-    const int c0 = (item - ib_first) * kIdxChunk;
+    const int ib_chunks = (ib_rows + kIdxChunk - 1) / kIdxChunk;
+    const int li = item - ib_first;
+    const int c0 = (qsplit ? li % ib_chunks : li) * kIdxChunk;
     uint8_t* dst0 = Ks + (item % NST) * kKStageBytes;
 #pragma unroll
     for (int i = 0; i < (kIdxChunk * 16) / kIdxThreads; ++i) {
@@ -117,7 +122,11 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       cb_end = prefix[cb + 1];
       cb_L = b.ctx_len[cb];
     }
-    const int c0 = (it - cb_first) * kIdxChunk;
+    const int cb_chunks = (request_rows(c, b.S, cb_L, score_all) + kIdxChunk - 1) / kIdxChunk;
+    const int li = it - cb_first;
+    const int c0 = (qsplit ? li % cb_chunks : li) * kIdxChunk;
+    const int gfirst = qsplit ? (li / cb_chunks) * qsplit : 0;      // this item's query group
+    const int gend = qsplit ? min(b.S, gfirst + qsplit) : b.S;
     const uint8_t* Kst = Ks + (it % NST) * kKStageBytes;
 
     // A fragments: this warp's 16 key rows x 128 dims, kept across queries
@@ -132,8 +141,8 @@ __global__ void __launch_bounds__(kIdxThreads, 1)
       }
     }
 
-    for (int g0 = 0; g0 < b.S; g0 += SG) {
-      const int ng = min(SG, b.S - g0);
+    for (int g0 = gfirst; g0 < gend; g0 += SG) {
+      const int ng = min(SG, gend - g0);
       if (cb != q_b || g0 != q_g) {
         __syncthreads();  // every warp is done with the previous q_idx group
         const uint4* src = reinterpret_cast<const uint4*>(
@@ -261,6 +270,18 @@ bool tensor_core_shape(const DevCfg& c) {
          c.Hi == kTcHi && c.Di == kTcDi;
 }
 
+// Queries per work item of the warp-MMA indexer: a request with more than
+// kMmaGroup queries (a prefill chunk) has its work split by query group, so
+// that its key chunks x groups spread over the SMs; 0 keeps one item per key
+// chunk (all queries), which the tcgen05 kernel always uses.  The work list
+// and the kernel take the same value.
+int indexer_qsplit(const DevCfg& c, int S) {
+  if (c.idx_fp8 || c.dtype != CSA_DTYPE_BF16 || c.Hi != kTcHi || c.Di != kTcDi) return 0;
+  if (S <= kMmaGroup) return 0;
+  const bool tc5 = tensor_core_shape(c) && indexer_impl() == kIndexerTc5 && indexer_tc5_fits(c, S);
+  return tc5 ? 0 : kMmaGroup;
+}
+
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
                    int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
                    bool pdl) {
@@ -275,7 +296,7 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
     if (r != -2) return r;  // -2: shape outside the tcgen05 kernel, use warp MMA
   }
   if (tensor_core_shape(c)) {
-    const int SG = b.S < 8 ? b.S : 8;
+    const int SG = b.S < kMmaGroup ? b.S : kMmaGroup;
     const int fixed = SG * kQBytes + kStashBytes + SG * kTcHi * 4;
     int NST = (227 * 1024 - fixed) / kKStageBytes;
     NST = NST > 4 ? 4 : NST;
@@ -290,7 +311,7 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
     int grid = num_sms;
     if (known > 0 && known < grid) grid = known;
     return launch_kernel(indexer_mma_kernel, dim3(grid), dim3(kIdxThreads), smem, st, pdl, items,
-                         c, b, ws, score_all, scores, ld, SG, NST);
+                         c, b, ws, score_all, scores, ld, SG, NST, indexer_qsplit(c, b.S));
   }
   int y = (c.max_vis + 7) / 8;
   if (y > 64) y = 64;

@@ -424,6 +424,69 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 
 }  // namespace
 
+// Launch shape of the tcgen05 indexer for S queries per request; false when
+// a request's queries leave no room for two key stages (the caller then uses
+// the warp-MMA kernel).  Tuning knobs, read once: CSA_T5_STAGES caps the ring
+// depth, CSA_T5_CTAS forces the CTAs per SM (1..4).
+struct T5Plan {
+  int ctas_per_sm, acc_cols, NB, NCB, NST, NQB, stage_bytes, conv_bytes, qbytes;
+};
+static bool plan_t5(const DevCfg& c, int S, T5Plan* p) {
+  static int max_stages = -1, forced_ctas = 0;
+  if (max_stages < 0) {
+    const char* e = getenv("CSA_T5_STAGES");
+    max_stages = e ? atoi(e) : 8;
+    if (max_stages < 2 || max_stages > 8) max_stages = 8;
+    const char* f = getenv("CSA_T5_CTAS");
+    forced_ctas = f ? atoi(f) : 0;
+    if (forced_ctas < 0 || forced_ctas > 4) forced_ctas = 0;
+  }
+  // CTAs per SM: two independent pipelines per SM stream measurably faster
+  // than one deeper ring (the ring depth beyond three stages does not
+  // matter), so two whenever a request's q_idx leaves room for two stages
+  // each.  FP8 keys: one CTA per SM (the converted buffers leave no room for
+  // a second CTA's ring).
+  const bool fp8 = c.idx_fp8 != 0;
+  p->ctas_per_sm = forced_ctas ? forced_ctas : ((S <= 2 && !fp8) ? 2 : 1);
+  const int G = S < 4 ? S : 4;
+  p->acc_cols = 32;
+  while (p->acc_cols < 64 * G) p->acc_cols <<= 1;  // power of two >= 32
+  p->NB = 512 / p->ctas_per_sm / p->acc_cols;       // accumulators that fit in TMEM
+  if (p->NB > 8) p->NB = 8;
+  if (p->NB < 2) return false;
+  p->qbytes = S * 2 * kQSubBytes;
+  const int per_cta = 228 * 1024 / p->ctas_per_sm - 1024;  // per-SM shared memory / CTAs
+  p->stage_bytes = fp8 ? kStage8Bytes : kStageBytes;
+  // FP8: two converted items (measured: a third adds nothing)
+  p->NCB = fp8 ? kConvBufs : 0;
+  p->conv_bytes = p->NCB * kStageBytes;
+  // key stages first: a CTA spans few requests, so a second q_idx buffer
+  // (prefetching the next request's queries) is kept only when it costs no
+  // key stage
+  const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4 - p->conv_bytes;
+  auto stages = [&](int nqb) {
+    const int n = (budget - nqb * p->qbytes) / p->stage_bytes;
+    return n > max_stages ? max_stages : n;
+  };
+  p->NQB = stages(2) >= stages(1) ? 2 : 1;
+  p->NST = stages(p->NQB);
+  return p->NST >= 2;
+}
+
+bool indexer_tc5_fits(const DevCfg& c, int S) {
+  T5Plan p;
+  return plan_t5(c, S, &p);
+}
+
+// Largest queries per request the FP8 kernel (tcgen05 only) takes.
+int indexer_fp8_max_queries() {
+  DevCfg c = {};
+  c.idx_fp8 = 1;
+  for (int S = 64; S >= 1; --S)
+    if (indexer_tc5_fits(c, S)) return S;
+  return 0;
+}
+
 // Launches the tcgen05 indexer; returns 1 on launch, 0 with nothing to do,
 // -1 if the launch (or the tensor-map encoding) failed, -2 if the shape does
 // not fit this kernel (the caller then uses the warp-MMA kernel).
@@ -434,53 +497,15 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   if (known == 0) return 0;
   if (b.idx_rows <= 0 || b.idx_rows > 0x7fffffffLL) return -2;
   const int S = b.S;
-  const int qbytes = S * 2 * kQSubBytes;
-  // CTAs per SM: two independent pipelines per SM stream measurably faster
-  // than one deeper ring (the ring depth beyond three stages does not
-  // matter), so two whenever a request's q_idx leaves room for two stages
-  // each.  Tuning knobs, read once: CSA_T5_STAGES caps the ring depth,
-  // CSA_T5_CTAS forces the CTAs per SM (1..4).
-  static int max_stages = -1, forced_ctas = 0;
-  if (max_stages < 0) {
-    const char* e = getenv("CSA_T5_STAGES");
-    max_stages = e ? atoi(e) : 8;
-    if (max_stages < 2 || max_stages > 8) max_stages = 8;
-    const char* f = getenv("CSA_T5_CTAS");
-    forced_ctas = f ? atoi(f) : 0;
-    if (forced_ctas < 0 || forced_ctas > 4) forced_ctas = 0;
-  }
-  // FP8 keys: one CTA per SM (the converted buffers leave no room for a
-  // second CTA's ring)
   const bool fp8 = c.idx_fp8 != 0;
-  const int ctas_per_sm = forced_ctas ? forced_ctas : ((S <= 2 && !fp8) ? 2 : 1);
-  const int G = S < 4 ? S : 4;
-  int acc_cols = 32;
-  while (acc_cols < 64 * G) acc_cols <<= 1;  // power of two >= 32
-  int NB = 512 / ctas_per_sm / acc_cols;     // accumulators that fit in TMEM
-  if (NB > 8) NB = 8;
-  if (NB < 2) return -2;
-  const int per_cta = 228 * 1024 / ctas_per_sm - 1024;  // per-SM shared memory / CTAs
-  // key stages first: a CTA spans few requests, so a second q_idx buffer
-  // (prefetching the next request's queries) is kept only when it costs no
-  // key stage
-  const int stage_bytes = fp8 ? kStage8Bytes : kStageBytes;
-  // FP8: two converted items (measured: a third adds nothing)
-  const int NCB = fp8 ? kConvBufs : 0;
-  const int conv_bytes = NCB * kStageBytes;
-  const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4 - conv_bytes;
-  auto stages = [&](int nqb) {
-    const int n = (budget - nqb * qbytes) / stage_bytes;
-    return n > max_stages ? max_stages : n;
-  };
-  const int NQB = stages(2) >= stages(1) ? 2 : 1;
-  const int NST = stages(NQB);
-  if (NST < 2) return -2;
+  T5Plan p;
+  if (!plan_t5(c, S, &p)) return -2;
   if (fp8 && !b.idx_scale) return -1;
   CUtensorMap kmap, qmap;
   if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk, fp8))
     return -1;
   if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
-  const int smem = 1024 + NST * stage_bytes + conv_bytes + NQB * qbytes + S * kTcHi * 4;
+  const int smem = 1024 + p.NST * p.stage_bytes + p.conv_bytes + p.NQB * p.qbytes + S * kTcHi * 4;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(indexer_tc5_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -489,14 +514,15 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                          227 * 1024 - (int)sizeof(T5Smem));
     attr = true;
   }
-  int grid = num_sms * ctas_per_sm;
+  int grid = num_sms * p.ctas_per_sm;
   if (known > 0 && known < grid) grid = known;
   if (fp8)
     return launch_kernel(indexer_tc5_kernel<true>, dim3(grid), dim3(kT5ThreadsFp8), smem, st, pdl,
-                         kmap, qmap, items, c, b, ws, score_all, scores, ld, NST, NQB, acc_cols, NB,
-                         NCB);
+                         kmap, qmap, items, c, b, ws, score_all, scores, ld, p.NST, p.NQB,
+                         p.acc_cols, p.NB, p.NCB);
   return launch_kernel(indexer_tc5_kernel<false>, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap,
-                       qmap, items, c, b, ws, score_all, scores, ld, NST, NQB, acc_cols, NB, 0);
+                       qmap, items, c, b, ws, score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB,
+                       0);
 }
 
 }  // namespace csa

@@ -11,7 +11,7 @@
 namespace csa {
 
 __global__ void __launch_bounds__(1024) prep_kernel(DevCfg c, DevBatch b, Workspace ws,
-                                                    int score_all) {
+                                                    int score_all, int qsplit) {
   __shared__ int scan_tmp[33];
   __shared__ int carry;
   pdl_wait();
@@ -23,6 +23,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(DevCfg c, DevBatch b, Worksp
     if (bi < b.B) {
       const int L = b.ctx_len[bi];
       items = (request_rows(c, b.S, L, score_all) + kIdxChunk - 1) / kIdxChunk;
+      if (qsplit) items *= (b.S + qsplit - 1) / qsplit;  // (query group, key chunk) items
     }
     int total;
     const int ex = block_exclusive_scan(items, scan_tmp, &total);
@@ -35,9 +36,9 @@ __global__ void __launch_bounds__(1024) prep_kernel(DevCfg c, DevBatch b, Worksp
   pdl_trigger();
 }
 
-int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all,
+int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all, int qsplit,
                 cudaStream_t st, bool pdl) {
-  return launch_kernel(prep_kernel, dim3(1), dim3(1024), 0, st, pdl, c, b, ws, score_all);
+  return launch_kernel(prep_kernel, dim3(1), dim3(1024), 0, st, pdl, c, b, ws, score_all, qsplit);
 }
 
 }  // namespace csa

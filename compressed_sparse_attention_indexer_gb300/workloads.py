@@ -120,6 +120,11 @@ WORKLOADS = {
         L_range=(1024, 65536), seed=1003,
         description="long_ragged_b64 (same lengths and draws) with the indexer keys stored as "
                     "FP8 E4M3 codes and one fp32 scale per row"),
+    "prefill_b2_t512": Workload(
+        "prefill_b2_t512", BF16_CFG, B=2, S=512, L=4096, seed=1006,
+        description="a prefill chunk: B=2 requests, 512 new tokens each at the end of a 4096-token "
+                    "context (positions 3584..4095, vis 896..1024 > K), each token scoring its "
+                    "visible compressed rows and taking its own Top-K; H=64, D=576, bf16"),
     "multitoken_hca_b16_s8": Workload(
         "multitoken_hca_b16_s8", replace(BF16_CFG, hca_ratio=128), B=16, S=8, L=32768, seed=1004,
         description="B=16 S=8 L=32768 with per-query causal visibility; CSA (ratio 4, K=512, "

@@ -71,10 +71,11 @@ def check_against_oracle(wl, hb, g, ref=None, what=""):
 
 
 # ---------------------------------------------------------------------------
-# the five named workloads, full size
+# the named workloads, full size (prefill_b2_t512: a 512-token prefill chunk
+# per request, each token with its own visibility and Top-K)
 
 @pytest.mark.parametrize("name", ["tiny_f32", "bypass_b16_l256", "topk_b16_l8192",
-                                  "long_ragged_b64", "multitoken_hca_b16_s8"])
+                                  "long_ragged_b64", "multitoken_hca_b16_s8", "prefill_b2_t512"])
 def test_workload_decode_step(name):
     wl = WORKLOADS[name]
     hb = make_batch(wl)
