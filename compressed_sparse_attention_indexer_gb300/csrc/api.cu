@@ -99,9 +99,6 @@ int validate_cfg(const csa_config* c) {
       (c->dtype != CSA_DTYPE_BF16 || c->idx_heads != csa::kTcHi || c->idx_dim != csa::kTcDi))
     return fail(CSA_ERR_UNSUPPORTED, "FP8 indexer keys need dtype bf16, idx_heads %d, idx_dim %d",
                 csa::kTcHi, csa::kTcDi);
-  if (c->idx_dtype == CSA_DTYPE_FP8_E4M3 && c->max_queries_per_req > csa::indexer_fp8_max_queries())
-    return fail(CSA_ERR_UNSUPPORTED, "FP8 indexer keys support at most %d queries per request",
-                csa::indexer_fp8_max_queries());
   if (c->max_batch < 1 || c->max_queries_per_req < 1 || c->max_context < 1)
     return fail(CSA_ERR_INVALID_ARG, "workspace maxima must be >= 1");
   if (c->max_context / c->ratio > kMaxVisCap)

@@ -199,15 +199,16 @@ int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int sco
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
                    int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
                    bool pdl);
-int indexer_fp8_max_queries();
 bool indexer_tc5_fits(const DevCfg& c, int S);
-// warp-MMA indexer: queries per q_idx group; above it a request's work is
-// split by query group (see indexer_qsplit)
+// queries per group when a request's work is split by query group (see
+// indexer_qsplit): the warp-MMA indexer's q_idx group, and the tcgen05
+// indexer's unit (one MMA of N = 4 x 64 over a key chunk)
 constexpr int kMmaGroup = 8;
+constexpr int kT5Group = 4;
 int indexer_qsplit(const DevCfg& c, int S);
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
-                       int num_sms, cudaStream_t st, bool pdl);
+                       int num_sms, int qsplit, cudaStream_t st, bool pdl);
 // The cache update before a step: pool[slot[t]] = src[t] (row_bytes each) for
 // t < n; strides in bytes; status may be NULL.
 int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, int n, void* pool,

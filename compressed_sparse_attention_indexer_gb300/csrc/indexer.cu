@@ -270,16 +270,20 @@ bool tensor_core_shape(const DevCfg& c) {
          c.Hi == kTcHi && c.Di == kTcDi;
 }
 
-// Queries per work item of the warp-MMA indexer: a request with more than
-// kMmaGroup queries (a prefill chunk) has its work split by query group, so
-// that its key chunks x groups spread over the SMs; 0 keeps one item per key
-// chunk (all queries), which the tcgen05 kernel always uses.  The work list
-// and the kernel take the same value.
+// Queries per work item: 0 keeps one item per key chunk with all of the
+// request's queries.  A request whose queries do not fit the kernel at once (a
+// prefill chunk) has its work split by query group, items being (group, key
+// chunk) pairs that spread over the SMs: groups of kT5Group queries for the
+// tcgen05 kernel (the FP8 keys' only kernel), of kMmaGroup for the warp-MMA
+// one.  The work list and the kernel take the same value.
 int indexer_qsplit(const DevCfg& c, int S) {
-  if (c.idx_fp8 || c.dtype != CSA_DTYPE_BF16 || c.Hi != kTcHi || c.Di != kTcDi) return 0;
-  if (S <= kMmaGroup) return 0;
-  const bool tc5 = tensor_core_shape(c) && indexer_impl() == kIndexerTc5 && indexer_tc5_fits(c, S);
-  return tc5 ? 0 : kMmaGroup;
+  if (c.dtype != CSA_DTYPE_BF16 || c.Hi != kTcHi || c.Di != kTcDi) return 0;
+  if (c.idx_fp8 || (tensor_core_shape(c) && indexer_impl() == kIndexerTc5)) {
+    if (indexer_tc5_fits(c, S)) return 0;
+    if (S > kT5Group && indexer_tc5_fits(c, kT5Group)) return kT5Group;
+    if (c.idx_fp8) return 0;  // unreachable: kT5Group queries always fit
+  }
+  return S > kMmaGroup ? kMmaGroup : 0;
 }
 
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
@@ -287,12 +291,15 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
                    bool pdl) {
   const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;  // items, if known
   if (known == 0) return 0;
+  const int qsplit = indexer_qsplit(c, b.S);
   if (c.idx_fp8) {  // FP8 keys: the tcgen05 kernel only (its shape is checked at create)
-    const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, st, pdl);
+    const int r =
+        launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, qsplit, st, pdl);
     return r == -2 ? -1 : r;
   }
   if (tensor_core_shape(c) && indexer_impl() == kIndexerTc5) {
-    const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, st, pdl);
+    const int r =
+        launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, qsplit, st, pdl);
     if (r != -2) return r;  // -2: shape outside the tcgen05 kernel, use warp MMA
   }
   if (tensor_core_shape(c)) {
@@ -311,7 +318,7 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
     int grid = num_sms;
     if (known > 0 && known < grid) grid = known;
     return launch_kernel(indexer_mma_kernel, dim3(grid), dim3(kIdxThreads), smem, st, pdl, items,
-                         c, b, ws, score_all, scores, ld, SG, NST, indexer_qsplit(c, b.S));
+                         c, b, ws, score_all, scores, ld, SG, NST, qsplit);
   }
   int y = (c.max_vis + 7) / 8;
   if (y > 64) y = 64;

@@ -8,8 +8,11 @@
 // Persistent kernel, one CTA per SM, warp-specialised:
 //   warp 4  TMA producer: per work item (128 key rows of one request) two
 //           128x64 bf16 boxes, 128-byte swizzled, into a ring of stages;
-//           the request's q_idx (S queries x 64 heads x 128) when the
-//           request changes;
+//           the work unit's q_idx (its queries x 64 heads x 128) when the
+//           unit changes.  A unit is a request's S queries, or, for a
+//           request whose queries do not fit (a prefill chunk), a group of
+//           four of them: the request's items are then (group, key chunk)
+//           pairs, group major;
 //   warp 5  allocates TMEM; one thread issues the MMAs:
 //           D[128 rows x 64*G heads] = K_tile[128 x 128] . Q^T, M = 128,
 //           N = 64*G (G <= 4 queries per MMA), eight K = 16 steps, into one
@@ -20,7 +23,7 @@
 //           it reads that row's 64 head dot products of a query and sums
 //           w_h * ReLU(.) as four 16-head partials (h ascending within each),
 //           added in ascending order, then writes the score.  w of the
-//           request is cached in shared memory.
+//           unit is cached in shared memory.
 // HBM reads per item are the 32 KB of keys (q_idx comes from L2), so the
 // kernel runs at the HBM roofline when enough stages are in flight.
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -103,6 +106,35 @@ struct ReqCursor {
   }
 };
 
+// The work unit of the current item within its request: the unit's first
+// query g0, its su queries (all S, or a group of qsplit of them) in ngroups
+// MMA groups of G, and the item's key chunk.  Placed with one division when a
+// request starts, then advanced item by item.
+struct UnitCursor {
+  int S, SU, G, qsplit;
+  int chunk, chunks, g0, su, ngroups;
+  __device__ __forceinline__ void set_unit() {
+    su = min(SU, S - g0);
+    ngroups = (su + G - 1) / G;
+  }
+  // item li of a request of `nchunks` key chunks (1 without qsplit)
+  __device__ __forceinline__ void start(int li, int nchunks) {
+    chunks = nchunks;
+    const int gq = qsplit ? li / chunks : 0;
+    chunk = li - gq * chunks;
+    g0 = gq * SU;
+    set_unit();
+  }
+  // to the request's next item; true if that item starts a new unit
+  __device__ __forceinline__ bool step() {
+    if (++chunk < chunks || !qsplit) return false;
+    chunk = 0;
+    g0 += SU;
+    set_unit();
+    return true;
+  }
+};
+
 // kFp8: the key pool holds FP8 E4M3 rows with a per-row fp32 scale
 // (b.idx_scale).  Warps 6-13 then convert each item's FP8 tile (one TMA box)
 // into the bf16 tile layout the MMA reads, and the epilogue multiplies each
@@ -113,7 +145,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
                        const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
                        int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
-                       int acc_cols, int NB, int NCB) {
+                       int acc_cols, int NB, int NCB, int qsplit) {
   // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
   // MMAs run up to NB jobs ahead of the epilogue
   const uint32_t tmem_cols = (uint32_t)(NB * acc_cols);
@@ -123,8 +155,12 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
   const uint32_t kbuf = base;                                  // NST x 32 KB (FP8: 16 KB)
   const uint32_t stage_bytes = kFp8 ? kStage8Bytes : kStageBytes;
   const uint32_t cbuf = kbuf + (uint32_t)NST * stage_bytes;    // FP8: converted items
+  // Work unit: a request's queries, or with qsplit a group of qsplit of them
+  // (a prefill chunk); a request's items are then (group, key chunk) pairs,
+  // group major, and a unit's q_idx / w are loaded when the unit changes.
   const int S = b.S;
-  const uint32_t qbytes = (uint32_t)S * 2u * kQSubBytes;       // one request's q_idx
+  const int SU = qsplit ? qsplit : S;                          // queries per unit
+  const uint32_t qbytes = (uint32_t)SU * 2u * kQSubBytes;      // one unit's q_idx
   const uint32_t qbuf = cbuf + (kFp8 ? (uint32_t)NCB * kStageBytes : 0u);  // NQB x qbytes
   float* w_sm = reinterpret_cast<float*>(smem_raw + (qbuf + (uint32_t)NQB * qbytes - smem_u32(smem_raw)));
 
@@ -164,8 +200,16 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
   pdl_trigger();
   if (lo >= hi) return;
 
-  const int G = S < kMaxG ? S : kMaxG;
-  const int ngroups = (S + G - 1) / G;
+  const int G = SU < kMaxG ? SU : kMaxG;
+  // the request's key chunks, needed only to walk (group, key chunk) items
+  auto chunks_of = [&](int bi) {
+    return qsplit ? (request_rows(c, S, b.ctx_len[bi], score_all) + kIdxChunk - 1) / kIdxChunk : 1;
+  };
+  UnitCursor u;
+  u.S = S;
+  u.SU = SU;
+  u.G = G;
+  u.qsplit = qsplit;
   volatile int* abort = &sm.abort;
 
   if (warp == 5) {
@@ -185,16 +229,22 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       cur.init(prefix, b.B, lo);
       int64_t off = 0;
       for (int it = lo; it < hi && !*abort; ++it) {
-        if (cur.advance(it) || it == lo) {
+        bool new_unit = cur.advance(it) || it == lo;
+        if (new_unit) {
           off = b.idx_table ? 0 : b.idx_off[cur.bi];
+          u.start(it - cur.first, chunks_of(cur.bi));
+        } else {
+          new_unit = u.step();
+        }
+        if (new_unit) {
           const int qb = qc % NQB;
           if (qc >= NQB && !tc5::mbar_wait(smem_u32(&sm.qempty[qb]), ((qc / NQB) - 1) & 1, abort))
             break;
-          tc5::mbar_expect_tx(smem_u32(&sm.qfull[qb]), qbytes);
-          for (int s = 0; s < S; ++s)
+          tc5::mbar_expect_tx(smem_u32(&sm.qfull[qb]), (uint32_t)u.su * 2u * kQSubBytes);
+          for (int s = 0; s < u.su; ++s)
             for (int kt = 0; kt < 2; ++kt)
-              tc5::tma_load_2d(qbuf + qb * qbytes + kt * (S * kQSubBytes) + s * kQSubBytes, &qmap,
-                               kt * 64, (cur.bi * S + s) * kTcHi, smem_u32(&sm.qfull[qb]));
+              tc5::tma_load_2d(qbuf + qb * qbytes + kt * (SU * kQSubBytes) + s * kQSubBytes, &qmap,
+                               kt * 64, (cur.bi * S + u.g0 + s) * kTcHi, smem_u32(&sm.qfull[qb]));
           ++qc;
         }
         const int st = kc % NST;
@@ -203,7 +253,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
         // the item's first pool row; a paged pool's blocks hold whole items
         // (block a multiple of 128 rows), an unmapped block reads as zeros
         // past the pool (its rows are reported by the epilogue)
-        const int64_t c0 = (int64_t)(it - cur.first) * kIdxChunk;
+        const int64_t c0 = (int64_t)u.chunk * kIdxChunk;
         int64_t y0 = b.idx_table ? idx_row(b, cur.bi, c0) : off + c0;
         if (y0 < 0) y0 = b.idx_rows;
         const int y = (int)y0;
@@ -228,7 +278,12 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       ReqCursor cur;
       cur.init(prefix, b.B, lo);
       for (int it = lo; it < hi && !*abort; ++it) {
-        if (cur.advance(it) || it == lo) {
+        bool new_unit = cur.advance(it) || it == lo;
+        if (new_unit)
+          u.start(it - cur.first, chunks_of(cur.bi));
+        else
+          new_unit = u.step();
+        if (new_unit) {
           if (qc > 0) tc5::mma_commit(smem_u32(&sm.qempty[(qc - 1) % NQB]));
           const int qb = qc % NQB;
           if (!tc5::mbar_wait(smem_u32(&sm.qfull[qb]), (qc / NQB) & 1, abort)) break;
@@ -245,8 +300,8 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
         const uint32_t ka = kFp8 ? cbuf + cb * kStageBytes : kbuf + st * kStageBytes;
         const uint32_t qa = qbuf + ((qc - 1) % NQB) * qbytes;
         bool ok = true;
-        for (int g = 0; g < ngroups; ++g) {
-          const int gn = min(G, S - g * G);
+        for (int g = 0; g < u.ngroups; ++g) {
+          const int gn = min(G, u.su - g * G);
           const int tb = job % NB;
           if (job >= NB && !tc5::mbar_wait(smem_u32(&sm.tempty[tb]), ((job / NB) - 1) & 1, abort)) {
             ok = false;
@@ -259,7 +314,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
             const uint32_t off = (uint32_t)(k & 3) * 32u;
             const uint64_t ad = tc5::sdesc_k_sw128(ka + (k >> 2) * kSubBytes + off);
             const uint64_t bd =
-                tc5::sdesc_k_sw128(qa + (k >> 2) * (S * kQSubBytes) + g * G * kQSubBytes + off);
+                tc5::sdesc_k_sw128(qa + (k >> 2) * (SU * kQSubBytes) + g * G * kQSubBytes + off);
             tc5::mma_bf16(tmem + tb * acc_cols, ad, bd, idesc, k > 0 ? 1u : 0u);
           }
           tc5::mma_commit(smem_u32(&sm.tfull[tb]));
@@ -313,16 +368,23 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     int L = 0;
     int64_t off = 0;
     for (int it = lo; it < hi && !*abort; ++it) {
-      if (cur.advance(it) || it == lo) {
+      bool new_unit = cur.advance(it) || it == lo;
+      if (new_unit) {
         L = b.ctx_len[cur.bi];
         off = b.idx_table ? 0 : b.idx_off[cur.bi];
-        // the request's w (S x 64) into shared memory, shared by its items
+        u.start(it - cur.first, chunks_of(cur.bi));
+      } else {
+        new_unit = u.step();
+      }
+      if (new_unit) {
+        // the unit's w (su x 64) into shared memory, shared by its items
         named_barrier_sync(1, 128);
-        for (int v = row; v < S * kTcHi; v += 128) w_sm[v] = __ldg(b.w + (int64_t)cur.bi * S * kTcHi + v);
+        const float* wsrc = b.w + ((int64_t)cur.bi * S + u.g0) * kTcHi;
+        for (int v = row; v < u.su * kTcHi; v += 128) w_sm[v] = __ldg(wsrc + v);
         named_barrier_sync(1, 128);
       }
       const int bi = cur.bi;
-      const int c0 = (it - cur.first) * kIdxChunk;
+      const int c0 = u.chunk * kIdxChunk;
       const int64_t gr = b.idx_table ? idx_row(b, bi, c0 + row) : off + c0 + row;
       const bool in_pool = gr >= 0 && gr < b.idx_rows;
       // FP8: the row's scale (loaded ahead of the accumulator wait); only rows
@@ -330,8 +392,8 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       float ks = 1.f;
       if (kFp8 && in_pool && c0 + row < L / c.ratio) ks = __ldg(b.idx_scale + gr);
       bool ok = true;
-      for (int g = 0; g < ngroups; ++g) {
-        const int gn = min(G, S - g * G);
+      for (int g = 0; g < u.ngroups; ++g) {
+        const int gn = min(G, u.su - g * G);
         const int tb = job % NB;
         if (!tc5::mbar_wait(smem_u32(&sm.tfull[tb]), (job / NB) & 1, abort)) {
           ok = false;
@@ -339,8 +401,9 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
         }
         tc5::fence_after_sync();
         for (int sl = 0; sl < gn; ++sl) {
-          const int qid = bi * S + g * G + sl;
-          const QueryPlan p = query_plan(c, S, L, g * G + sl, score_all);
+          const int s = u.g0 + g * G + sl;  // query within the request
+          const int qid = bi * S + s;
+          const QueryPlan p = query_plan(c, S, L, s, score_all);
           if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
           const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + tb * acc_cols + sl * kTcHi;
           float v[64];
@@ -478,34 +541,27 @@ bool indexer_tc5_fits(const DevCfg& c, int S) {
   return plan_t5(c, S, &p);
 }
 
-// Largest queries per request the FP8 kernel (tcgen05 only) takes.
-int indexer_fp8_max_queries() {
-  DevCfg c = {};
-  c.idx_fp8 = 1;
-  for (int S = 64; S >= 1; --S)
-    if (indexer_tc5_fits(c, S)) return S;
-  return 0;
-}
-
 // Launches the tcgen05 indexer; returns 1 on launch, 0 with nothing to do,
 // -1 if the launch (or the tensor-map encoding) failed, -2 if the shape does
-// not fit this kernel (the caller then uses the warp-MMA kernel).
+// not fit this kernel (the caller then uses the warp-MMA kernel).  qsplit:
+// the work list's queries per item (0: all of a request's).
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
-                       int num_sms, cudaStream_t st, bool pdl) {
+                       int num_sms, int qsplit, cudaStream_t st, bool pdl) {
   const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;
   if (known == 0) return 0;
   if (b.idx_rows <= 0 || b.idx_rows > 0x7fffffffLL) return -2;
   const int S = b.S;
   const bool fp8 = c.idx_fp8 != 0;
+  const int SU = qsplit ? qsplit : S;  // queries per work unit
   T5Plan p;
-  if (!plan_t5(c, S, &p)) return -2;
+  if (!plan_t5(c, SU, &p)) return -2;
   if (fp8 && !b.idx_scale) return -1;
   CUtensorMap kmap, qmap;
   if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk, fp8))
     return -1;
   if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
-  const int smem = 1024 + p.NST * p.stage_bytes + p.conv_bytes + p.NQB * p.qbytes + S * kTcHi * 4;
+  const int smem = 1024 + p.NST * p.stage_bytes + p.conv_bytes + p.NQB * p.qbytes + SU * kTcHi * 4;
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(indexer_tc5_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -519,10 +575,10 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   if (fp8)
     return launch_kernel(indexer_tc5_kernel<true>, dim3(grid), dim3(kT5ThreadsFp8), smem, st, pdl,
                          kmap, qmap, items, c, b, ws, score_all, scores, ld, p.NST, p.NQB,
-                         p.acc_cols, p.NB, p.NCB);
+                         p.acc_cols, p.NB, p.NCB, qsplit);
   return launch_kernel(indexer_tc5_kernel<false>, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap,
                        qmap, items, c, b, ws, score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB,
-                       0);
+                       0, qsplit);
 }
 
 }  // namespace csa

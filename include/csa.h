@@ -110,8 +110,7 @@ typedef struct {
      * cache as a key pool plus a per-row scale pool ("Fix: complete DeepSeek
      * V4 TP CSA decode", PR description: idx_kv_cache and idx_kv_scale); the
      * element format is this library's choice.  FP8 keys need dtype bf16,
-     * idx_heads 64 and idx_dim 128 (the tcgen05 indexer) and a
-     * max_queries_per_req small enough for its shared memory (7), else
+     * idx_heads 64 and idx_dim 128 (the tcgen05 indexer), else
      * CSA_ERR_UNSUPPORTED.  The score is unchanged:
      * score_j = sum_h w_h * ReLU(q_idx[h] . key_j). */
     int32_t idx_dtype;
