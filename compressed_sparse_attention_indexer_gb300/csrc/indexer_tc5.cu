@@ -139,13 +139,16 @@ struct UnitCursor {
 // (b.idx_scale).  Warps 6-13 then convert each item's FP8 tile (one TMA box)
 // into the bf16 tile layout the MMA reads, and the epilogue multiplies each
 // row's dot products by its scale before the ReLU.
-template <bool kFp8>
+// kSplit: the work list splits requests by query group (qsplit queries per
+// unit); without it the unit bookkeeping folds away.
+template <bool kFp8, bool kSplit>
 __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     indexer_tc5_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
                        int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
-                       int acc_cols, int NB, int NCB, int qsplit) {
+                       int acc_cols, int NB, int NCB, int qsplit_arg) {
+  const int qsplit = kSplit ? qsplit_arg : 0;
   // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
   // MMAs run up to NB jobs ahead of the epilogue
   const uint32_t tmem_cols = (uint32_t)(NB * acc_cols);
@@ -564,21 +567,22 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   const int smem = 1024 + p.NST * p.stage_bytes + p.conv_bytes + p.NQB * p.qbytes + SU * kTcHi * 4;
   static bool attr = false;
   if (!attr) {
-    cudaFuncSetAttribute(indexer_tc5_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         227 * 1024 - (int)sizeof(T5Smem));
-    cudaFuncSetAttribute(indexer_tc5_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         227 * 1024 - (int)sizeof(T5Smem));
+    const int max_dyn = 227 * 1024 - (int)sizeof(T5Smem);
+    cudaFuncSetAttribute(indexer_tc5_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+    cudaFuncSetAttribute(indexer_tc5_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+    cudaFuncSetAttribute(indexer_tc5_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
+    cudaFuncSetAttribute(indexer_tc5_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
     attr = true;
   }
   int grid = num_sms * p.ctas_per_sm;
   if (known > 0 && known < grid) grid = known;
-  if (fp8)
-    return launch_kernel(indexer_tc5_kernel<true>, dim3(grid), dim3(kT5ThreadsFp8), smem, st, pdl,
-                         kmap, qmap, items, c, b, ws, score_all, scores, ld, p.NST, p.NQB,
-                         p.acc_cols, p.NB, p.NCB, qsplit);
-  return launch_kernel(indexer_tc5_kernel<false>, dim3(grid), dim3(kT5Threads), smem, st, pdl, kmap,
-                       qmap, items, c, b, ws, score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB,
-                       0, qsplit);
+  const dim3 block(fp8 ? kT5ThreadsFp8 : kT5Threads);
+  auto go = [&](auto kernel) {
+    return launch_kernel(kernel, dim3(grid), block, smem, st, pdl, kmap, qmap, items, c, b, ws,
+                         score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB, p.NCB, qsplit);
+  };
+  if (fp8) return qsplit ? go(indexer_tc5_kernel<true, true>) : go(indexer_tc5_kernel<true, false>);
+  return qsplit ? go(indexer_tc5_kernel<false, true>) : go(indexer_tc5_kernel<false, false>);
 }
 
 }  // namespace csa
