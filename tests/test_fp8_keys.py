@@ -82,6 +82,13 @@ def test_fp8_host_check_codes(L, cfg_kw, batch_kw, code):
     assert csa.last_error()
 
 
+def test_fp8_keys_take_prefill_chunks(L):
+    # a request's queries beyond what the tcgen05 indexer holds at once are
+    # split into query groups, so FP8 keys take any queries per request
+    assert check(_cfg(max_queries_per_req=512), _batch(S=512)) == csa.CSA_OK
+    assert check(_cfg(max_queries_per_req=13), _batch(S=13)) == csa.CSA_OK
+
+
 def test_bf16_keys_ignore_the_scale_pointer(L):
     assert check(_cfg(idx_dtype=0), _batch(idx_scale=None, idx_stride=128)) == csa.CSA_OK
 
