@@ -191,9 +191,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if (tid == 0) cnt_out[q] = K;
 }
 
-// Register-resident variant for rows of at most kRegMax keys (the common
+// Register-resident variant for rows of at most kJ * 1024 keys (the common
 // case: max_context / ratio <= 16384).  Thread t holds keys t + 1024 j,
-// j < 16, in registers for the whole selection.  The result is defined by a
+// j < kJ, in registers for the whole selection: kJ = 16, or kJ = 2 for rows
+// of at most 2048 keys (short contexts, prefill chunks), whose smaller
+// register footprint fits two blocks per SM.  The result is defined by a
 // threshold pair (tkey, tidx): the K-th entry in the order (key descending,
 // index ascending); a key is selected iff it precedes or is that entry.
 //   1. radix passes as above (histogram of the next digit among keys that
@@ -207,12 +209,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 //      threshold index is the need-th of them in index order, from per-row
 //      ballots and one block scan;
 //   4. output: per (row j, warp) ballots of the selection, one block scan over
-//      the 512 counts in index order, and each selected key writes its index
-//      at its position, so the output is in ascending index order.
-constexpr int kRegKeys = 16;
+//      the kJ * 32 counts in index order, and each selected key writes its
+//      index at its position, so the output is in ascending index order.
+constexpr int kRegKeys = 16;  // keys per thread of the long-row instantiation
 constexpr int kRegMax = kRegKeys * kTopkThreads;
-constexpr int kRows = kRegKeys * 32;  // (row j, warp) pairs, in index order
-constexpr int kCand = kTopkThreads;   // candidates ranked directly
+constexpr int kShortKeys = 2;  // keys per thread of the short-row one
+constexpr int kCand = kTopkThreads;  // candidates ranked directly
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -220,11 +222,13 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1)
+template <int kJ>
+__global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     topk_reg_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
                     const int* __restrict__ n_override, int* __restrict__ idx_out,
                     int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
                     int early) {
+  constexpr int kRows = kJ * 32;  // (row j, warp) pairs, in index order
   __shared__ int hist[kBins];
   __shared__ uint32_t cand_key[kCand];
   __shared__ int cand_idx[kCand];
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     if (!early) plan_len();
     if (bad && tid == 0) set_status(status, kStatusBadIndex);
   }
-  if (n > kRegMax) {  // the launcher picks this kernel only when max_vis <= kRegMax
+  if (n > kJ * kTopkThreads) {  // the launcher picks this kernel only for rows that fit
     if (tid == 0) set_status(status, kStatusBadIndex);
     n = 0;
   }
@@ -278,17 +282,17 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if (tid == 0) s_ncand = 0;
   // keys in registers (all sixteen loads in flight), and the OR / AND over
   // the row: bits where they differ are the ones still to decide
-  uint32_t k[kRegKeys];
+  uint32_t k[kJ];
   uint32_t vmask = 0u, aor = 0u, aand = ~0u;
   {
-    float v[kRegKeys];
+    float v[kJ];
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) {
+    for (int j = 0; j < kJ; ++j) {
       const int i = j * kTopkThreads + tid;
       v[j] = i < n ? __ldg(sc + i) : 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) {
+    for (int j = 0; j < kJ; ++j) {
       k[j] = score_key_fast(v[j]);
       if (j * kTopkThreads + tid < n) {
         vmask |= 1u << j;
@@ -331,11 +335,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     __syncthreads();
     if (first_pass) {  // every key shares the common prefix
 #pragma unroll
-      for (int j = 0; j < kRegKeys; ++j)
+      for (int j = 0; j < kJ; ++j)
         if ((vmask >> j) & 1u) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
     } else {  // start < 32 after a pass
 #pragma unroll
-      for (int j = 0; j < kRegKeys; ++j)
+      for (int j = 0; j < kJ; ++j)
         if (((vmask >> j) & 1u) && (k[j] >> start) == prefix) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
     }
     __syncthreads();
@@ -379,7 +383,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if (mode == 2) {
     // compact the keys that match the prefix, then rank each among them
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) {
+    for (int j = 0; j < kJ; ++j) {
       const bool m = ((vmask >> j) & 1u) && (k[j] >> start) == prefix;  // start < 32 here
       const uint32_t bal = __ballot_sync(0xffffffffu, m);
       if (bal) {
@@ -414,7 +418,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     // start == 0: more than kCand keys equal `prefix` and `need` of them are
     // kept, the lowest indices first
 #pragma unroll
-    for (int j = 0; j < kRegKeys; ++j) {
+    for (int j = 0; j < kJ; ++j) {
       const uint32_t bal = __ballot_sync(0xffffffffu, ((vmask >> j) & 1u) && k[j] == prefix);
       if (lane == 0) rowbits[j * 32 + warp] = bal;
     }
@@ -435,7 +439,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   // selection: keys before the threshold in (key desc, index asc) order
   uint32_t smask = 0u;
 #pragma unroll
-  for (int j = 0; j < kRegKeys; ++j) {
+  for (int j = 0; j < kJ; ++j) {
     const int i = j * kTopkThreads + tid;
     const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
     smask |= (uint32_t)sel << j;
@@ -481,9 +485,10 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
   DevBatch none = {};
   none.S = 1;
   if (topk_use_reg(max_vis))
-    return launch_kernel(topk_reg_kernel, dim3(nq), dim3(kTopkThreads), 0, st, pdl, c,
-                         b ? *b : none, scores, ld, n_override, idx_out, cnt_out, status, max_vis,
-                         (pdl && early) ? 1 : 0);
+    return launch_kernel(max_vis <= kShortKeys * kTopkThreads ? topk_reg_kernel<kShortKeys>
+                                                              : topk_reg_kernel<kRegKeys>,
+                         dim3(nq), dim3(kTopkThreads), 0, st, pdl, c, b ? *b : none, scores, ld,
+                         n_override, idx_out, cnt_out, status, max_vis, (pdl && early) ? 1 : 0);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
   static int attr_smem = 0;
   if (smem > 48 * 1024 && smem > attr_smem) {

@@ -200,6 +200,32 @@ def test_topk_select_bit_exact():
         assert (gi[i, ref.size:] == -1).all()
 
 
+def test_topk_select_bit_exact_short_rows():
+    # max_context / ratio <= 2048: the register kernel with two keys per thread
+    rng = np.random.default_rng(2026)
+    cfg = BF16_CFG
+    cases = [(name, s) for name, s in _topk_cases(rng) if s.size <= 2048]
+    cases.append(("full_2048_ties", (np.round(rng.standard_normal(2048) * 2) / 2).astype(np.float32)))
+    cases.append(("all_equal_2048", np.full(2048, 0.75, np.float32)))
+    dec = csa.Decoder(cfg, len(cases), 1, 8192)
+    ld = 2048
+    sc = np.full((len(cases), ld), np.nan, np.float32)
+    n = np.zeros(len(cases), np.int32)
+    for i, (_, s) in enumerate(cases):
+        sc[i, :s.size] = s
+        n[i] = s.size
+    idx = torch.empty(len(cases), cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(len(cases), dtype=torch.int32, device=DEV)
+    dec.topk_select(torch.from_numpy(sc).to(DEV), torch.from_numpy(n).to(DEV), idx, cnt)
+    assert dec.status() == csa.CSA_OK
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    for i, (name, s) in enumerate(cases):
+        ref = oracle.topk(s.astype(np.float64), cfg.topk)
+        assert gc[i] == ref.size, name
+        assert gi[i, :ref.size].tolist() == ref.tolist(), f"{name} n={s.size}"
+        assert (gi[i, ref.size:] == -1).all()
+
+
 def test_topk_select_bit_exact_rows_past_16384():
     # max_context / ratio above 16384: the shared-memory Top-K kernel
     rng = np.random.default_rng(2025)
