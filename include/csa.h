@@ -23,7 +23,9 @@
  *       and packing", PR description).
  *
  * Definitions used throughout (query s of request b, context length L_b
- * including the S new tokens):
+ * including the S new tokens; S = 1 is single-token decode, a few tokens are
+ * multi-token decode, and a prefill chunk of T tokens is S = T, each token
+ * with its own visibility and Top-K):
  *   pos  = L_b - S + s                (0-based position of the query)
  *   vis  = floor((pos + 1) / ratio)   (compressed rows whose raw span ends at or before pos)
  *   nwin = min(WIN, pos + 1)          (window = raw rows pos-nwin+1 .. pos)
