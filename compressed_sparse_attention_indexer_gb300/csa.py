@@ -22,7 +22,8 @@ ERROR_NAMES = {0: "CSA_OK", 1: "CSA_ERR_INVALID_ARG", 2: "CSA_ERR_UNSUPPORTED", 
 EXPORTS = ("csa_decode_create", "csa_decode_destroy", "csa_indexer_topk", "csa_sparse_attn",
            "csa_decode_step", "csa_indexer_scores", "csa_topk_select", "csa_check_batch",
            "csa_get_status", "csa_last_error", "csa_last_launch_count", "csa_abi_version",
-           "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static", "csa_cache_writeback")
+           "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static", "csa_cache_writeback",
+           "csa_debug_set_wait_polls")
 STAGES = ("plan", "indexer", "topk", "attention")
 
 
@@ -95,6 +96,7 @@ def lib(path: str | None = None):
             L.csa_abi_version.restype = i32
             L.csa_profile_enable.argtypes = [H, i32]
             L.csa_profile_read.argtypes = [H, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(i32)]
+            L.csa_debug_set_wait_polls.argtypes = [H, i32]
             L.csa_indexer_topk_static.argtypes = [ctypes.POINTER(CConfig), ctypes.POINTER(CBatch), vp,
                                                   vp, vp, vp]
             L.csa_cache_writeback.argtypes = [vp, ctypes.c_int64, vp, i32, vp, ctypes.c_int64,
@@ -102,7 +104,7 @@ def lib(path: str | None = None):
             for name in ("csa_decode_create", "csa_indexer_topk", "csa_sparse_attn", "csa_decode_step",
                          "csa_indexer_scores", "csa_topk_select", "csa_check_batch", "csa_get_status",
                          "csa_profile_enable", "csa_profile_read", "csa_indexer_topk_static",
-                         "csa_cache_writeback"):
+                         "csa_cache_writeback", "csa_debug_set_wait_polls"):
                 getattr(L, name).restype = ctypes.c_int
             _lib = L
     return _lib
@@ -239,6 +241,11 @@ class Decoder:
 
     def last_launch_count(self) -> int:
         return lib().csa_last_launch_count(self.handle)
+
+    def debug_wait_polls(self, polls: int):
+        """Test hook: the attention tile kernel's consumer waits give up after
+        `polls` polls (0: at once); negative restores the default."""
+        _check(lib().csa_debug_set_wait_polls(self.handle, int(polls)))
 
     def profile(self, enable: bool):
         _check(lib().csa_profile_enable(self.handle, 1 if enable else 0))

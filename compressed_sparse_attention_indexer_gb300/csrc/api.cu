@@ -10,6 +10,8 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+
 #include "csa_internal.cuh"
 
 struct csa_handle {
@@ -264,9 +266,14 @@ struct Launches {
   }
 };
 
+thread_local std::string g_launch_why;  // see csa::launch_fail
+
 int finish(csa_handle* h, const Launches& L) {
   h->last_launches = L.n;
+  std::string why;
+  why.swap(g_launch_why);
   if (!L.ok) {
+    if (!why.empty()) return fail(CSA_ERR_CUDA, "kernel launch: %s", why.c_str());
     cudaError_t e = cudaGetLastError();
     return cuda_fail(e, "kernel launch");
   }
@@ -298,10 +305,49 @@ void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-constexpr int kMaxStaticDevices = 64;
+// The array's device address is a property of the CUDA context the module is
+// loaded in: normally one (the primary context) per device, but a device reset
+// or a driver-API context made current loads the module again, possibly at
+// another address.  The address is therefore kept per context, keyed by the
+// context's unique id, and looked up the first time a context calls in.
+struct StaticSlot {
+  unsigned long long ctx_id;
+  void* addr;
+  int sms;
+};
+constexpr int kMaxStaticContexts = 64;
 std::mutex g_static_mu;
-void* g_static_addr[kMaxStaticDevices];  // device address of g_static_scratch, per device
-int g_static_sms[kMaxStaticDevices];
+StaticSlot g_static_slots[kMaxStaticContexts];
+int g_static_nslots = 0;
+
+// Unique id of the calling thread's current context (cuCtxGetCurrent and
+// cuCtxGetId, through the runtime's driver entry points so that nothing links
+// the driver library directly).  After a runtime call has run on the current
+// device (cudaGetDevice does not create a context, the caller's cudaSetDevice
+// or any earlier call does), its primary context is current.  False if the
+// driver lacks the calls or no context is current.
+bool current_context_id(unsigned long long* id) {
+  typedef CUresult (*GetCurrent)(CUcontext*);
+  typedef CUresult (*GetId)(CUcontext, unsigned long long*);
+  static const GetCurrent get_current = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    return (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess && r == cudaDriverEntryPointSuccess)
+               ? reinterpret_cast<GetCurrent>(p) : nullptr;
+  }();
+  static const GetId get_id = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    return (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &r) ==
+                cudaSuccess && r == cudaDriverEntryPointSuccess)
+               ? reinterpret_cast<GetId>(p) : nullptr;
+  }();
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 // The config as the kernels read it (what csa_decode_create stores in a
 // handle).
@@ -315,6 +361,7 @@ csa::DevCfg static_devcfg(const csa_config& c) {
   d.rope_base = c.rope_base;
   d.max_context = c.max_context;
   d.max_vis = c.max_context / c.ratio;
+  d.wait_polls = -1;
   for (int i = 0; i < csa::kRopeTable; ++i)
     d.rope_theta[i] = (d.R > 0 && i < d.R / 2)
                           ? pow((double)c.rope_base, -2.0 * (double)i / (double)d.R) : 0.0;
@@ -333,6 +380,19 @@ size_t static_scratch_need(const csa_config& c, const csa_batch* b, size_t* o_pr
 }
 
 }  // namespace
+
+namespace csa {
+int launch_fail(const char* what, cudaError_t e) {
+  if (g_launch_why.empty()) {  // the first failure of a call is the one to report
+    g_launch_why = what;
+    if (e != cudaSuccess) {
+      g_launch_why += ": ";
+      g_launch_why += cudaGetErrorString(e);
+    }
+  }
+  return -1;
+}
+}  // namespace csa
 
 extern "C" {
 
@@ -357,6 +417,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   d.rope_base = cfg->rope_base;
   d.max_context = cfg->max_context;
   d.max_vis = cfg->max_context / cfg->ratio;
+  d.wait_polls = -1;
   for (int i = 0; i < csa::kRopeTable; ++i)
     d.rope_theta[i] = (d.R > 0 && i < d.R / 2)
                           ? pow((double)cfg->rope_base, -2.0 * (double)i / (double)d.R) : 0.0;
@@ -378,7 +439,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   const bool tc = csa::tensor_core_shape(d);
   h->max_jobs = tc ? csa::max_jobs_per_query(d) : 0;
   const size_t o_jobs = off; off += al(sizeof(int) * (maxT + 1));
-  const size_t o_part = off; off += tc ? al(sizeof(__half) * (size_t)maxT * h->max_jobs * d.H * d.V) : 0;
+  const size_t o_part = off; off += tc ? al(sizeof(__nv_bfloat16) * (size_t)maxT * h->max_jobs * d.H * d.V) : 0;
   const size_t o_plse = off; off += tc ? al(sizeof(float) * (size_t)maxT * h->max_jobs * d.H) : 0;
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws_base, off);
@@ -393,7 +454,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   w.topk_idx = reinterpret_cast<int*>(base + o_idx);
   w.topk_cnt = reinterpret_cast<int*>(base + o_cnt);
   w.job_prefix = reinterpret_cast<int*>(base + o_jobs);
-  w.part_o = tc ? reinterpret_cast<__half*>(base + o_part) : nullptr;
+  w.part_o = tc ? reinterpret_cast<__nv_bfloat16*>(base + o_part) : nullptr;
   w.part_lse = tc ? reinterpret_cast<float*>(base + o_plse) : nullptr;
   w.max_T = maxT;
   w.max_batch = cfg->max_batch;
@@ -518,29 +579,53 @@ int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* 
                 "B*S = %d queries x max_context/ratio = %d scores need %zu bytes of scratch, above "
                 "the %zu bytes of the allocation-free entry point (use csa_indexer_topk)",
                 b->B * b->S, cfg->max_context / cfg->ratio, need, kStaticScratchBytes);
-  // set-up, once per device: the scratch array's address and the SM count
+  // set-up, once per context (normally once per device), with the device
+  // current: the scratch array's address and the SM count
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxStaticDevices)
-    return fail(CSA_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxStaticDevices - 1);
+  unsigned long long ctx = 0;
+  void* looked_up = nullptr;
+  if (!current_context_id(&ctx)) {
+    // no context is current on this thread yet: the lookup, a runtime call
+    // that needs one, makes the device's primary context current
+    e = cudaGetSymbolAddress(&looked_up, g_static_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    if (!current_context_id(&ctx))
+      return fail(CSA_ERR_CUDA, "no current CUDA context (cuCtxGetCurrent / cuCtxGetId)");
+  }
   void* base = nullptr;
   int sms = 0;
   {
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_addr[dev]) {
-      void* a = nullptr;
-      e = cudaGetSymbolAddress(&a, g_static_scratch);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
-      e = cudaDeviceGetAttribute(&g_static_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    int k = 0;
+    while (k < g_static_nslots && g_static_slots[k].ctx_id != ctx) ++k;
+    if (k == g_static_nslots) {
+      if (k == kMaxStaticContexts)
+        return fail(CSA_ERR_UNSUPPORTED, "more than %d CUDA contexts used the allocation-free entry point",
+                    kMaxStaticContexts);
+      void* a = looked_up;
+      if (!a) {
+        e = cudaGetSymbolAddress(&a, g_static_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+      }
+      int n = 0;
+      e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-      g_static_addr[dev] = a;
+      g_static_slots[k] = StaticSlot{ctx, a, n};
+      g_static_nslots = k + 1;
     }
-    base = g_static_addr[dev];
-    sms = g_static_sms[dev];
+    base = g_static_slots[k].addr;
+    sms = g_static_slots[k].sms;
   }
-  if (b->B == 0) return CSA_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (b->B == 0) {  // nothing to select: the status reads clean
+    if (status_out) {
+      e = cudaMemsetAsync(status_out, 0, sizeof(int32_t), st);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(status_out)");
+    }
+    return CSA_OK;
+  }
   char* sb = static_cast<char*>(base);
   // a handle on the stack that borrows the static scratch: the same launch
   // sequence as csa_indexer_topk, with no workspace of its own
@@ -594,9 +679,18 @@ int csa_cache_writeback(const void* rows, int64_t rows_stride, const int64_t* sl
   if (rows_stride < row_bytes || pool_stride < row_bytes)
     return fail(CSA_ERR_INVALID_ARG, "a stride below row_bytes");
   if (csa::launch_writeback(rows, rows_stride, slot, n, pool, pool_stride, pool_rows, row_bytes,
-                            status, static_cast<cudaStream_t>(stream), false) < 0)
-    return cuda_fail(cudaGetLastError(), "kernel launch");
+                            status, static_cast<cudaStream_t>(stream), false) < 0) {
+    std::string why;
+    why.swap(g_launch_why);
+    return fail(CSA_ERR_CUDA, "kernel launch: %s", why.empty() ? "failed" : why.c_str());
+  }
   g_err.clear();
+  return CSA_OK;
+}
+
+int csa_debug_set_wait_polls(csa_handle* h, int32_t polls) {
+  if (!h) return fail(CSA_ERR_INVALID_ARG, "handle is NULL");
+  h->dc.wait_polls = polls < 0 ? -1 : polls;
   return CSA_OK;
 }
 

@@ -489,11 +489,10 @@ __global__ void __launch_bounds__(256) attn_simt_kernel(DevCfg c, DevBatch b, Wo
 // merge by default (measured faster); CSA_ATTN=mma selects the warp-MMA
 // kernel.
 int attention_impl() {
-  static int impl = -1;
-  if (impl < 0) {
+  static const int impl = [] {
     const char* e = getenv("CSA_ATTN");
-    impl = (e && strcmp(e, "mma") == 0) ? kAttnMma : kAttnTc5;
-  }
+    return (e && strcmp(e, "mma") == 0) ? kAttnMma : kAttnTc5;
+  }();
   return impl;
 }
 
@@ -504,11 +503,11 @@ int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, co
   const int T = b.B * b.S;
   if (T == 0) return 0;
   if (tensor_core_shape(c)) {
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmem);
-      attr_done = true;
-    }
+    static PerDeviceOnce attr;
+    if (const cudaError_t e = attr.run([] {
+          return allow_max_dynamic_smem(attn_tc_kernel);
+        }))
+      return launch_fail("cudaFuncSetAttribute(attn_tc_kernel)", e);
     return launch_kernel(attn_tc_kernel, dim3(T * 2), dim3(kAttnThreads), kAttnSmem, st, pdl, c, b,
                          ws, topk_idx, topk_cnt, static_cast<__nv_bfloat16*>(out), lse_out);
   }

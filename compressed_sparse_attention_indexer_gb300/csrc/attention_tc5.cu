@@ -32,7 +32,7 @@
 //            tile max exceeds it by 2^8 (then O^T is rescaled in TMEM by all
 //            128 threads), write the head's row of P^T as bf16 and sum the
 //            rounded weights.  At a segment's end all four warps read O^T
-//            (thread = dim) and write the normalised partial output (fp16,
+//            (thread = dim) and write the normalised partial output (bf16,
 //            heads x dims) and the heads' log-sum-exp to the workspace.
 // attn_merge_kernel: per query and 64 output dims, the log-sum-exp merge of
 // the query's segments in job order, inverse RoPE on the last R dims, the
@@ -74,6 +74,7 @@ struct __align__(16) A5Smem {
   // job n's PV first
   uint64_t p_full[2];
   uint64_t pv_done, o_full, o_empty, qfull, qdone, done;
+  uint64_t sbar;                   // the softmax warps' bounded barrier
   uint32_t tmem_base;
   int abort;
   int flag[2][4];                  // per job parity and warp: some head needs a rescale
@@ -243,6 +244,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   pdl_trigger();
   if (lo >= hi) return;
   volatile int* abort = &sm.abort;
+  // polls before a consumer wait gives up (the default: about a second)
+  const uint32_t wpolls = c.wait_polls < 0 ? tc5::kBackoffPolls : (uint32_t)c.wait_polls;
 
   if (warp == 4) {
     tc5::tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -264,6 +267,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     tc5::mbar_init(smem_u32(&sm.qfull), 1);
     tc5::mbar_init(smem_u32(&sm.qdone), 1);
     tc5::mbar_init(smem_u32(&sm.done), 1);
+    tc5::mbar_init(smem_u32(&sm.sbar), 128);
     sm.abort = 0;
     tc5::fence_mbar_init();
   }
@@ -331,8 +335,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       }
       bool ok = true;
       if (lane == 0) {
-        if (m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.empty[g]), (m - 1) & 1, abort, 256)) ok = false;
-        if (ok && m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.mempty[g]), (m - 1) & 1, abort, 256)) ok = false;
+        if (m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.empty[g]), (m - 1) & 1, abort, 256, wpolls)) ok = false;
+        if (ok && m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.mempty[g]), (m - 1) & 1, abort, 256, wpolls)) ok = false;
         if (ok) {
           sm.mask[g][lw] = bits;
           tc5::mbar_arrive(smem_u32(&sm.mfull[g]));
@@ -478,18 +482,19 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     JobCursor cur;
     cur.init(prefix, T, lo);
     int n = 0, seg = 0, slot = lo;
+    uint32_t sphase = 0;
     for (int job = lo; job < hi && !*abort; ++job, ++n) {
       cur.advance(job);
       const bool first = job == lo || job == cur.first;
       const bool last = job + 1 == hi || job + 1 == cur.end;
       if (first) slot = job;
       const int g = n & 1, m = n >> 1;
-      if (!tc5::mbar_wait_backoff(smem_u32(&sm.mfull[g]), m & 1, abort, 64)) break;
+      if (!tc5::mbar_wait_backoff(smem_u32(&sm.mfull[g]), m & 1, abort, 64, wpolls)) break;
       uint64_t mk = 0;
 #pragma unroll
       for (int w = 0; w < kLoadWarps; ++w) mk |= sm.mask[g][w];
       tc5::mbar_arrive(smem_u32(&sm.mempty[g]));
-      if (!tc5::mbar_wait_backoff(smem_u32(&sm.s_full[g]), m & 1, abort, 64)) break;
+      if (!tc5::mbar_wait_backoff(smem_u32(&sm.s_full[g]), m & 1, abort, 64, wpolls)) break;
       tc5::fence_after_sync();
       float s[64];
       tc5::tmem_ld32x2(tmem + kTmemS + 64 * g + lanes, s, s + 32);
@@ -542,11 +547,12 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       }
       const bool any = __any_sync(0xffffffffu, owner && resc);
       if (lane == 0) sm.flag[g][warp] = any ? 1 : 0;
-      named_barrier_sync(1, 128);
+      // (a bounded barrier: a warp that gave up a wait must not strand the others)
+      if (!tc5::bar_bounded(smem_u32(&sm.sbar), sphase, abort)) break;
       if (sm.flag[g][0] | sm.flag[g][1] | sm.flag[g][2] | sm.flag[g][3]) {
         // O^T of the segment so far, times 2^(m_old - m_new) per head (column),
         // once the previous job's PV is complete; thread = TMEM lane = dim
-        if (!tc5::mbar_wait_backoff(smem_u32(&sm.pv_done), (n - 1) & 1, abort, 64)) break;
+        if (!tc5::mbar_wait_backoff(smem_u32(&sm.pv_done), (n - 1) & 1, abort, 64, wpolls)) break;
         tc5::fence_after_sync();
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
@@ -578,12 +584,14 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         if (owner) {
           ws.part_lse[(int64_t)slot * kTcH + h] = lrun > 0.f ? mref + log2f(lrun) : -INFINITY;
         }
-        if (!tc5::mbar_wait_backoff(smem_u32(&sm.o_full), seg & 1, abort, 64)) break;
+        if (!tc5::mbar_wait_backoff(smem_u32(&sm.o_full), seg & 1, abort, 64, wpolls)) break;
         tc5::fence_after_sync();
-        // heads x dims, fp16: lanes 2i and 2i+1 swap values so that each
+        // heads x dims, bf16 (the range of fp32: a partial is a convex
+        // combination of value rows, which may be any bf16 magnitude; fp16
+        // would overflow past 65504): lanes 2i and 2i+1 swap values so that each
         // holds dims 2i, 2i+1 of one head of a pair (j, j+1); a warp store
         // covers 32 consecutive dims of two heads (two 64-byte runs)
-        __half* po = ws.part_o + (int64_t)slot * kTcH * kTcV;
+        __nv_bfloat16* po = ws.part_o + (int64_t)slot * kTcH * kTcV;
         const bool odd = lane & 1;
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
@@ -601,15 +609,15 @@ __global__ void __launch_bounds__(kA5Threads, 1)
             float o[32];
             tc5::tmem_ld32(tmem + kTmemO + 64 * cc + 32 * half + lanes, o);
             const int d0 = cc * 128 + warp * 32 + (lane & ~1);  // the pair's first dim
-            __half* row = po + (int64_t)(32 * half + (odd ? 1 : 0)) * kTcV + d0;
+            __nv_bfloat16* row = po + (int64_t)(32 * half + (odd ? 1 : 0)) * kTcV + d0;
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
               // even lane keeps head j, odd lane head j+1; each sends the other
               const float mine = odd ? o[j + 1] * inv[j + 1] : o[j] * inv[j];
               const float give = odd ? o[j] * inv[j] : o[j + 1] * inv[j + 1];
               const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-              *reinterpret_cast<__half2*>(row + (int64_t)j * kTcV) =
-                  odd ? __floats2half2_rn(got, mine) : __floats2half2_rn(mine, got);
+              *reinterpret_cast<__nv_bfloat162*>(row + (int64_t)j * kTcV) =
+                  odd ? __floats2bfloat162_rn(got, mine) : __floats2bfloat162_rn(mine, got);
             }
           }
         }
@@ -733,7 +741,7 @@ __global__ void __launch_bounds__(256, 4)
     for (int kk = 0; kk < kMergeUnroll; ++kk) {
       const float w = (M == -INFINITY || lk[kk] == -INFINITY) ? 0.f : exp2f(lk[kk] - M);
       tot += w;
-      const __half2* a = reinterpret_cast<const __half2*>(&u[kk][0]);
+      const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&u[kk][0]);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         acc[2 * e] = fmaf(w, __low2float(a[e]), acc[2 * e]);
@@ -789,21 +797,8 @@ __global__ void __launch_bounds__(1024) job_prep_kernel(DevCfg c, DevBatch b, Wo
   pdl_trigger();
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult r;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &r) ==
-            cudaSuccess &&
-        r == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t stride, uint32_t box_rows) {
-  auto fn = encode_fn();
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)kTcD, rows};
   cuuint64_t strides[1] = {stride * 2};
@@ -857,13 +852,15 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
       b.cmp_rows > 0x7fffffffLL || b.hca_rows > 0x7fffffffLL || (int64_t)T * kTcH > 0x7fffffffLL)
     return -2;
   CUtensorMap qmap;
-  if (!make_map(&qmap, b.q, (uint64_t)T * kTcH, kTcD, kTcH)) return -1;
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(attn_tile_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kA5Dyn);
-    cudaFuncSetAttribute(attn_tile_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kA5Dyn);
-    attr = true;
-  }
+  if (!make_map(&qmap, b.q, (uint64_t)T * kTcH, kTcD, kTcH))
+    return launch_fail("cuTensorMapEncodeTiled(q)", cudaSuccess);
+  static PerDeviceOnce attr;
+  if (const cudaError_t e = attr.run([] {
+        cudaError_t r = allow_max_dynamic_smem(attn_tile_kernel<false>);
+        if (r == cudaSuccess) r = allow_max_dynamic_smem(attn_tile_kernel<true>);
+        return r;
+      }))
+    return launch_fail("cudaFuncSetAttribute(attn_tile_kernel)", e);
   const bool paged = b.raw_table || b.cmp_table || b.hca_table;
   int n = 0;
   if (jobs.host_B < 0) {

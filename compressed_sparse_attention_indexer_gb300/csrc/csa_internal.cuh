@@ -6,6 +6,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "csa.h"
 
 namespace csa {
@@ -29,6 +32,10 @@ struct DevCfg {
   int idx_fp8;  // indexer keys are FP8 E4M3 rows with a per-row fp32 scale
   float scale, rope_base;
   int max_context, max_vis;
+  // polls after which the attention tile kernel's consumer waits give up
+  // (negative: the default, about a second); set through the test hook
+  // csa_debug_set_wait_polls
+  int wait_polls;
   double rope_theta[kRopeTable];  // base^(-2i/R), i < min(R/2, kRopeTable), set on the host
 };
 
@@ -157,7 +164,8 @@ struct Workspace {
   int* topk_idx;      // [max_T, K]
   int* topk_cnt;      // [max_T]
   int* job_prefix;    // [max_T + 1] attention tiles per query, prefix (device-built)
-  __half* part_o;     // [max_T * max_jobs, H, V] per-segment normalised attention output
+  __nv_bfloat16* part_o;  // [max_T * max_jobs, H, V] per-segment normalised attention output
+                          // (bf16: the range of fp32, so any row magnitude survives)
   float* part_lse;    // [max_T * max_jobs, H] per-segment log-sum-exp (log2 units)
   int max_T, max_batch;
   int64_t scores_ld;
@@ -172,6 +180,11 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
+
+// Records why a launch helper gives up (the entry point's error message then
+// names the failing call and its CUDA error); returns -1.  The record is per
+// host thread and is consumed by the entry point that made the call.
+int launch_fail(const char* what, cudaError_t e);
 
 // Launch with or without the programmatic-stream-serialisation attribute.
 // Returns 1 on a successful launch, -1 otherwise.
@@ -188,8 +201,66 @@ int launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cu
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = pdl ? at : nullptr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...) == cudaSuccess ? 1 : -1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+  return e == cudaSuccess ? 1 : launch_fail("cudaLaunchKernelEx", e);
 }
+
+// Host-side set-up that belongs to one device, done once per device and
+// process, safely from several host threads: a kernel's shared-memory opt-in
+// (cudaFuncSetAttribute) is a property of the function on the device that is
+// current when it is set, so a process that drives several GPUs needs it on
+// each of them.  run(set) calls set() the first time the current device
+// comes through and returns true once set() has succeeded there; false if
+// set() failed (it is retried by the next call) or the current device cannot
+// be determined or has an ordinal of kMaxDevices or more (as a CUDA error
+// code, see run()).
+constexpr int kMaxDevices = 64;
+class PerDeviceOnce {
+ public:
+  // set() returns cudaSuccess or the error of the call that failed; run()
+  // returns it (cudaErrorInvalidDevice for an ordinal >= kMaxDevices)
+  template <typename F>
+  cudaError_t run(F&& set) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = set();
+    if (e != cudaSuccess) return e;
+    done_[dev].store(true, std::memory_order_release);
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<bool> done_[kMaxDevices]{};
+};
+
+// Raises kern's dynamic shared-memory limit on the current device to the most
+// the device allows it: the per-block opt-in maximum minus the kernel's own
+// static shared memory (queried, not assumed, so that it holds whatever the
+// compiler adds).  A launch then fails only if it asks for more than that.
+template <typename Kern>
+cudaError_t allow_max_dynamic_smem(Kern* kern) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  int dev = 0, optin = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              optin - (int)fa.sharedSizeBytes);
+}
+
+// The driver's cuTensorMapEncodeTiled, looked up once per process (a
+// function-local static: its initialisation is thread-safe); NULL if the
+// driver does not provide it.
+void* tensor_map_encoder();
 
 // ---- launch wrappers (defined in the kernel files) -------------------------
 // Each returns the number of kernels launched (>= 0) or -1 on a launch error.

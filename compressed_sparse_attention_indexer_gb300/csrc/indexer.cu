@@ -257,11 +257,10 @@ __global__ void __launch_bounds__(256) indexer_simt_kernel(DevCfg c, DevBatch b,
 // CSA_INDEXER=mma in the environment selects the warp-MMA kernel (kept as the
 // measured baseline of the tcgen05 one).
 int indexer_impl() {
-  static int impl = -1;
-  if (impl < 0) {
+  static const int impl = [] {
     const char* e = getenv("CSA_INDEXER");
-    impl = (e && strcmp(e, "mma") == 0) ? kIndexerMma : kIndexerTc5;
-  }
+    return (e && strcmp(e, "mma") == 0) ? kIndexerMma : kIndexerTc5;
+  }();
   return impl;
 }
 
@@ -307,14 +306,13 @@ int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, cons
     const int fixed = SG * kQBytes + kStashBytes + SG * kTcHi * 4;
     int NST = (227 * 1024 - fixed) / kKStageBytes;
     NST = NST > 4 ? 4 : NST;
-    if (NST < 2) return -1;
+    if (NST < 2) return launch_fail("warp-MMA indexer: no room for two key stages", cudaSuccess);
     const int smem = fixed + NST * kKStageBytes;
-    static bool attr_done = false;
-    if (!attr_done) {
-      cudaFuncSetAttribute(indexer_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           227 * 1024);
-      attr_done = true;
-    }
+    static PerDeviceOnce attr;
+    if (const cudaError_t e = attr.run([] {
+          return allow_max_dynamic_smem(indexer_mma_kernel);
+        }))
+      return launch_fail("cudaFuncSetAttribute(indexer_mma_kernel)", e);
     int grid = num_sms;
     if (known > 0 && known < grid) grid = known;
     return launch_kernel(indexer_mma_kernel, dim3(grid), dim3(kIdxThreads), smem, st, pdl, items,

@@ -51,6 +51,7 @@ constexpr int kMaxG = 4;                        // queries per MMA group
 struct T5Smem {
   uint64_t full[8], empty[8], qfull[2], qempty[2], tfull[8], tempty[8], done;
   uint64_t cfull[kConvBufs], cempty[kConvBufs];  // FP8 keys: converted items
+  uint64_t ebar;                                 // the epilogue warps' bounded barrier
   uint32_t tmem_base;
   int abort;
 };
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       tc5::mbar_init(smem_u32(&sm.tempty[i]), 128);
     }
     tc5::mbar_init(smem_u32(&sm.done), 1);
+    tc5::mbar_init(smem_u32(&sm.ebar), 128);
     sm.abort = 0;
     tc5::fence_mbar_init();
   }
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     cur.init(prefix, b.B, lo);
     int L = 0;
     int64_t off = 0;
+    uint32_t ephase = 0;
     for (int it = lo; it < hi && !*abort; ++it) {
       bool new_unit = cur.advance(it) || it == lo;
       if (new_unit) {
@@ -381,10 +384,12 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       }
       if (new_unit) {
         // the unit's w (su x 64) into shared memory, shared by its items
-        named_barrier_sync(1, 128);
+        // (bounded barriers: a warp that gave up a wait must not strand the
+        // others)
+        if (!tc5::bar_bounded(smem_u32(&sm.ebar), ephase, abort)) break;
         const float* wsrc = b.w + ((int64_t)cur.bi * S + u.g0) * kTcHi;
         for (int v = row; v < u.su * kTcHi; v += 128) w_sm[v] = __ldg(wsrc + v);
-        named_barrier_sync(1, 128);
+        if (!tc5::bar_bounded(smem_u32(&sm.ebar), ephase, abort)) break;
       }
       const int bi = cur.bi;
       const int c0 = u.chunk * kIdxChunk;
@@ -458,24 +463,11 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
   if (warp == 5) tc5::tmem_dealloc(tmem, tmem_cols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // 2D tensor [rows, cols] with a row stride in elements; boxes of
 // [box_rows, 128 bytes] (one 128-byte swizzle row): 64 bf16 or 128 FP8.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint64_t stride,
               uint32_t box_rows, bool fp8 = false) {
-  auto fn = encode_fn();
+  auto fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
   if (!fn) return false;
   const uint64_t es = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {cols, rows};
@@ -498,15 +490,16 @@ struct T5Plan {
   int ctas_per_sm, acc_cols, NB, NCB, NST, NQB, stage_bytes, conv_bytes, qbytes;
 };
 static bool plan_t5(const DevCfg& c, int S, T5Plan* p) {
-  static int max_stages = -1, forced_ctas = 0;
-  if (max_stages < 0) {
+  static const int max_stages = [] {
     const char* e = getenv("CSA_T5_STAGES");
-    max_stages = e ? atoi(e) : 8;
-    if (max_stages < 2 || max_stages > 8) max_stages = 8;
+    const int v = e ? atoi(e) : 8;
+    return (v < 2 || v > 8) ? 8 : v;
+  }();
+  static const int forced_ctas = [] {
     const char* f = getenv("CSA_T5_CTAS");
-    forced_ctas = f ? atoi(f) : 0;
-    if (forced_ctas < 0 || forced_ctas > 4) forced_ctas = 0;
-  }
+    const int v = f ? atoi(f) : 0;
+    return (v < 0 || v > 4) ? 0 : v;
+  }();
   // CTAs per SM: two independent pipelines per SM stream measurably faster
   // than one deeper ring (the ring depth beyond three stages does not
   // matter), so two whenever a request's q_idx leaves room for two stages
@@ -559,21 +552,22 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   const int SU = qsplit ? qsplit : S;  // queries per work unit
   T5Plan p;
   if (!plan_t5(c, SU, &p)) return -2;
-  if (fp8 && !b.idx_scale) return -1;
+  if (fp8 && !b.idx_scale) return launch_fail("FP8 keys without idx_scale", cudaSuccess);
   CUtensorMap kmap, qmap;
   if (!make_map(&kmap, b.idx, (uint64_t)b.idx_rows, kTcDi, (uint64_t)b.idx_stride, kIdxChunk, fp8))
-    return -1;
-  if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi)) return -1;
+    return launch_fail("cuTensorMapEncodeTiled(idx_k)", cudaSuccess);
+  if (!make_map(&qmap, b.q_idx, (uint64_t)b.B * S * kTcHi, kTcDi, kTcDi, kTcHi))
+    return launch_fail("cuTensorMapEncodeTiled(q_idx)", cudaSuccess);
   const int smem = 1024 + p.NST * p.stage_bytes + p.conv_bytes + p.NQB * p.qbytes + SU * kTcHi * 4;
-  static bool attr = false;
-  if (!attr) {
-    const int max_dyn = 227 * 1024 - (int)sizeof(T5Smem);
-    cudaFuncSetAttribute(indexer_tc5_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
-    cudaFuncSetAttribute(indexer_tc5_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
-    cudaFuncSetAttribute(indexer_tc5_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
-    cudaFuncSetAttribute(indexer_tc5_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn);
-    attr = true;
-  }
+  static PerDeviceOnce attr;
+  if (const cudaError_t e = attr.run([] {
+        cudaError_t r = allow_max_dynamic_smem(indexer_tc5_kernel<false, false>);
+        if (r == cudaSuccess) r = allow_max_dynamic_smem(indexer_tc5_kernel<false, true>);
+        if (r == cudaSuccess) r = allow_max_dynamic_smem(indexer_tc5_kernel<true, false>);
+        if (r == cudaSuccess) r = allow_max_dynamic_smem(indexer_tc5_kernel<true, true>);
+        return r;
+      }))
+    return launch_fail("cudaFuncSetAttribute(indexer_tc5_kernel)", e);
   int grid = num_sms * p.ctas_per_sm;
   if (known > 0 && known < grid) grid = known;
   const dim3 block(fp8 ? kT5ThreadsFp8 : kT5Threads);

@@ -36,6 +36,19 @@ __global__ void __launch_bounds__(1024) prep_kernel(DevCfg c, DevBatch b, Worksp
   pdl_trigger();
 }
 
+void* tensor_map_encoder() {
+  static void* const fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult r;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &r) !=
+            cudaSuccess ||
+        r != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return p;
+  }();
+  return fn;
+}
+
 int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all, int qsplit,
                 cudaStream_t st, bool pdl) {
   return launch_kernel(prep_kernel, dim3(1), dim3(1024), 0, st, pdl, c, b, ws, score_all, qsplit);

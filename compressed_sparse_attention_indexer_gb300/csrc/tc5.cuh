@@ -53,12 +53,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 // As mbar_wait, but after a few tight polls the thread sleeps between polls
 // (32 ns doubling up to max_ns), so that waiting warps leave the issue slots
-// and the shared-memory pipe to the warps that work.  Gives up after about a
-// second in total.
+// and the shared-memory pipe to the warps that work.  Gives up after `limit`
+// polls (by default about a second in total; 0 gives up at once).
+constexpr uint32_t kBackoffPolls = 1u << 23;
 __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity, volatile int* abort,
-                                                  uint32_t max_ns) {
+                                                  uint32_t max_ns, uint32_t limit = kBackoffPolls) {
   uint32_t ns = 32;
-  for (uint32_t i = 0; i < (1u << 23); ++i) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i >= 8) {
       __nanosleep(ns);
@@ -68,6 +69,22 @@ __device__ __forceinline__ bool mbar_wait_backoff(uint32_t bar, uint32_t parity,
   }
   *abort = 1;
   return false;
+}
+
+// A barrier over the threads an mbarrier was initialised for (its arrival
+// count) that, unlike bar.sync, cannot block forever: each thread arrives,
+// then waits with mbar_wait_backoff, so it gives up (false, abort set) when
+// the wait runs out or another role has set *abort.  A thread of the group
+// that has left its loop after a failed wait therefore cannot strand the
+// others at the barrier.  `phase` counts the calling thread's uses (each
+// thread keeps its own); a thread arrives for use k + 1 only after it saw
+// use k complete, and use k + 1 cannot complete before every thread has
+// arrived for it, so no thread is ever two phases behind.
+__device__ __forceinline__ bool bar_bounded(uint32_t bar, uint32_t& phase, volatile int* abort) {
+  mbar_arrive(bar);
+  const bool ok = mbar_wait_backoff(bar, phase & 1u, abort, 32);
+  ++phase;
+  return ok;
 }
 
 // Orders this thread's generic-proxy shared-memory writes before later

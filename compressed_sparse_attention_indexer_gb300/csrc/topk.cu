@@ -28,6 +28,10 @@ namespace {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kBins = 2048;
+// dynamic shared memory of topk_kernel at the longest row a config may have
+// (max_context / ratio <= 40960 keys, one pad word per 16)
+constexpr int kMaxRowKeys = 40960;
+constexpr int kTopkSmemMax = (kMaxRowKeys + kMaxRowKeys / 16 + 1) * 4;
 
 __device__ __forceinline__ uint32_t score_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -470,11 +474,10 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
 // The register kernel when every row fits it (CSA_TOPK=radix keeps the
 // shared-memory kernel, its measured baseline).
 bool topk_use_reg(int max_vis) {
-  static int forced = -1;
-  if (forced < 0) {
+  static const bool forced = [] {
     const char* e = getenv("CSA_TOPK");
-    forced = (e && e[0] == 'r') ? 1 : 0;
-  }
+    return e && e[0] == 'r';
+  }();
   return !forced && max_vis <= kRegMax;
 }
 
@@ -490,10 +493,15 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
                          dim3(nq), dim3(kTopkThreads), 0, st, pdl, c, b ? *b : none, scores, ld,
                          n_override, idx_out, cnt_out, status, max_vis, (pdl && early) ? 1 : 0);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
-  static int attr_smem = 0;
-  if (smem > 48 * 1024 && smem > attr_smem) {
-    cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_smem = smem;
+  if (smem > kTopkSmemMax)  // rows are bounded at create time
+    return launch_fail("Top-K: rows longer than the kernel holds", cudaSuccess);
+  // the opt-in for the longest rows a config may have, once per device
+  static PerDeviceOnce attr;
+  if (smem > 48 * 1024) {
+    if (const cudaError_t e = attr.run([] {
+          return allow_max_dynamic_smem(topk_kernel);
+        }))
+      return launch_fail("cudaFuncSetAttribute(topk_kernel)", e);
   }
   return launch_kernel(topk_kernel, dim3(nq), dim3(kTopkThreads), smem, st, pdl, c, b ? *b : none,
                        scores, ld, n_override, idx_out, cnt_out, status, max_vis);

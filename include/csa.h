@@ -56,6 +56,15 @@
  *  - A handle may be used from one host thread at a time.  Calls that share
  *    a handle must be ordered on the GPU (same stream, or the caller orders
  *    them): they share the handle's workspace.
+ *  - Several devices in one process: a handle belongs to the device that was
+ *    current at csa_decode_create and must be used with that device current.
+ *    Handles of different devices may be used from different host threads
+ *    at the same time; the library's per-device set-up (kernel shared-memory
+ *    opt-ins) is done once per device, under a lock.
+ *  - Value range: the kernels accumulate in fp32, so products and sums of
+ *    the inputs (q . row over D dims, softmax-weighted sums of rows, indexer
+ *    dot products) must stay within the fp32 range; any bf16 magnitude is
+ *    otherwise accepted (intermediate attention partials are bf16).
  */
 #ifndef CSA_H
 #define CSA_H
@@ -173,7 +182,12 @@ CSA_API int csa_indexer_topk(csa_handle *h, const csa_batch *b, int32_t *topk_id
  * writes them; every index must lie in [0, vis) and count <= min(vis, K),
  * else CSA_ERR_BAD_INDEX is recorded and the bad entries are skipped).
  * out [B,S,H,V] in the config dtype; lse_out [B,S,H] fp32 natural-log
- * log-sum-exp of the merged streams, may be NULL. */
+ * log-sum-exp of the merged streams, may be NULL.  Accuracy of lse_out on the
+ * bf16 tensor-core path: the softmax weights are rounded to bf16 (the tensor
+ * cores' operand type) before they are summed, so ln(sum) may differ from the
+ * exact value by up to u/(1-u) ~ 1.96e-3 with u = 2^-9; this bound comes from
+ * that operand choice, not from the method, and is the tolerance the parity
+ * tests apply to lse_out (the fp32 path: 1e-5). */
 CSA_API int csa_sparse_attn(csa_handle *h, const csa_batch *b, const int32_t *topk_idx,
                     const int32_t *topk_cnt, void *out, float *lse_out, void *stream);
 
@@ -209,17 +223,21 @@ CSA_API int csa_topk_select(csa_handle *h, int32_t nq, const float *scores, int6
  * message giving the size (csa_indexer_topk has no such limit).  cfg's
  * max_batch / max_queries_per_req bound B and S as for a handle.
  *
- * The first call on each device looks up the array's address (and the SM
- * count) and keeps them; make that first call, for example with B = 0,
- * outside stream capture.  Each call clears the status word on `stream`
- * before its kernels run.  The array is shared by every call in the process
- * on that device: calls whose execution overlaps (other streams or host
- * threads) race on it and must be ordered by the caller.
+ * The first call in each CUDA context (normally one per device, its primary
+ * context) looks up the array's address and the SM count and keeps them,
+ * keyed by the context's unique id: a context created later on the same
+ * device (after cudaDeviceReset, which unloads the module, or a driver-API
+ * context made current) gets a lookup of its own.  Make that first call, for
+ * example with B = 0, outside stream capture.  Each call clears the status
+ * word on `stream` before its kernels run.  The array is shared by every
+ * call in the process on that device: calls whose execution overlaps (other
+ * streams or host threads) race on it and must be ordered by the caller.
  *
  * topk_idx / topk_cnt as csa_indexer_topk.  status_out: NULL or a device
- * int32 that receives the status word after the kernels: 0, or bit 1 (a
- * length or row index out of range, what csa_get_status reports as
- * CSA_ERR_BAD_INDEX) and bit 2 (a device wait gave up, CSA_ERR_TIMEOUT).
+ * int32 that receives the status word after the kernels (with B = 0, a 0
+ * written on `stream`): 0, or an OR of the value 1 (bit 0: a length or row
+ * index out of range, what csa_get_status reports as CSA_ERR_BAD_INDEX) and
+ * the value 2 (bit 1: a device wait gave up, CSA_ERR_TIMEOUT).
  * Launches on `stream`; does not synchronise. */
 CSA_API int csa_indexer_topk_static(const csa_config *cfg, const csa_batch *b, int32_t *topk_idx,
                             int32_t *topk_cnt, int32_t *status_out, void *stream);
@@ -260,6 +278,18 @@ CSA_API int csa_get_status(csa_handle *h, void *stream);
  * records per launch; leave it off for end-to-end timing. */
 CSA_API int csa_profile_enable(csa_handle *h, int32_t enable);
 CSA_API int csa_profile_read(csa_handle *h, float *ms, int32_t *launches);
+
+/* Test hook for the device-side timeout path.  Every wait of this library's
+ * kernels on another thread's progress (an mbarrier phase) is bounded: after
+ * about a second it gives up, the block winds down (copies and tensor-core
+ * operations already started are waited for, tensor memory is freed) and the
+ * status word records CSA_ERR_TIMEOUT, so a stalled pipeline returns an error
+ * instead of hanging the GPU.  With polls >= 0, the consumer waits of the
+ * attention tile kernel launched by later calls on this handle give up after
+ * `polls` polls (0: at their first wait, whatever the data), which drives that
+ * path on purpose; the outputs of such a call are then undefined.  polls < 0
+ * restores the default.  Returns CSA_ERR_INVALID_ARG for a NULL handle. */
+CSA_API int csa_debug_set_wait_polls(csa_handle *h, int32_t polls);
 
 /* Message for the last error on this host thread ("" if none). */
 CSA_API const char *csa_last_error(void);

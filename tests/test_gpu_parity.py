@@ -332,6 +332,52 @@ def test_generic_shapes_simt_path():
 
 
 # ---------------------------------------------------------------------------
+# value range: KV rows of any bf16 magnitude.  Multiplying every KV row by 2^e
+# and q by 2^-e leaves every score q . row unchanged, so the exact output is
+# 2^e times the unscaled output.  Every rounding the step makes (fp32
+# accumulation, the bf16 segment partials, the bf16 output) commutes with a
+# power-of-two scale while values stay inside their type's normal range, so
+# the scaled GPU output must be the unscaled GPU output times 2^e bit for bit,
+# and within the usual tolerance of the oracle run on the scaled inputs.
+# 2^17 puts outputs near 1e5 (past fp16's 65504) and 2^-20 near 1e-7 (below
+# fp16's normal range).
+
+def _scaled_rows(hb, e):
+    out = dict(hb)
+    f = 2.0 ** e
+    out["q"] = (hb["q"].float() * (1.0 / f)).to(hb["q"].dtype)
+    for k in ("raw_kv", "cmp_kv", "hca_kv"):
+        if hb.get(k) is not None:
+            out[k] = (hb[k].float() * f).to(hb[k].dtype)
+    return out
+
+
+@pytest.mark.parametrize("name,lens,e", [("topk_b16_l8192", [8192, 5000, 700, 129], 17),
+                                         ("topk_b16_l8192", [8192, 5000, 700, 129], -20),
+                                         ("multitoken_hca_b16_s8", [32768, 4100], 17),
+                                         ("long_ragged_b64", [65536, 1024, 30001], 17)])
+def test_value_range_scaled_rows(name, lens, e):
+    wl = WORKLOADS[name]
+    hb = make_batch(wl, lens=lens)
+    hs = _scaled_rows(hb, e)
+    # the scaled inputs are exact: q * 2^-e * 2^e and row * 2^e * 2^-e round-trip
+    assert torch.equal((hs["q"].float() * 2.0 ** e).to(hb["q"].dtype), hb["q"])
+    assert torch.equal((hs["cmp_kv"].float() * 2.0 ** -e).to(hb["cmp_kv"].dtype), hb["cmp_kv"])
+    mc = max(lens)
+    g = run_step(wl, hb, max_context=mc, host_lens=True)
+    gs = run_step(wl, hs, max_context=mc, host_lens=True)
+    assert gs["status"] == csa.CSA_OK, csa.last_error()
+    assert np.isfinite(gs["out"]).all()
+    np.testing.assert_array_equal(gs["out"], g["out"] * 2.0 ** e)
+    np.testing.assert_array_equal(gs["lse"], g["lse"])
+    np.testing.assert_array_equal(gs["idx"], g["idx"])
+    ref = oracle.decode(wl.cfg, hs)
+    assert_topk_sets(gs["idx"], gs["cnt"], ref, scores_fn(wl.cfg, hs), wl.cfg.topk, name)
+    assert_close(gs["out"] * 2.0 ** -e, ref["out"] * 2.0 ** -e, TOL_BF16, f"{name} 2^{e} out")
+    assert_close(gs["lse"], ref["lse"], (2.5e-3, 5e-4), f"{name} 2^{e} lse")
+
+
+# ---------------------------------------------------------------------------
 # determinism, empty batch, device-side error reporting
 
 def test_bitwise_deterministic():

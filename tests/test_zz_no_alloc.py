@@ -109,3 +109,12 @@ def test_static_entry_with_an_empty_batch_only_sets_up():
                                            None, None)
     assert rc == csa.CSA_OK
     torch.cuda.synchronize()
+    # with a status word to fill, an empty batch reports a clean status
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream()
+    rc = csa.lib().csa_indexer_topk_static(ctypes.byref(cc), ctypes.byref(b), 0x10000, 0x10000,
+                                           ctypes.c_void_p(status.data_ptr()),
+                                           ctypes.c_void_p(stream.cuda_stream))
+    assert rc == csa.CSA_OK
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
