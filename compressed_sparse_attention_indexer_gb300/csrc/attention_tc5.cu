@@ -41,6 +41,7 @@
 #include <cudaTypedefs.h>
 #include <stddef.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "csa_internal.cuh"
 #include "tc5.cuh"
@@ -49,12 +50,13 @@ namespace csa {
 
 namespace {
 
-constexpr int kLoadWarps = 3;    // per loader group
-constexpr int kA5Threads = 32 * (5 + 2 * kLoadWarps);  // warps 0-3 softmax, 4 MMA + Q, 5-10 loaders
+constexpr int kLoadWarps = 3;              // per row-loader group
+constexpr int kA5Threads = 32 * (5 + 2 * kLoadWarps);  // warps 0-3 softmax, 4 MMA + Q, 5-10 row loaders
 constexpr int kTile = 64;                  // rows per job
 constexpr int kQuadsPerWarp = (kTile / 4 + kLoadWarps - 1) / kLoadWarps;
+constexpr int kNSub = 9;                   // 64-dim sub-tiles of a 576-wide row
 constexpr int kSub = kTile * 128;          // 64 rows x 64 dims bf16: 8 KB
-constexpr int kBuf = 9 * kSub;             // a job's rows: 72 KB (rope sub-tile -> P^T)
+constexpr int kBuf = kNSub * kSub;         // a job's rows: 72 KB (rope sub-tile -> P^T)
 constexpr int kQSub = kTcH * 128;          // 64 heads x 64 dims: 8 KB
 constexpr int kQBytes = 9 * kQSub;         // the query's heads, resident: 72 KB
 constexpr int kA5Dyn = 1024 + kQBytes + 2 * kBuf;
@@ -67,18 +69,21 @@ constexpr int kMergeMaxJobs = 64;          // jobs per query the merge handles (
 constexpr uint32_t kTmemS = 0, kTmemO = 256;
 
 struct __align__(16) A5Smem {
-  uint64_t full[2], empty[2], mfull[2], mempty[2], s_full[2], s_empty[2];
+  // per job buffer: its rows have landed / the MMAs that read them are done
+  uint64_t full[2], empty[2];
+  uint64_t mfull[2], mempty[2], s_full[2], s_empty[2];
   // p_full per job buffer: with one barrier the softmax could complete two
   // jobs' phases before the MMA thread polls the first, and a parity wait
   // cannot tell phase n from phase n + 2; per buffer, job n + 2's phase needs
   // job n's PV first
   uint64_t p_full[2];
   uint64_t pv_done, o_full, o_empty, qfull, qdone, done;
-  uint64_t sbar;                   // the softmax warps' bounded barrier
   uint32_t tmem_base;
   int abort;
-  int flag[2][4];                  // per job parity and warp: some head needs a rescale
-  uint64_t mask[2][kLoadWarps];    // per buffer and loader warp: bit i = row i exists
+  // per job parity and softmax warp: bit 0 some head needs a rescale, bit 1
+  // the warp saw a wait give up (every softmax thread then leaves together)
+  int flag[2][4];
+  uint64_t mask[2][kLoadWarps];    // per buffer and loader warp: bit i = row i of the job exists
   alignas(16) float alpha[2][kTcH];  // per job parity: per-head rescale factor
   alignas(16) float linv[2][kTcH];   // per segment parity: per-head 1 / (sum of the weights)
 };
@@ -216,8 +221,7 @@ __device__ __forceinline__ int job_row(const DevBatch& b, const JobCtx& x, int s
 // row lookups are one add)
 template <bool kPaged>
 __global__ void __launch_bounds__(kA5Threads, 1)
-    attn_tile_kernel(const __grid_constant__ CUtensorMap qmap,
-                     const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
+    attn_tile_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
                      const int* __restrict__ topk_idx, const int* __restrict__ topk_cnt,
                      int early) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -231,10 +235,11 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   const int T = b.B * b.S;
   // Launched right after this library's Top-K kernel of the same step
   // (early != 0), every input but the Top-K outputs was complete before the
-  // step's first kernel passed its own wait, so only the threads that read
-  // topk_idx / topk_cnt wait for the previous grid, and setup, Q and window
-  // rows overlap its tail.  Otherwise (a caller's kernel before this one, or
-  // a job list built on the device) every thread waits first.
+  // step's first kernel passed its own wait, so only the row loaders wait
+  // for the previous grid, when they first read topk_idx / topk_cnt, and
+  // setup, Q and window rows overlap its tail.  Otherwise (a caller's kernel
+  // before this one, or a job list built on the device) every thread waits
+  // first.
   const bool wait_all = !(early && jobs.host_B >= 0);
   if (wait_all) pdl_wait();
   const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
@@ -253,21 +258,20 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   }
   if (tid == 0) {
     for (int g = 0; g < 2; ++g) {
-      tc5::mbar_init(smem_u32(&sm.full[g]), 32 * kLoadWarps);  // every thread of the group
-      tc5::mbar_init(smem_u32(&sm.empty[g]), 1);
+      tc5::mbar_init(smem_u32(&sm.full[g]), kLoadWarps);  // one arrival per loader warp
+      tc5::mbar_init(smem_u32(&sm.empty[g]), 1);          // an MMA commit
       tc5::mbar_init(smem_u32(&sm.mfull[g]), kLoadWarps);  // one arrival per loader warp
       tc5::mbar_init(smem_u32(&sm.mempty[g]), 128);  // the softmax threads
       tc5::mbar_init(smem_u32(&sm.s_full[g]), 1);
       tc5::mbar_init(smem_u32(&sm.s_empty[g]), 128);
+      tc5::mbar_init(smem_u32(&sm.p_full[g]), 128);
     }
-    for (int g = 0; g < 2; ++g) tc5::mbar_init(smem_u32(&sm.p_full[g]), 128);
     tc5::mbar_init(smem_u32(&sm.pv_done), 1);
     tc5::mbar_init(smem_u32(&sm.o_full), 1);
     tc5::mbar_init(smem_u32(&sm.o_empty), 128);
     tc5::mbar_init(smem_u32(&sm.qfull), 1);
     tc5::mbar_init(smem_u32(&sm.qdone), 1);
     tc5::mbar_init(smem_u32(&sm.done), 1);
-    tc5::mbar_init(smem_u32(&sm.sbar), 128);
     sm.abort = 0;
     tc5::fence_mbar_init();
   }
@@ -278,8 +282,14 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 
   if (warp >= 5) {
     // ------------------------------------------------------------ row loaders
-    // group g takes jobs lo+g, lo+g+2, ...; an instruction moves four rows x
-    // 128 bytes, and warp lw of the group takes row quads lw, lw+3, ...
+    // Group g (three warps) takes jobs lo+g, lo+g+2, ... into job buffer g.
+    // Lane l of a warp moves 16-byte chunk l & 7 of row quads lw, lw+3, ...
+    // (rows 4 quad + l / 8), with cp.async into the 128-byte swizzled
+    // sub-tiles; a row that does not exist (or is out of range) reads zeros.
+    // Once the buffer's previous job has released it, the whole job is in
+    // flight at once; each thread then waits for its copies and fences them
+    // for the async proxy, and one lane per warp arrives on the buffer's
+    // barrier.
     const int g = (warp - 5) / kLoadWarps, lw = (warp - 5) % kLoadWarps;
     const uint32_t buf = bufs + g * kBuf;
     const __nv_bfloat16* null_src = static_cast<const __nv_bfloat16*>(b.q);
@@ -288,7 +298,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     cur.init(prefix, T, lo);
     int m = 0;
     bool waited = wait_all;
-    for (int job = lo + g; job < hi && !*abort; job += 2, ++m) {
+    for (int job = lo + g; job < hi; job += 2, ++m) {
+      if (__shfl_sync(0xffffffffu, *abort, 0)) break;
       cur.advance(job);
       const int q = cur.q;
       JobCtx x = job_ctx(c, b, q);
@@ -300,8 +311,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       const int* tbl = kPaged ? (sid == 0 ? b.raw_table : (sid == 1 ? b.cmp_table : b.hca_table)) : nullptr;
       const int64_t off = tbl ? -1 : (sid == 0 ? b.raw_off[x.bi] : (sid == 1 ? b.cmp_off[x.bi] : b.hca_off[x.bi]));
       // this lane's rows: their Top-K indices are loaded together with the
-      // count they are checked against (read before waiting for the buffer,
-      // so that the loads overlap the wait)
+      // count they are checked against
       int jr[kQuadsPerWarp];
 #pragma unroll
       for (int i = 0; i < kQuadsPerWarp; ++i) jr[i] = -1;
@@ -335,24 +345,27 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       }
       bool ok = true;
       if (lane == 0) {
-        if (m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.empty[g]), (m - 1) & 1, abort, 256, wpolls)) ok = false;
-        if (ok && m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.mempty[g]), (m - 1) & 1, abort, 256, wpolls)) ok = false;
+        if (m >= 1 && !tc5::mbar_wait_backoff(smem_u32(&sm.mempty[g]), (m - 1) & 1, abort, 256, wpolls))
+          ok = false;
         if (ok) {
           sm.mask[g][lw] = bits;
           tc5::mbar_arrive(smem_u32(&sm.mfull[g]));
         }
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (lane == 0 && m >= 1 &&
+          !tc5::mbar_wait_backoff(smem_u32(&sm.empty[g]), (m - 1) & 1, abort, 256, wpolls))
+        ok = false;
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
 #pragma unroll 3
-      for (int sub = 0; sub < 9; ++sub) {
+      for (int k = 0; k < kNSub; ++k) {
 #pragma unroll
         for (int i = 0; i < kQuadsPerWarp; ++i) {
           const int rq = lw + kLoadWarps * i;
           if (rq < kTile / 4) {
             const int rt = 4 * rq + (lane >> 3);  // row within the job
-            const uint32_t dst = buf + sub * kSub + rt * 128 + ((ch ^ (rt & 7)) << 4);
-            cp_async16(dst, src[i] ? (const void*)(src[i] + sub * 64 + ch * 8) : (const void*)null_src,
+            const uint32_t dst = buf + k * kSub + rt * 128 + ((ch ^ (rt & 7)) << 4);
+            cp_async16(dst, src[i] ? (const void*)(src[i] + k * 64 + ch * 8) : (const void*)null_src,
                        src[i] ? 16 : 0);
           }
         }
@@ -360,7 +373,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async();
-      tc5::mbar_arrive(smem_u32(&sm.full[g]));
+      __syncwarp();
+      if (lane == 0) tc5::mbar_arrive(smem_u32(&sm.full[g]));
     }
     cp_async_wait<0>();
   } else if (warp == 4) {
@@ -390,11 +404,12 @@ __global__ void __launch_bounds__(kA5Threads, 1)
           pc.advance(job);
           const bool first = job == lo || job == pc.first;
           const bool last = job + 1 == hi || job + 1 == pc.end;
+          const int g = np & 1;
           if ((!first || seg == 0 || tc5::mbar_try_wait(smem_u32(&sm.o_empty), (seg - 1) & 1)) &&
-              tc5::mbar_try_wait(smem_u32(&sm.p_full[np & 1]), (np >> 1) & 1)) {
+              tc5::mbar_try_wait(smem_u32(&sm.p_full[g]), (np >> 1) & 1)) {
             // O^T += V^T . P^T (overwrite at a segment's first job)
             tc5::fence_after_sync();
-            const uint32_t vo = ((np & 1) * kBuf) >> 4;           // buffer offset, 16-byte units
+            const uint32_t vo = (g * kBuf) >> 4;                  // buffer offset, 16-byte units
             const uint64_t dp = dbuf + vo + ((8 * kSub) >> 4);    // P^T in the rope sub-tile
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
@@ -402,7 +417,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
               for (int i = 0; i < 4; ++i)
                 tc5::mma_bf16(tmem + kTmemO + 64 * cc, dv + vo + ((2 * cc * kSub + i * 2048) >> 4),
                               dp + 2 * i, idesc_o, (!first || i > 0) ? 1u : 0u);
-            tc5::mma_commit(smem_u32(&sm.empty[np & 1]));
+            tc5::mma_commit(smem_u32(&sm.empty[g]));
             tc5::mma_commit(smem_u32(&sm.pv_done));
             if (last) {
               tc5::mma_commit(smem_u32(&sm.o_full));
@@ -443,7 +458,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
             const uint64_t db = dbuf + ((g * kBuf) >> 4);
             const uint32_t ds = tmem + kTmemS + 64 * g;
 #pragma unroll
-            for (int k = 0; k < 9; ++k)
+            for (int k = 0; k < kNSub; ++k)
 #pragma unroll
               for (int i = 0; i < 4; ++i)
                 tc5::mma_bf16(ds, dq + ((k * kQSub + 32 * i) >> 4), db + ((k * kSub + 32 * i) >> 4),
@@ -471,10 +486,14 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    // lanes 0-15 of warp w own head h = 16w + lane (its TMEM lane in the
-    // score buffers): the job's 64 scores, the reference max and the sum of
-    // the weights stay in the thread
-    const bool owner = lane < 16;
+    // Two threads per head: lanes i and i + 16 of warp w own head h = 16w + i
+    // (its TMEM lane in the M = 64 score layout), rows 0-31 and 32-63 of the
+    // job respectively; the reference max and the sum of the weights are
+    // shared by the pair (one shuffle each) and kept identically in both.
+    // The four warps meet once per job at a named barrier; a thread whose
+    // wait gave up skips its work but still reaches the barrier, and the
+    // flags read after it make every softmax thread leave at the same job.
+    const int hf = lane >> 4;  // which half of the job's rows
     const int h = 16 * warp + (lane & 15);
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const float sc2 = c.scale * kLog2e;
@@ -482,31 +501,50 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     JobCursor cur;
     cur.init(prefix, T, lo);
     int n = 0, seg = 0, slot = lo;
-    uint32_t sphase = 0;
-    for (int job = lo; job < hi && !*abort; ++job, ++n) {
+    bool bad = false;  // a wait of this thread gave up
+    for (int job = lo; job < hi; ++job, ++n) {
       cur.advance(job);
       const bool first = job == lo || job == cur.first;
       const bool last = job + 1 == hi || job + 1 == cur.end;
       if (first) slot = job;
       const int g = n & 1, m = n >> 1;
-      if (!tc5::mbar_wait_backoff(smem_u32(&sm.mfull[g]), m & 1, abort, 64, wpolls)) break;
       uint64_t mk = 0;
+      if (!bad && !tc5::mbar_wait_backoff(smem_u32(&sm.mfull[g]), m & 1, abort, 64, wpolls)) bad = true;
+      if (!bad) {
 #pragma unroll
-      for (int w = 0; w < kLoadWarps; ++w) mk |= sm.mask[g][w];
-      tc5::mbar_arrive(smem_u32(&sm.mempty[g]));
-      if (!tc5::mbar_wait_backoff(smem_u32(&sm.s_full[g]), m & 1, abort, 64, wpolls)) break;
-      tc5::fence_after_sync();
-      float s[64];
-      tc5::tmem_ld32x2(tmem + kTmemS + 64 * g + lanes, s, s + 32);
-      tc5::fence_before_sync();
-      tc5::mbar_arrive(smem_u32(&sm.s_empty[g]));
-      // tile max of the scaled scores over the rows that exist (log2 units)
-      float mt = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        s[j] = ((mk >> j) & 1u) ? s[j] * sc2 : -INFINITY;
-        mt = fmaxf(mt, s[j]);
+        for (int w = 0; w < kLoadWarps; ++w) mk |= sm.mask[g][w];
       }
+      tc5::mbar_arrive(smem_u32(&sm.mempty[g]));
+      if (!bad && !tc5::mbar_wait_backoff(smem_u32(&sm.s_full[g]), m & 1, abort, 64, wpolls)) bad = true;
+      float s[32];
+      if (!bad) {
+        tc5::fence_after_sync();
+        tc5::tmem_ld16x32bx2_32(tmem + kTmemS + 64 * g + lanes, s);
+        tc5::fence_before_sync();
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) s[j] = 0.f;
+      }
+      tc5::mbar_arrive(smem_u32(&sm.s_empty[g]));
+      // tile max of the scaled scores over the rows that exist (log2 units),
+      // as four independent running maxima, then across the pair
+      const uint32_t mh = (uint32_t)(mk >> (32 * hf));
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (mh == 0xffffffffu) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          s[j] *= sc2;
+          m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          s[j] = ((mh >> j) & 1u) ? s[j] * sc2 : -INFINITY;
+          m4[j & 3] = fmaxf(m4[j & 3], s[j]);
+        }
+      }
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
       // lazy rescale: keep the reference unless the tile max exceeds it by 2^8
       float alpha = 1.f;
       bool resc = false;
@@ -518,61 +556,70 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         mref = mt;
         resc = true;
       }
-      // P = 2^(s - m_ref) as bf16: the head's 128-byte row of P^T (K-major B
-      // operand, 128-byte swizzle) in the job's rope sub-tile, which QK is
-      // done with; the weights are summed as rounded, like the MMA sees them
-      float psum = 0.f;
-      if (owner) {
+      // P = 2^(s - m_ref) as bf16: this thread's half (64 bytes) of the
+      // head's 128-byte row of P^T (K-major B operand, 128-byte swizzle) in
+      // the job's rope sub-tile, which QK is done with; the weights are
+      // summed as rounded, like the MMA sees them
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      if (!bad) {
         uint8_t* prow = gen + g * kBuf + 8 * kSub + h * 128;
         const float mo = mref == -INFINITY ? 0.f : mref;  // no row yet: every score is -inf
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int cl = 0; cl < 4; ++cl) {
           uint32_t w4[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int j = 8 * c8 + 2 * e;
+            const int j = 8 * cl + 2 * e;
             const float p0 = ex2_approx(s[j] - mo);  // 0 for a masked row (-inf)
             const float p1 = ex2_approx(s[j + 1] - mo);
             const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            psum += __low2float(b2);
-            psum += __high2float(b2);
+            ps[e] += __low2float(b2) + __high2float(b2);
             w4[e] = *reinterpret_cast<const uint32_t*>(&b2);
           }
+          const int c8 = 4 * hf + cl;  // 16-byte chunk: rows 8 c8 .. 8 c8 + 7
           *reinterpret_cast<uint4*>(prow + ((c8 ^ (h & 7)) << 4)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         fence_proxy_async();
-        lrun = lrun * alpha + psum;
+      }
+      float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      psum += __shfl_xor_sync(0xffffffffu, psum, 16);  // the same sum in both threads of the pair
+      lrun = lrun * alpha + psum;
+      if (hf == 0) {
         sm.alpha[g][h] = alpha;
         if (last) sm.linv[seg & 1][h] = lrun > 0.f ? 1.f / lrun : 0.f;
       }
-      const bool any = __any_sync(0xffffffffu, owner && resc);
-      if (lane == 0) sm.flag[g][warp] = any ? 1 : 0;
-      // (a bounded barrier: a warp that gave up a wait must not strand the others)
-      if (!tc5::bar_bounded(smem_u32(&sm.sbar), sphase, abort)) break;
-      if (sm.flag[g][0] | sm.flag[g][1] | sm.flag[g][2] | sm.flag[g][3]) {
+      const bool any = __any_sync(0xffffffffu, resc);
+      const bool anybad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) sm.flag[g][warp] = (any ? 1 : 0) | ((anybad || *abort) ? 2 : 0);
+      named_barrier_sync(1, 128);
+      const int fl = sm.flag[g][0] | sm.flag[g][1] | sm.flag[g][2] | sm.flag[g][3];
+      if (fl & 2) break;  // the same decision in every softmax thread
+      if (fl & 1) {
         // O^T of the segment so far, times 2^(m_old - m_new) per head (column),
         // once the previous job's PV is complete; thread = TMEM lane = dim
-        if (!tc5::mbar_wait_backoff(smem_u32(&sm.pv_done), (n - 1) & 1, abort, 64, wpolls)) break;
-        tc5::fence_after_sync();
+        if (!bad && !tc5::mbar_wait_backoff(smem_u32(&sm.pv_done), (n - 1) & 1, abort, 64, wpolls)) bad = true;
+        if (!bad) {
+          tc5::fence_after_sync();
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
+          for (int cc = 0; cc < 4; ++cc) {
 #pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            float o[32];
-            const uint32_t col = kTmemO + 64 * cc + 32 * half;
-            tc5::tmem_ld32(tmem + col + lanes, o);
+            for (int half = 0; half < 2; ++half) {
+              float o[32];
+              const uint32_t col = kTmemO + 64 * cc + 32 * half;
+              tc5::tmem_ld32(tmem + col + lanes, o);
 #pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-              const float4 a4 = reinterpret_cast<const float4*>(sm.alpha[g])[8 * half + i4];
-              o[4 * i4 + 0] *= a4.x;
-              o[4 * i4 + 1] *= a4.y;
-              o[4 * i4 + 2] *= a4.z;
-              o[4 * i4 + 3] *= a4.w;
+              for (int i4 = 0; i4 < 8; ++i4) {
+                const float4 a4 = reinterpret_cast<const float4*>(sm.alpha[g])[8 * half + i4];
+                o[4 * i4 + 0] *= a4.x;
+                o[4 * i4 + 1] *= a4.y;
+                o[4 * i4 + 2] *= a4.z;
+                o[4 * i4 + 3] *= a4.w;
+              }
+              tc5::tmem_st32(tmem + col + lanes, o);
             }
-            tc5::tmem_st32(tmem + col + lanes, o);
           }
+          tc5::tmem_wait_st();
         }
-        tc5::tmem_wait_st();
       }
       tc5::fence_before_sync();
       tc5::mbar_arrive(smem_u32(&sm.p_full[g]));
@@ -581,43 +628,45 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         // segment epilogue: thread (warp, lane) owns dim 128cc + 32warp + lane
         // of each chunk; writes the normalised output and each head's
         // log-sum-exp (log2 units)
-        if (owner) {
+        if (hf == 0) {
           ws.part_lse[(int64_t)slot * kTcH + h] = lrun > 0.f ? mref + log2f(lrun) : -INFINITY;
         }
-        if (!tc5::mbar_wait_backoff(smem_u32(&sm.o_full), seg & 1, abort, 64, wpolls)) break;
-        tc5::fence_after_sync();
-        // heads x dims, bf16 (the range of fp32: a partial is a convex
-        // combination of value rows, which may be any bf16 magnitude; fp16
-        // would overflow past 65504): lanes 2i and 2i+1 swap values so that each
-        // holds dims 2i, 2i+1 of one head of a pair (j, j+1); a warp store
-        // covers 32 consecutive dims of two heads (two 64-byte runs)
-        __nv_bfloat16* po = ws.part_o + (int64_t)slot * kTcH * kTcV;
-        const bool odd = lane & 1;
+        if (!bad && !tc5::mbar_wait_backoff(smem_u32(&sm.o_full), seg & 1, abort, 64, wpolls)) bad = true;
+        if (!bad) {
+          tc5::fence_after_sync();
+          // heads x dims, bf16 (the range of fp32: a partial is a convex
+          // combination of value rows, which may be any bf16 magnitude; fp16
+          // would overflow past 65504): lanes 2i and 2i+1 swap values so that
+          // each holds dims 2i, 2i+1 of one head of a pair (j, j+1); a warp
+          // store covers 32 consecutive dims of two heads (two 64-byte runs)
+          __nv_bfloat16* po = ws.part_o + (int64_t)slot * kTcH * kTcV;
+          const bool odd = lane & 1;
 #pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float inv[32];
+          for (int half = 0; half < 2; ++half) {
+            float inv[32];
 #pragma unroll
-          for (int i4 = 0; i4 < 8; ++i4) {
-            const float4 l4 = reinterpret_cast<const float4*>(sm.linv[seg & 1])[8 * half + i4];
-            inv[4 * i4 + 0] = l4.x;
-            inv[4 * i4 + 1] = l4.y;
-            inv[4 * i4 + 2] = l4.z;
-            inv[4 * i4 + 3] = l4.w;
-          }
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const float4 l4 = reinterpret_cast<const float4*>(sm.linv[seg & 1])[8 * half + i4];
+              inv[4 * i4 + 0] = l4.x;
+              inv[4 * i4 + 1] = l4.y;
+              inv[4 * i4 + 2] = l4.z;
+              inv[4 * i4 + 3] = l4.w;
+            }
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            float o[32];
-            tc5::tmem_ld32(tmem + kTmemO + 64 * cc + 32 * half + lanes, o);
-            const int d0 = cc * 128 + warp * 32 + (lane & ~1);  // the pair's first dim
-            __nv_bfloat16* row = po + (int64_t)(32 * half + (odd ? 1 : 0)) * kTcV + d0;
+            for (int cc = 0; cc < 4; ++cc) {
+              float o[32];
+              tc5::tmem_ld32(tmem + kTmemO + 64 * cc + 32 * half + lanes, o);
+              const int d0 = cc * 128 + warp * 32 + (lane & ~1);  // the pair's first dim
+              __nv_bfloat16* row = po + (int64_t)(32 * half + (odd ? 1 : 0)) * kTcV + d0;
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              // even lane keeps head j, odd lane head j+1; each sends the other
-              const float mine = odd ? o[j + 1] * inv[j + 1] : o[j] * inv[j];
-              const float give = odd ? o[j] * inv[j] : o[j + 1] * inv[j + 1];
-              const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-              *reinterpret_cast<__nv_bfloat162*>(row + (int64_t)j * kTcV) =
-                  odd ? __floats2bfloat162_rn(got, mine) : __floats2bfloat162_rn(mine, got);
+              for (int j = 0; j < 32; j += 2) {
+                // even lane keeps head j, odd lane head j+1; each sends the other
+                const float mine = odd ? o[j + 1] * inv[j + 1] : o[j] * inv[j];
+                const float give = odd ? o[j] * inv[j] : o[j + 1] * inv[j + 1];
+                const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                *reinterpret_cast<__nv_bfloat162*>(row + (int64_t)j * kTcV) =
+                    odd ? __floats2bfloat162_rn(got, mine) : __floats2bfloat162_rn(mine, got);
+              }
             }
           }
         }

@@ -237,6 +237,28 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, float* v0, float* v1
   }
 }
 
+// The .16x32bx2 shape, 32 repetitions, half-split offset 32 columns: threads
+// 0-15 of the warp get TMEM lanes base .. base+15 (base = the warp's lane
+// quarter), columns col .. col+31; threads 16-31 get the same 16 lanes,
+// columns col+32 .. col+63.  Reads an M = 64 accumulator (rows in lanes 0-15
+// of each quarter) with all 32 threads of the warp, half the columns each.
+__device__ __forceinline__ void tmem_ld16x32bx2_32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32], 32;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  tmem_wait_ld(r);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // 32 lanes x 32 consecutive fp32 columns from registers (the store mirror of
 // tmem_ld32); tmem_wait_st orders the stores before later tcgen05 work.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
