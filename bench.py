@@ -3,7 +3,9 @@
 One step = the whole hot path (plan, indexer score, Top-K, gather + split
 softmax attention + LSE merge + inverse RoPE) over one batch of the long
 ragged workload (B=64, S=1, L_b ~ U{1024..65536}, H=64, D=576, K=512,
-WIN=128, bf16) through the C ABI.  Prints one JSON line.
+WIN=128, bf16) through the C ABI.  Prints one JSON line; its "workloads"
+object carries the same measurements (throughput, roofline, oracle on all
+host cores and on one) for every other named workload.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle on the host cores
@@ -43,6 +45,10 @@ def parse():
     ap.add_argument("--copies", type=int, default=3, help="device copies of the inputs, rotated per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--workloads", default="all",
+                    help="other named workloads measured after the headline one: all, none, or a comma list")
+    ap.add_argument("--other-steps", type=int, default=300, help="timed steps of each other workload")
+    ap.add_argument("--cpu-seconds", type=float, default=6.0, help="wall time of each oracle baseline")
     return ap.parse_args()
 
 
@@ -186,24 +192,29 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def cpu_baseline(wl, hb, budget_s=6.0, nq=16):
-    """The oracle as it stands, on the host cores, over a bounded sample of queries."""
+def cpu_baseline(wl, hb, budget_s=6.0, threads=None):
+    """The oracle as it stands, on the host cores, over a bounded sample of
+    queries: the first max(16, threads) queries of the batch (one oracle
+    thread per query, so every thread has a query), repeated for about
+    budget_s seconds.  threads=None uses every host core."""
     import numpy as np
     import oracle
     oracle.build()
-    cores = os.cpu_count() or 1
+    cores = threads or os.cpu_count() or 1
     T = hb["B"] * hb["S"]
-    qids = np.arange(min(nq, T), dtype=np.int32)
+    nq = min(T, max(16, cores))
+    used = min(cores, nq)
+    qids = np.arange(nq, dtype=np.int32)
     done, t0 = 0, time.perf_counter()
     while True:
-        oracle.decode(wl.cfg, hb, qids=qids, nthreads=cores)
+        oracle.decode(wl.cfg, hb, qids=qids, nthreads=used)
         done += qids.size
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return {"value": done / el, "unit": "queries/s", "cores": min(cores, qids.size), "kind": "oracle",
-            "sample": f"{qids.size} queries of {wl.name} (first {qids.size} requests, their full "
-                      f"context), repeated {done // qids.size}x, fp64 C oracle, {el:.1f} s wall"}
+    return {"value": done / el, "unit": "queries/s", "cores": used, "kind": "oracle",
+            "sample": f"{nq} queries of {wl.name} (the first {nq} of the batch, their full context), "
+                      f"repeated {done // nq}x, fp64 C oracle, {used} thread(s), {el:.1f} s wall"}
 
 
 def run_reference(args):
@@ -347,31 +358,23 @@ def run_e2e(args, csa, dec, hb, copies, lens_host, out, idx, cnt, stream, dev, T
                     "the neighbouring steps' kernels; KV/indexer caches stay resident"}
 
 
-def run_ours(args):
-    import numpy as np
+def measure(args, name, steps, warmup, dev, ws, rank, dist, with_e2e, with_cpu):
+    """One workload: K timed steps through csa_decode_step (inputs resident in
+    HBM, rotated over device copies), per-stage times, roofline of the
+    dominant stage, optionally the end-to-end leg and the oracle baseline."""
     import torch
 
-    from compressed_sparse_attention_indexer_gb300 import build as csa_build
     from compressed_sparse_attention_indexer_gb300 import csa
     from compressed_sparse_attention_indexer_gb300.workloads import WORKLOADS, make_batch, to_device
 
-    ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-    csa_build.build()
-    wl = WORKLOADS[args.workload]
+    wl = WORKLOADS[name]
     cfg = wl.cfg
     # weak scaling: every rank decodes its own batch (different seed per rank)
     hb = make_batch(wl, seed=rank_seed(wl.seed, rank))
     B, S = hb["B"], hb["S"]
     T = B * S
     lens = [int(x) for x in hb["ctx_len"]]
-    max_ctx = 65536 if args.workload == "long_ragged_b64" else max(lens)
+    max_ctx = 65536 if name.startswith("long_ragged") else max(lens)
     copies = [to_device(hb, dev)]
     for _ in range(args.copies - 1):
         copies.append({k: (v.clone() if isinstance(v, torch.Tensor) else v) for k, v in copies[0].items()})
@@ -386,12 +389,12 @@ def run_ours(args):
     def step(i):
         dec.decode_step(structs[i % len(structs)], out, None, idx, cnt, stream)
 
-    for i in range(max(args.warmup, 3)):
+    for i in range(max(warmup, 3)):
         step(i)
     torch.cuda.synchronize()
     st = dec.status()
     if st != csa.CSA_OK:
-        raise RuntimeError(f"device status {st}: {csa.last_error()}")
+        raise RuntimeError(f"{name}: device status {st}: {csa.last_error()}")
     launches_per_step = dec.last_launch_count()
     sel = idx.cpu().numpy().reshape(T, cfg.topk)
     bytes_ = step_bytes(cfg, lens, S, sel)
@@ -403,70 +406,118 @@ def run_ours(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
         ev0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
-    ms = reduce_max(ev0.elapsed_time(ev1) / args.steps, dist if ws > 1 else None, dev)
+    ms = reduce_max(ev0.elapsed_time(ev1) / steps, dist if ws > 1 else None, dev)
     st = dec.status()
     if st != csa.CSA_OK:
-        raise RuntimeError(f"device status {st} after the timed steps: {csa.last_error()}")
+        raise RuntimeError(f"{name}: device status {st} after the timed steps: {csa.last_error()}")
     if ws > 1:
         dist.barrier()
 
     # ---- per-kernel times (events around each launch, same stream), separate pass
     dec.profile(True)
-    for i in range(args.steps):
+    for i in range(steps):
         step(i)
     torch.cuda.synchronize()
     prof = dec.profile_read()
     dec.profile(False)
     per_kernel_ms = {k: (v[0] / v[1] if v[1] else 0.0) for k, v in prof.items()}
     dom = max(("indexer", "attention", "topk"), key=lambda k: prof[k][0])
-    peak, peak_kind, peaks = measured_peaks()
+    peak, peak_kind, _ = measured_peaks()
     alg = bytes_[dom] if dom in bytes_ else None
-    if alg is not None:
-        achieved = alg / (per_kernel_ms[dom] * 1e-3) / 1e9
-    else:
-        achieved = None
+    achieved = alg / (per_kernel_ms[dom] * 1e-3) / 1e9 if (alg and per_kernel_ms[dom] > 0) else None
     roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
             "frac": (achieved / peak) if achieved else None, "peak_source": peak_kind,
             "algorithmic_bytes_per_launch": alg,
-            "traffic": load_traffic(dom, args.workload),
+            "traffic": load_traffic(dom, name),
             "per_kernel_us": {k: round(v * 1e3, 3) for k, v in per_kernel_ms.items()},
             "time_share": {k: round(v[0] / max(sum(x[0] for x in prof.values()), 1e-9), 4)
                            for k, v in prof.items()},
-            "step_achieved_gbs": bytes_["total"] / (ms * 1e-3) / 1e9}
+            "step_achieved_gbs": bytes_["total"] / (ms * 1e-3) / 1e9,
+            "step_frac": bytes_["total"] / (ms * 1e-3) / 1e9 / peak}
 
     # ---- end to end through the public API with host buffers
     e2e = None
-    if not args.no_e2e:
+    if with_e2e:
         e2e = run_e2e(args, csa, dec, hb, copies, lens_host, out, idx, cnt, stream, dev, T, ws,
                       dist if ws > 1 else None)
-
-    if rank != 0:
-        if ws > 1:
-            dist.destroy_process_group()
-        return
-    cpu = None
-    if ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, hb)
+    cpu = cpu1 = None
+    if with_cpu:
+        cpu = cpu_baseline(wl, hb, budget_s=args.cpu_seconds)
+        cpu1 = cpu_baseline(wl, hb, budget_s=max(2.0, args.cpu_seconds / 3), threads=1)
     foot = sum(v.numel() * v.element_size() for v in copies[0].values() if isinstance(v, torch.Tensor))
-    line = {
-        "metric": "csa_decode_queries_per_s", "value": job_throughput(T, ws, ms), "unit": "queries/s",
-        "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
-        "data": "synthetic (seeded normal / uniform draws, shapes of the workload)",
+    res = {
+        "value": job_throughput(T, ws, ms), "unit": "queries/s", "ms_per_step": ms, "steps": steps,
+        "dtype": cfg.dtype,
         "config": {"workload": wl.name, "B": B, "S": S, "H": cfg.H, "D": cfg.D, "K": cfg.topk,
                    "WIN": cfg.win, "L_range": list(wl.L_range) if wl.L_range else wl.L,
                    "sum_L": int(sum(lens)), "parallelism": f"replicas{ws}",
                    "l2": f"inputs rotate over {len(copies)} device copies ({foot / 1e9:.2f} GB each); "
-                         f"each step reads ~{bytes_['total'] / 1e6:.0f} MB > L2 {L2_BYTES / 1e6:.0f} MB",
+                         f"each step reads ~{bytes_['total'] / 1e6:.1f} MB (L2 {L2_BYTES / 1e6:.0f} MB)",
                    "algorithmic_bytes_per_step": bytes_["total"]},
         "achieved_hbm_gbs": bytes_["total"] / (ms * 1e-3) / 1e9,
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-        "clocks": clk.summary(), "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof, "cpu_baseline": cpu, "cpu_baseline_1core": cpu1, "e2e": e2e,
+        "clocks": clk.summary(), "gpu_launches": launches_per_step * steps,
         "launches_per_step": launches_per_step,
+    }
+    dec.close()
+    del copies, structs
+    torch.cuda.empty_cache()
+    return res
+
+
+# the other named workloads, measured after the headline one (their shapes are
+# the pages' decode shapes, the Top-K-active and multi-token variants, the
+# prefill chunk and the FP8-key cache)
+OTHER_WORKLOADS = ("tiny_f32", "bypass_b16_l256", "topk_b16_l8192", "multitoken_hca_b16_s8",
+                   "prefill_b2_t512", "long_ragged_b64_fp8idx")
+
+
+def run_ours(args):
+    import torch
+
+    from compressed_sparse_attention_indexer_gb300 import build as csa_build
+
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    csa_build.build()
+    head = measure(args, args.workload, args.steps, args.warmup, dev, ws, rank, dist,
+                   with_e2e=not args.no_e2e, with_cpu=(ws == 1 and rank == 0 and not args.no_cpu_baseline))
+    others = {}
+    names = [] if args.workloads == "none" else (
+        [n for n in OTHER_WORKLOADS if n != args.workload] if args.workloads == "all" else args.workloads.split(","))
+    for n in names:
+        r = measure(args, n, min(args.steps, args.other_steps), args.warmup, dev, ws, rank, dist,
+                    with_e2e=False, with_cpu=(ws == 1 and rank == 0 and not args.no_cpu_baseline))
+        others[n] = {k: r[k] for k in ("value", "unit", "ms_per_step", "steps", "dtype", "achieved_hbm_gbs",
+                                       "roofline", "cpu_baseline", "cpu_baseline_1core", "launches_per_step")}
+        others[n]["config"] = r["config"]
+    if rank != 0:
+        if ws > 1:
+            dist.destroy_process_group()
+        return
+    line = {
+        "metric": "csa_decode_queries_per_s", "value": head["value"], "unit": "queries/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": head["dtype"],
+        "data": "synthetic (seeded normal / uniform draws, shapes of the workload)",
+        "config": head["config"],
+        "achieved_hbm_gbs": head["achieved_hbm_gbs"],
+        "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"],
+        "cpu_baseline_1core": head["cpu_baseline_1core"], "e2e": head["e2e"],
+        "clocks": head["clocks"], "gpu_launches": head["gpu_launches"],
+        "launches_per_step": head["launches_per_step"],
+        "workloads": others,
     }
     print(json.dumps(line), flush=True)
     if ws > 1:

@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     const uint32_t buf = bufs + g * kBuf;
     const __nv_bfloat16* null_src = static_cast<const __nv_bfloat16*>(b.q);
     const int ch = lane & 7;
+    const uint64_t rpol = tc5::policy_evict_first();  // rows are read once per step
     JobCursor cur;
     cur.init(prefix, T, lo);
     int m = 0;
@@ -365,8 +366,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
           if (rq < kTile / 4) {
             const int rt = 4 * rq + (lane >> 3);  // row within the job
             const uint32_t dst = buf + k * kSub + rt * 128 + ((ch ^ (rt & 7)) << 4);
-            cp_async16(dst, src[i] ? (const void*)(src[i] + k * 64 + ch * 8) : (const void*)null_src,
-                       src[i] ? 16 : 0);
+            cp_async16_hint(dst, src[i] ? (const void*)(src[i] + k * 64 + ch * 8) : (const void*)null_src,
+                            src[i] ? 16 : 0, rpol);
           }
         }
       }
@@ -692,8 +693,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 // 16 consecutive dims (t & 3) of the block's 64: it loads its head's LSE and
 // a 32-byte piece of the partials, four segments per batch, derives the
 // weights itself (running max across batches), and stores 32 bytes.
-constexpr int kMergeUnroll = 4;  // partials whose loads are in flight together
-__global__ void __launch_bounds__(256, 4)
+constexpr int kMergeUnroll = 2;  // partials whose loads are in flight together
+__global__ void __launch_bounds__(256, 3)
     attn_merge_kernel(const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
                       int G, __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   __shared__ int seg[kMergeMaxJobs + 1];

@@ -229,6 +229,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
   if (warp == 4) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      const uint64_t kpol = tc5::policy_evict_first();
       int kc = 0, qc = 0;
       ReqCursor cur;
       cur.init(prefix, b.B, lo);
@@ -263,11 +264,13 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
         if (y0 < 0) y0 = b.idx_rows;
         const int y = (int)y0;
         tc5::mbar_expect_tx(smem_u32(&sm.full[st]), stage_bytes);
+        // keys are read once per step: evict them first from L2
         if (kFp8) {  // one box: 128 rows x 128 FP8 keys
-          tc5::tma_load_2d(kbuf + st * stage_bytes, &kmap, 0, y, smem_u32(&sm.full[st]));
+          tc5::tma_load_2d_hint(kbuf + st * stage_bytes, &kmap, 0, y, smem_u32(&sm.full[st]), kpol);
         } else {
-          tc5::tma_load_2d(kbuf + st * kStageBytes, &kmap, 0, y, smem_u32(&sm.full[st]));
-          tc5::tma_load_2d(kbuf + st * kStageBytes + kSubBytes, &kmap, 64, y, smem_u32(&sm.full[st]));
+          tc5::tma_load_2d_hint(kbuf + st * kStageBytes, &kmap, 0, y, smem_u32(&sm.full[st]), kpol);
+          tc5::tma_load_2d_hint(kbuf + st * kStageBytes + kSubBytes, &kmap, 64, y, smem_u32(&sm.full[st]),
+                                kpol);
         }
         ++kc;
       }

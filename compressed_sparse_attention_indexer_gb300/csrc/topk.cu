@@ -220,6 +220,17 @@ constexpr int kRegMax = kRegKeys * kTopkThreads;
 constexpr int kShortKeys = 2;  // keys per thread of the short-row one
 constexpr int kCand = kTopkThreads;  // candidates ranked directly
 
+// A global load issued exactly where it is written (asm volatile): the value
+// then lives in a register (or is spilled) for the rest of the kernel.  A
+// read-only load (ld.global.nc) may instead be issued again at each later use
+// when registers are scarce, turning every pass over a thread's keys into a
+// round trip to L2.
+__device__ __forceinline__ float ld_once(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
   asm("mov.u32 %0, %%lanemask_lt;\n" : "=r"(m));
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       const int i = j * kTopkThreads + tid;
-      v[j] = i < n ? __ldg(sc + i) : 0.f;
+      v[j] = i < n ? ld_once(sc + i) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
