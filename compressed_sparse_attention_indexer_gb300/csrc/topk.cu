@@ -196,12 +196,14 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 }
 
 // Register-resident variant for rows of at most kJ * 1024 keys (the common
-// case: max_context / ratio <= 16384).  Thread t holds keys t + 1024 j,
-// j < kJ, in registers for the whole selection: kJ = 16, or kJ = 2 for rows
-// of at most 2048 keys (short contexts, prefill chunks), whose smaller
-// register footprint fits two blocks per SM.  The result is defined by a
-// threshold pair (tkey, tidx): the K-th entry in the order (key descending,
-// index ascending); a key is selected iff it precedes or is that entry.
+// case: max_context / ratio <= 16384).  Thread t holds the kJ consecutive
+// keys kJ t .. kJ t + kJ - 1 in registers for the whole selection (kJ = 16,
+// or kJ = 2 for rows of at most 2048 keys: short contexts, prefill chunks,
+// whose smaller register footprint fits two blocks per SM), so the block's
+// threads and each thread's keys are both in index order.  The result is
+// defined by a threshold pair (tkey, tidx): the K-th entry in the order (key
+// descending, index ascending); a key is selected iff it precedes or is that
+// entry.
 //   1. radix passes as above (histogram of the next digit among keys that
 //      match the prefix), until the digit's keys are exactly the ones needed
 //      (threshold = the digit's lowest key, any index) or few enough to rank
@@ -210,31 +212,38 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 //      and each candidate's rank among them is counted by one thread; rank
 //      need - 1 is the threshold;
 //   3. keys all equal and more than 1024 of them straddle the threshold: the
-//      threshold index is the need-th of them in index order, from per-row
-//      ballots and one block scan;
-//   4. output: per (row j, warp) ballots of the selection, one block scan over
-//      the kJ * 32 counts in index order, and each selected key writes its
-//      index at its position, so the output is in ascending index order.
+//      threshold index is the need-th of them in index order (a block scan of
+//      the per-thread counts);
+//   4. output: a block scan of the per-thread counts of selected keys gives
+//      each thread its first output position; it writes its selected indices
+//      there in order, so the output is in ascending index order.
 constexpr int kRegKeys = 16;  // keys per thread of the long-row instantiation
 constexpr int kRegMax = kRegKeys * kTopkThreads;
 constexpr int kShortKeys = 2;  // keys per thread of the short-row one
 constexpr int kCand = kTopkThreads;  // candidates ranked directly
 
 // A global load issued exactly where it is written (asm volatile): the value
-// then lives in a register (or is spilled) for the rest of the kernel.  A
-// read-only load (ld.global.nc) may instead be issued again at each later use
-// when registers are scarce, turning every pass over a thread's keys into a
-// round trip to L2.
+// then lives in a register (or is spilled) for the rest of the kernel,
+// instead of a read-only load that the compiler may issue again at a later
+// use when registers are scarce.
 __device__ __forceinline__ float ld_once(const float* p) {
   float v;
   asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
-
-__device__ __forceinline__ uint32_t lanemask_lt() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;\n" : "=r"(m));
-  return m;
+// The same for two and four consecutive floats.
+__device__ __forceinline__ float4 ld_once4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_once2(const float* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "l"(p) : "memory");
+  return v;
 }
 
 template <int kJ>
@@ -243,12 +252,10 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
                     const int* __restrict__ n_override, int* __restrict__ idx_out,
                     int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
                     int early) {
-  constexpr int kRows = kJ * 32;  // (row j, warp) pairs, in index order
+  static_assert(kJ == 2 || kJ % 4 == 0, "keys are loaded as float2 or float4 vectors");
   __shared__ int hist[kBins];
   __shared__ uint32_t cand_key[kCand];
   __shared__ int cand_idx[kCand];
-  __shared__ uint32_t rowbits[kRows];
-  __shared__ int rowbase[kRows];
   __shared__ int scan_tmp[33];
   __shared__ uint32_t warp_or[32], warp_and[32];
   __shared__ uint32_t s_tkey;
@@ -295,21 +302,37 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   }
   const float* sc = scores + (int64_t)q * ld;
   if (tid == 0) s_ncand = 0;
-  // keys in registers (all sixteen loads in flight), and the OR / AND over
+  // this thread's keys (all loads in flight at once), and the OR / AND over
   // the row: bits where they differ are the ones still to decide
+  const int i0 = tid * kJ;
   uint32_t k[kJ];
   uint32_t vmask = 0u, aor = 0u, aand = ~0u;
   {
     float v[kJ];
+    const bool vec = ((reinterpret_cast<uintptr_t>(sc) & (kJ == 2 ? 7u : 15u)) == 0) && i0 + kJ <= n;
+    if (vec) {
+      if (kJ == 2) {
+        const float2 x = ld_once2(sc + i0);
+        v[0] = x.x;
+        v[1] = x.y;
+      } else {
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const int i = j * kTopkThreads + tid;
-      v[j] = i < n ? ld_once(sc + i) : 0.f;
+        for (int j = 0; j < kJ; j += 4) {
+          const float4 x = ld_once4(sc + i0 + j);
+          v[j] = x.x;
+          v[j + 1] = x.y;
+          v[j + 2] = x.z;
+          v[j + 3] = x.w;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) v[j] = i0 + j < n ? ld_once(sc + i0 + j) : 0.f;
     }
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       k[j] = score_key_fast(v[j]);
-      if (j * kTopkThreads + tid < n) {
+      if (i0 + j < n) {
         vmask |= 1u << j;
         aor |= k[j];
         aand &= k[j];
@@ -396,21 +419,23 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   if (mode == 0 && in_bin <= kCand) mode = 2;
 
   if (mode == 2) {
-    // compact the keys that match the prefix, then rank each among them
+    // compact the keys that match the prefix (this thread's, contiguous
+    // slots), then rank each among them
+    uint32_t m = 0u;
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const bool m = ((vmask >> j) & 1u) && (k[j] >> start) == prefix;  // start < 32 here
-      const uint32_t bal = __ballot_sync(0xffffffffu, m);
-      if (bal) {
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&s_ncand, __popc(bal));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        const int slot = base + __popc(bal & lanemask_lt());
-        if (m && slot < kCand) {
-          cand_key[slot] = k[j];
-          cand_idx[slot] = j * kTopkThreads + tid;
+    for (int j = 0; j < kJ; ++j)
+      if (((vmask >> j) & 1u) && (k[j] >> start) == prefix) m |= 1u << j;  // start < 32 here
+    if (m) {
+      int slot = atomicAdd(&s_ncand, __popc(m));
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if ((m >> j) & 1u) {
+          if (slot < kCand) {
+            cand_key[slot] = k[j];
+            cand_idx[slot] = i0 + j;
+          }
+          ++slot;
         }
-      }
     }
     __syncthreads();
     if (tid < in_bin) {
@@ -431,52 +456,41 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     tidx = s_tidx;
   } else if (mode == 0) {
     // start == 0: more than kCand keys equal `prefix` and `need` of them are
-    // kept, the lowest indices first
+    // kept, the lowest indices first: the thread holding the need-th of them
+    // in index order finds it among its keys
+    int eq = 0;
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, ((vmask >> j) & 1u) && k[j] == prefix);
-      if (lane == 0) rowbits[j * 32 + warp] = bal;
-    }
-    __syncthreads();
-    const int cv = tid < kRows ? __popc(rowbits[tid]) : 0;
+    for (int j = 0; j < kJ; ++j) eq += (((vmask >> j) & 1u) && k[j] == prefix) ? 1 : 0;
     int tot;
-    const int ex = block_exclusive_scan(cv, scan_tmp, &tot);
-    if (tid < kRows && ex < need && ex + cv >= need) {
-      uint32_t bits = rowbits[tid];
-      for (int r = ex + 1; r < need; ++r) bits &= bits - 1u;  // drop the lower set bits
-      s_tidx = (tid >> 5) * kTopkThreads + (tid & 31) * 32 + (__ffs(bits) - 1);
+    const int ex = block_exclusive_scan(eq, scan_tmp, &tot);
+    if (ex < need && ex + eq >= need) {
+      int r = ex;
+#pragma unroll
+      for (int j = 0; j < kJ; ++j)
+        if (((vmask >> j) & 1u) && k[j] == prefix && ++r == need) s_tidx = i0 + j;
     }
     __syncthreads();
     tkey = prefix;
     tidx = s_tidx;
   }
 
-  // selection: keys before the threshold in (key desc, index asc) order
+  // selection: keys before the threshold in (key desc, index asc) order;
+  // a block scan of the per-thread counts gives each thread its output slot
   uint32_t smask = 0u;
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
-    const int i = j * kTopkThreads + tid;
+    const int i = i0 + j;
     const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
     smask |= (uint32_t)sel << j;
-    const uint32_t bal = __ballot_sync(0xffffffffu, sel);
-    if (lane == 0) rowbits[j * 32 + warp] = bal;
   }
-  __syncthreads();
-  {
-    const int cv = tid < kRows ? __popc(rowbits[tid]) : 0;
-    int tot;
-    const int ex = block_exclusive_scan(cv, scan_tmp, &tot);
-    if (tid < kRows) rowbase[tid] = ex;
-  }
-  __syncthreads();
-  const uint32_t lt = lanemask_lt();
-  while (smask) {  // this thread's selected keys (few: K of n)
-    const int j = __ffs(smask) - 1;
-    smask &= smask - 1u;
-    const int e = j * 32 + warp;
-    const int pos = rowbase[e] + __popc(rowbits[e] & lt);
-    if (pos < K) out[pos] = j * kTopkThreads + tid;
-  }
+  int tot;
+  int pos = block_exclusive_scan(__popc(smask), scan_tmp, &tot);
+#pragma unroll
+  for (int j = 0; j < kJ; ++j)
+    if ((smask >> j) & 1u) {
+      if (pos < K) out[pos] = i0 + j;
+      ++pos;
+    }
   if (tid == 0) cnt_out[q] = K;
 }
 
