@@ -30,8 +30,9 @@ struct csa_handle {
   std::vector<Mark> marks;
   std::vector<cudaEvent_t> spare;
   csa::ItemList items;  // host-built indexer work list of the current call
-  csa::ItemList jobs;   // host-built attention job list of the current call
+  csa::JobLists jobs;   // host-built attention job lists of the current call
   int max_jobs = 0;     // attention tiles per query, at most
+  int epoch = 0;        // decode steps launched (the Top-K ready flags' value)
 };
 
 namespace {
@@ -247,12 +248,22 @@ bool use_pdl() {
 // SIMT kernel
 // early: the Top-K kernel of the same call runs right before (see
 // launch_attention_tc5)
+// The tile CTAs' split of the job lists follows from the batch alone (the
+// queries whose Top-K blocks select, vis > K, keep SMs busy when the tile
+// kernel of a decode step starts), whichever entry point launches it, so the
+// same batch and Top-K give the same output bits from csa_decode_step and
+// csa_sparse_attn.
 int run_attention(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, const int* idx,
                   const int* cnt, void* out, float* lse, cudaStream_t st, bool pdl, bool early) {
   if (csa::tensor_core_shape(h->dc) && csa::attention_impl() == csa::kAttnTc5) {
-    csa::host_jobs(h->dc, b->B, b->S, b->ctx_len_host, &h->jobs);
+    int selecting = 0;
+    if (b->ctx_len_host)
+      for (int i = 0; i < b->B; ++i)
+        for (int s = 0; s < b->S; ++s)
+          selecting += (b->ctx_len_host[i] - b->S + s + 1) / h->cfg.ratio > h->cfg.topk ? 1 : 0;
+    csa::host_jobs(h->dc, b->B, b->S, b->ctx_len_host, h->num_sms, selecting, &h->jobs);
     const int r = csa::launch_attention_tc5(h->dc, db, h->ws, h->jobs, idx, cnt, out, lse,
-                                            h->num_sms, st, pdl, early);
+                                            h->num_sms, st, pdl, early, h->epoch);
     if (r != -2) return r;
   }
   return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse, h->num_sms, st, pdl);
@@ -438,7 +449,8 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   const size_t o_cnt = off; off += al(sizeof(int) * maxT);
   const bool tc = csa::tensor_core_shape(d);
   h->max_jobs = tc ? csa::max_jobs_per_query(d) : 0;
-  const size_t o_jobs = off; off += al(sizeof(int) * (maxT + 1));
+  const size_t o_jobs = off; off += al(sizeof(int) * 2 * (maxT + 1));
+  const size_t o_ready = off; off += al(sizeof(int) * maxT);
   const size_t o_part = off; off += tc ? al(sizeof(__nv_bfloat16) * (size_t)maxT * h->max_jobs * d.H * d.V) : 0;
   const size_t o_plse = off; off += tc ? al(sizeof(float) * (size_t)maxT * h->max_jobs * d.H) : 0;
   h->ws_bytes = off;
@@ -446,6 +458,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaMalloc(workspace)"); }
   char* base = static_cast<char*>(h->ws_base);
   e = cudaMemset(base + o_status, 0, sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(base + o_ready, 0, sizeof(int) * maxT);  // epoch 0: never a step's
   if (e != cudaSuccess) { cudaFree(h->ws_base); delete h; return cuda_fail(e, "cudaMemset"); }
   csa::Workspace& w = h->ws;
   w.status = reinterpret_cast<int*>(base + o_status);
@@ -454,6 +467,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   w.topk_idx = reinterpret_cast<int*>(base + o_idx);
   w.topk_cnt = reinterpret_cast<int*>(base + o_cnt);
   w.job_prefix = reinterpret_cast<int*>(base + o_jobs);
+  w.topk_ready = reinterpret_cast<int*>(base + o_ready);
   w.part_o = tc ? reinterpret_cast<__nv_bfloat16*>(base + o_part) : nullptr;
   w.part_lse = tc ? reinterpret_cast<float*>(base + o_plse) : nullptr;
   w.max_T = maxT;
@@ -521,12 +535,16 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
   int* idx = topk_idx_out ? topk_idx_out : h->ws.topk_idx;
   int* cnt = topk_cnt_out ? topk_cnt_out : h->ws.topk_cnt;
   const bool pdl = use_pdl();
+  // this step's value of the per-query Top-K ready flags (never 0, the value
+  // the flags start with)
+  h->epoch = h->epoch == 0x7fffffff ? 1 : h->epoch + 1;
   Launches L;
   run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
   const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr, idx,
-                            cnt, h->ws.status, h->dc.max_vis, st, pdl, early);
+                            cnt, h->ws.status, h->dc.max_vis, st, pdl, early, h->ws.topk_ready,
+                            h->epoch);
   }));
   L.add(staged(h, kStageAttention, st, [&] {
     return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl, true);
@@ -644,6 +662,7 @@ int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* 
   w.topk_idx = nullptr;
   w.topk_cnt = nullptr;
   w.job_prefix = nullptr;
+  w.topk_ready = nullptr;
   w.part_o = nullptr;
   w.part_lse = nullptr;
   w.max_T = b->B * b->S;

@@ -117,8 +117,20 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
-// Job list: jobs of query q are [prefix[q], prefix[q+1]); in each query the
-// window tiles, then the compressed tiles, then the heavy tiles.
+// Coherent global loads of values another running kernel writes (never the
+// read-only path), and the acquire load of a flag.
+__device__ __forceinline__ int ld_cg(const int* p) {
+  int v;
+  asm volatile("ld.global.cg.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// One job list (see JobLists): jobs of query q are [prefix[q], prefix[q+1]).
 struct JobCursor {
   const int* prefix;
   int q, first, end;
@@ -139,6 +151,67 @@ struct JobCursor {
       first = end;
       end = prefix[q + 1];
     }
+  }
+};
+
+// The split of the two job lists over the tile CTAs.  CTA i takes the W jobs
+// [wstart(i), wstart(i+1)), spread over the first E CTAs (the ones that start
+// while the Top-K kernel still runs), then the C jobs [cstart(i),
+// cstart(i+1)), spread over all G.  Job ids: W jobs 0 .. NW-1, C jobs
+// NW .. NW+NC-1; a segment's partial output sits at the id of its first job.
+struct Sched {
+  const int* wp;
+  const int* cp;
+  int T, NW, NC, G, E;
+  __device__ __forceinline__ int wstart(int i) const {
+    return i >= E ? NW : (int)((int64_t)i * NW / E);
+  }
+  __device__ __forceinline__ int cstart(int i) const { return (int)((int64_t)i * NC / G); }
+};
+
+// A job of a CTA's sequence: its query, list (0 = W, 1 = C), index within
+// the query's jobs of that list, id, and whether it opens / closes a segment
+// (the CTA's consecutive jobs of one query in one list).
+struct JobRef {
+  int q, list, local, gid;
+  bool first, last;
+};
+
+// Walks a CTA's jobs in order (n increasing; the same n may be asked again).
+struct JobWalk {
+  JobCursor wc, cc;
+  int nw, nc, wlo, clo, NW;
+  __device__ __forceinline__ void init(const Sched& s, int cta) {
+    wlo = s.wstart(cta);
+    nw = s.wstart(cta + 1) - wlo;
+    clo = s.cstart(cta);
+    nc = s.cstart(cta + 1) - clo;
+    NW = s.NW;
+    if (nw > 0) wc.init(s.wp, s.T, wlo);
+    if (nc > 0) cc.init(s.cp, s.T, clo);
+  }
+  __device__ __forceinline__ JobRef get(int n) {
+    JobRef r;
+    if (n < nw) {
+      const int idx = wlo + n;
+      wc.advance(idx);
+      r.q = wc.q;
+      r.list = 0;
+      r.local = idx - wc.first;
+      r.gid = idx;
+      r.first = n == 0 || idx == wc.first;
+      r.last = n == nw - 1 || idx + 1 == wc.end;
+    } else {
+      const int m = n - nw, idx = clo + m;
+      cc.advance(idx);
+      r.q = cc.q;
+      r.list = 1;
+      r.local = idx - cc.first;
+      r.gid = NW + idx;
+      r.first = m == 0 || idx == cc.first;
+      r.last = m == nc - 1 || idx + 1 == cc.end;
+    }
+    return r;
   }
 };
 
@@ -168,20 +241,26 @@ __device__ __forceinline__ JobCtx job_ctx(const DevCfg& c, const DevBatch& b, in
 }
 
 // The compressed stream's length: the Top-K count, bounded by min(vis, K).
-__device__ __forceinline__ void job_topk_cnt(JobCtx& x, int q, const int* __restrict__ topk_cnt) {
+__device__ __forceinline__ void job_topk_cnt(JobCtx& x, int q, const int* topk_cnt) {
   int cnt = 0;
   if (!(x.p.flags & kPlanBad)) {
-    cnt = topk_cnt[q];
+    cnt = ld_cg(topk_cnt + q);
     cnt = cnt < 0 ? 0 : (cnt > x.p.cnt ? x.p.cnt : cnt);
   }
   x.n[1] = cnt;
 }
 
-__device__ __forceinline__ void job_stream(const JobCtx& x, int local, int& sid, int& t) {
-  if (local < x.nt[0]) { sid = 0; t = local; }
-  else if (local < x.nt[0] + x.nt[1]) { sid = 1; t = local - x.nt[0]; }
-  else { sid = 2; t = local - x.nt[0] - x.nt[1]; }
+// The stream and tile of a job (see JobLists): with the split, W jobs are
+// the window tiles, then the heavy tiles, and C jobs the compressed tiles;
+// without it a query's jobs are its window, compressed, then heavy tiles.
+__device__ __forceinline__ void job_stream(const JobCtx& x, const JobRef& r, bool split, int& sid,
+                                           int& t) {
+  if (split && r.list == 1) { sid = 1; t = r.local; }
+  else if (r.local < x.nt[0]) { sid = 0; t = r.local; }
+  else if (!split && r.local < x.nt[0] + x.nt[1]) { sid = 1; t = r.local - x.nt[0]; }
+  else { sid = 2; t = r.local - x.nt[0] - (split ? 0 : x.nt[1]); }
 }
+
 
 // Pool row of stream row i of the job, or -1 (read as zeros by the gather and
 // masked by the softmax) when the row does not exist or is out of range.
@@ -221,9 +300,9 @@ __device__ __forceinline__ int job_row(const DevBatch& b, const JobCtx& x, int s
 // row lookups are one add)
 template <bool kPaged>
 __global__ void __launch_bounds__(kA5Threads, 1)
-    attn_tile_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
-                     const int* __restrict__ topk_idx, const int* __restrict__ topk_cnt,
-                     int early) {
+    attn_tile_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ JobLists jobs,
+                     DevCfg c, DevBatch b, Workspace ws, const int* topk_idx, const int* topk_cnt,
+                     int early, int epoch) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ A5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -233,21 +312,31 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = b.B * b.S;
-  // Launched right after this library's Top-K kernel of the same step
-  // (early != 0), every input but the Top-K outputs was complete before the
-  // step's first kernel passed its own wait, so only the row loaders wait
-  // for the previous grid, when they first read topk_idx / topk_cnt, and
-  // setup, Q and window rows overlap its tail.  Otherwise (a caller's kernel
-  // before this one, or a job list built on the device) every thread waits
-  // first.
-  const bool wait_all = !(early && jobs.host_B >= 0);
-  if (wait_all) pdl_wait();
-  const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
-  const int N = prefix[T];
-  const int lo = (int)((int64_t)blockIdx.x * N / gridDim.x);
-  const int hi = (int)((int64_t)(blockIdx.x + 1) * N / gridDim.x);
+  // Launched right after this library's Top-K kernel of the same step with
+  // host-built job lists (flags = early != 0), every input but the Top-K
+  // outputs was complete before the step's first kernel passed its own wait,
+  // so nothing waits for the previous grid up front: setup, Q and the W jobs
+  // overlap the Top-K kernel, and a query's C jobs start once that query's
+  // Top-K block has published its output (ws.topk_ready[q] == epoch).
+  // Otherwise (a caller's kernel before this one, or job lists built on the
+  // device) every thread waits for the previous grid first.
+  const bool flags = early && jobs.host_T >= 0;
+  if (!flags) pdl_wait();
+  Sched sc;
+  sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
+  sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
+  sc.T = T;
+  sc.NW = sc.wp[T];
+  sc.NC = sc.cp[T];
+  sc.G = gridDim.x;
+  sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < (int)gridDim.x) ? jobs.early : (int)gridDim.x;
+  const int J = (sc.wstart(blockIdx.x + 1) - sc.wstart(blockIdx.x)) +
+                (sc.cstart(blockIdx.x + 1) - sc.cstart(blockIdx.x));
   pdl_trigger();
-  if (lo >= hi) return;
+  if (J == 0) {
+    if (flags) pdl_wait();  // this grid completes after its predecessor
+    return;
+  }
   volatile int* abort = &sm.abort;
   // polls before a consumer wait gives up (the default: about a second)
   const uint32_t wpolls = c.wait_polls < 0 ? tc5::kBackoffPolls : (uint32_t)c.wait_polls;
@@ -295,17 +384,17 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     const __nv_bfloat16* null_src = static_cast<const __nv_bfloat16*>(b.q);
     const int ch = lane & 7;
     const uint64_t rpol = tc5::policy_evict_first();  // rows are read once per step
-    JobCursor cur;
-    cur.init(prefix, T, lo);
+    JobWalk walk;
+    walk.init(sc, blockIdx.x);
     int m = 0;
-    bool waited = wait_all;
-    for (int job = lo + g; job < hi; job += 2, ++m) {
+    bool waited = !flags;
+    for (int n = g; n < J; n += 2, ++m) {
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
-      cur.advance(job);
-      const int q = cur.q;
+      const JobRef r = walk.get(n);
+      const int q = r.q;
       JobCtx x = job_ctx(c, b, q);
       int sid, t;
-      job_stream(x, job - cur.first, sid, t);
+      job_stream(x, r, jobs.host_T >= 0 && jobs.split, sid, t);
       const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(
           sid == 0 ? b.raw : (sid == 1 ? b.cmp : b.hca));
       const int64_t stride = sid == 0 ? b.raw_stride : (sid == 1 ? b.cmp_stride : b.hca_stride);
@@ -317,7 +406,28 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 #pragma unroll
       for (int i = 0; i < kQuadsPerWarp; ++i) jr[i] = -1;
       if (sid == 1) {
-        if (!waited) {
+        if (flags) {
+          // this query's Top-K output: lane 0 polls its flag (bounded), then
+          // every lane acquires it before reading the output
+          bool ok = true;
+          if (lane == 0) {
+            uint32_t ns = 32;
+            uint32_t i = 0;
+            while (ld_acquire(ws.topk_ready + q) != epoch) {
+              if (++i >= wpolls || (((i & 15u) == 15u) && *abort)) {
+                *abort = 1;
+                ok = false;
+                break;
+              }
+              if (i >= 8) {
+                __nanosleep(ns);
+                ns = ns * 2 > 256 ? 256 : ns * 2;
+              }
+            }
+          }
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+          (void)ld_acquire(ws.topk_ready + q);
+        } else if (!waited) {
           pdl_wait();
           waited = true;
         }
@@ -325,7 +435,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         for (int i = 0; i < kQuadsPerWarp; ++i) {
           const int rq = lw + kLoadWarps * i;
           const int ri = t * kTile + 4 * rq + (lane >> 3);
-          if (rq < kTile / 4 && ri < c.K) jr[i] = topk_idx[(int64_t)q * c.K + ri];
+          if (rq < kTile / 4 && ri < c.K) jr[i] = ld_cg(topk_idx + (int64_t)q * c.K + ri);
         }
         job_topk_cnt(x, q, topk_cnt);
       }
@@ -390,21 +500,20 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       const uint64_t dq = tc5::sdesc_k_sw128(qres);
       const uint64_t dbuf = tc5::sdesc_k_sw128(bufs);
       const uint64_t dv = sdesc_mn_sw128(bufs, kSub);
-      JobCursor qc, pc;  // cursors of the next QK job and the next PV job
-      qc.init(prefix, T, lo);
-      pc.init(prefix, T, lo);
-      const int J = hi - lo;
+      JobWalk qw, pw;  // the next QK job and the next PV job
+      qw.init(sc, blockIdx.x);
+      pw.init(sc, blockIdx.x);
       int nk = 0, np = 0;  // CTA-local index of the next job to QK / to PV
-      int nq = 0, nqd = 0, seg = 0, cur_q = -1;
-      int qstate = 0;      // 0 Q of cur_q resident, 1 waiting for qdone, 2 waiting for qfull
+      int nq = 0, nqd = 0, seg = 0;
+      int qseg = -1;       // first job of the segment whose Q is resident (or loading)
+      int kseg = 0;        // first job of nk's segment
+      int qstate = 0;      // 0 Q of qseg resident, 1 waiting for qdone, 2 waiting for qfull
       uint32_t idle = 0;
       while (np < J) {
         bool progressed = false;
         if (np < nk) {
-          const int job = lo + np;
-          pc.advance(job);
-          const bool first = job == lo || job == pc.first;
-          const bool last = job + 1 == hi || job + 1 == pc.end;
+          const JobRef r = pw.get(np);
+          const bool first = r.first, last = r.last;
           const int g = np & 1;
           if ((!first || seg == 0 || tc5::mbar_try_wait(smem_u32(&sm.o_empty), (seg - 1) & 1)) &&
               tc5::mbar_try_wait(smem_u32(&sm.p_full[g]), (np >> 1) & 1)) {
@@ -429,11 +538,11 @@ __global__ void __launch_bounds__(kA5Threads, 1)
           }
         }
         if (nk < J) {
-          const int job = lo + nk;
-          qc.advance(job);
-          if (qc.q != cur_q) {
-            // a new query: its heads replace Q once the QK MMAs of the
-            // previous query are done (qdone)
+          const JobRef r = qw.get(nk);
+          if (r.first) kseg = nk;
+          if (kseg != qseg) {
+            // a new segment: its query's heads replace Q once the QK MMAs of
+            // the previous segment are done (qdone)
             if (qstate == 0) qstate = nk == 0 ? 3 : 1;
             if (qstate == 1 && tc5::mbar_try_wait(smem_u32(&sm.qdone), nqd & 1)) {
               ++nqd;
@@ -442,17 +551,17 @@ __global__ void __launch_bounds__(kA5Threads, 1)
             if (qstate == 3) {
               tc5::mbar_expect_tx(smem_u32(&sm.qfull), kQBytes);
               for (int k = 0; k < 9; ++k)
-                tc5::tma_load_2d(qres + k * kQSub, &qmap, k * 64, qc.q * kTcH, smem_u32(&sm.qfull));
+                tc5::tma_load_2d(qres + k * kQSub, &qmap, k * 64, r.q * kTcH, smem_u32(&sm.qfull));
               qstate = 2;
             }
             if (qstate == 2 && tc5::mbar_try_wait(smem_u32(&sm.qfull), nq & 1)) {
               ++nq;
               qstate = 0;
-              cur_q = qc.q;
+              qseg = kseg;
             }
           }
           const int g = nk & 1, m = nk >> 1;
-          if (qc.q == cur_q && (m == 0 || tc5::mbar_try_wait(smem_u32(&sm.s_empty[g]), (m - 1) & 1)) &&
+          if (kseg == qseg && (m == 0 || tc5::mbar_try_wait(smem_u32(&sm.s_empty[g]), (m - 1) & 1)) &&
               tc5::mbar_try_wait(smem_u32(&sm.full[g]), m & 1)) {
             // S = Q . R^T over 576 dims (M = 64 heads, N = 64 rows)
             tc5::fence_after_sync();
@@ -465,7 +574,8 @@ __global__ void __launch_bounds__(kA5Threads, 1)
                 tc5::mma_bf16(ds, dq + ((k * kQSub + 32 * i) >> 4), db + ((k * kSub + 32 * i) >> 4),
                               idesc_s, (k | i) ? 1u : 0u);
             tc5::mma_commit(smem_u32(&sm.s_full[g]));
-            if (job + 1 < hi && job + 1 == qc.end) tc5::mma_commit(smem_u32(&sm.qdone));
+            // Q is reloaded at every segment start: its last QK frees it
+            if (r.last && nk + 1 < J) tc5::mma_commit(smem_u32(&sm.qdone));
             ++nk;
             progressed = true;
           }
@@ -499,15 +609,14 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const float sc2 = c.scale * kLog2e;
     float mref = -INFINITY, lrun = 0.f;
-    JobCursor cur;
-    cur.init(prefix, T, lo);
-    int n = 0, seg = 0, slot = lo;
+    JobWalk walk;
+    walk.init(sc, blockIdx.x);
+    int seg = 0, slot = 0;
     bool bad = false;  // a wait of this thread gave up
-    for (int job = lo; job < hi; ++job, ++n) {
-      cur.advance(job);
-      const bool first = job == lo || job == cur.first;
-      const bool last = job + 1 == hi || job + 1 == cur.end;
-      if (first) slot = job;
+    for (int n = 0; n < J; ++n) {
+      const JobRef r = walk.get(n);
+      const bool first = r.first, last = r.last;
+      if (first) slot = r.gid;
       const int g = n & 1, m = n >> 1;
       uint64_t mk = 0;
       if (!bad && !tc5::mbar_wait_backoff(smem_u32(&sm.mfull[g]), m & 1, abort, 64, wpolls)) bad = true;
@@ -683,32 +792,51 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   __syncthreads();
   tc5::fence_after_sync();
   if (warp == 4) tc5::tmem_dealloc(tmem, 512);
+  // with flags nothing above waited for the previous grid: this grid then
+  // completes only after it (the Top-K blocks have published by now), so
+  // that every later kernel of the stream still follows the Top-K kernel
+  if (flags) pdl_wait();
 }
 
-// Per (query, 64 output dims): LSE merge of the query's segment partials in
-// job order, inverse RoPE on the last R dims, bf16 store.  The segments are
-// the query's job range cut at the tile kernel's CTA boundaries (CTA i takes
-// jobs [iN/G, (i+1)N/G)); with N >= G the starts are strictly increasing, so
-// segment k > 0 starts at (i0 + k)N/G directly.  Thread t owns head t >> 2 and
+// Per (query, 64 output dims): LSE merge of the query's segment partials,
+// inverse RoPE on the last R dims, bf16 store.  The segments are the query's
+// W jobs cut at the tile CTAs' W ranges, then its C jobs cut at their C
+// ranges (see Sched); one thread lists them.  Thread t owns head t >> 2 and
 // 16 consecutive dims (t & 3) of the block's 64: it loads its head's LSE and
-// a 32-byte piece of the partials, four segments per batch, derives the
+// a 32-byte piece of the partials, two segments per batch, derives the
 // weights itself (running max across batches), and stores 32 bytes.
 constexpr int kMergeUnroll = 2;  // partials whose loads are in flight together
-__global__ void __launch_bounds__(256, 3)
-    attn_merge_kernel(const __grid_constant__ ItemList jobs, DevCfg c, DevBatch b, Workspace ws,
+
+// Appends to seg[] the partial slots of the CTA ranges that intersect the
+// jobs [a, b) of one list of n jobs split at start(i), i < g (id offset
+// `base`); returns the new count.
+template <typename Start>
+__device__ int list_segments(int a, int b, int n, int g, int base, Start start, int* seg, int k) {
+  if (b <= a || n <= 0) return k;
+  int i = (int)((int64_t)a * g / n);
+  if (i >= g) i = g - 1;
+  while (i + 1 < g && start(i + 1) <= a) ++i;
+  for (; i < g && k < kMergeMaxJobs; ++i) {
+    const int lo = start(i), hi = i + 1 < g ? start(i + 1) : n;
+    if (lo >= b) break;
+    if (hi > lo && hi > a) seg[k++] = base + (lo > a ? lo : a);
+  }
+  return k;
+}
+
+__global__ void __launch_bounds__(256, 4)
+    attn_merge_kernel(const __grid_constant__ JobLists jobs, DevCfg c, DevBatch b, Workspace ws,
                       int G, __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   __shared__ int seg[kMergeMaxJobs + 1];
   __shared__ int nseg_s;
   __shared__ float2 rope[kRopeTable];  // cos, sin of the block's rotary pairs
-  // The segment list and the rotary table need only the job list and the
+  // The segment list and the rotary table need only the job lists and the
   // lengths, which are complete before the tile kernel lets this grid
   // launch (the tile kernel waits for the job-list kernel before it
   // triggers, and for the caller's inputs before it or its predecessor
   // does); only the partials wait for the tile grid.
   const int q = blockIdx.x, dg = blockIdx.y, t = threadIdx.x;
   const int T = b.B * b.S;
-  const int* __restrict__ prefix = jobs.host_B >= 0 ? jobs.prefix : ws.job_prefix;
-  const int N = prefix[T], j0 = prefix[q], j1 = prefix[q + 1];
   const int rope0 = kTcV - c.R;  // first rotary dim
   if (dg * kMergeDims + kMergeDims > rope0 && t >= 64 && t < 64 + c.R / 2 && t - 64 < kRopeTable) {
     const int bi = q / b.S;
@@ -716,37 +844,19 @@ __global__ void __launch_bounds__(256, 3)
     const int i = t - 64;
     rope[i] = (p.flags & kPlanBad) ? make_float2(1.f, 0.f) : rope_cos_sin((double)p.pos, c.rope_theta[i]);
   }
-  // CTA i starts at job (i N) / G; 32-bit arithmetic while i N fits
-  const bool small = (uint64_t)N * (uint64_t)G < (1ull << 32);
-  auto cta_start = [&](int i) -> int {
-    return small ? (int)((uint32_t)i * (uint32_t)N / (uint32_t)G) : (int)((int64_t)i * N / G);
-  };
-  if (j1 <= j0) {
-    if (t == 0) nseg_s = 0;
-  } else if (N >= G) {
-    // starts strictly increase: with i0 the CTA holding j0, segment t > 0
-    // starts at (i0 + t)N/G while that is < j1
-    if (t < kMergeMaxJobs) {
-      int i0 = small ? (int)((uint32_t)j0 * (uint32_t)G / (uint32_t)N) : (int)((int64_t)j0 * G / N);
-      if (i0 + 1 < G && cta_start(i0 + 1) <= j0) ++i0;
-      const int i = i0 + t;
-      const int l = t == 0 ? j0 : (i < G ? cta_start(i) : j1);
-      if (l < j1) seg[t] = l;
-      const int lnext = i + 1 < G ? cta_start(i + 1) : j1;
-      if (l < j1 && lnext >= j1) nseg_s = t + 1;  // the last segment
-    }
-  } else if (t == 0) {
-    // more CTAs than jobs: runs of equal starts, walked in order
-    int k = 0, last = j0;
-    seg[k++] = j0;
-    for (int i = (int)((int64_t)j0 * G / N) + 1; i < G && k < kMergeMaxJobs; ++i) {
-      const int l = cta_start(i);
-      if (l >= j1) break;
-      if (l > last) {
-        seg[k++] = l;
-        last = l;
-      }
-    }
+  if (t == 0) {
+    Sched sc;
+    sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
+    sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
+    sc.T = T;
+    sc.NW = sc.wp[T];
+    sc.NC = sc.cp[T];
+    sc.G = G;
+    sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < G) ? jobs.early : G;
+    int k = list_segments(sc.wp[q], sc.wp[q + 1], sc.NW, sc.E, 0,
+                          [&](int i) { return sc.wstart(i); }, seg, 0);
+    k = list_segments(sc.cp[q], sc.cp[q + 1], sc.NC, sc.G, sc.NW,
+                      [&](int i) { return sc.cstart(i); }, seg, k);
     nseg_s = k;
   }
   __syncthreads();
@@ -820,30 +930,50 @@ __global__ void __launch_bounds__(256, 3)
     lse_out[(int64_t)q * kTcH + h] = M == -INFINITY ? -INFINITY : (M + log2f(tot)) * 0.6931471805599453f;
 }
 
-// Counts each query's jobs into ws.job_prefix when the host has no lengths.
+// W and C job counts of a query (see JobLists), from the bound min(vis, K).
+__host__ __device__ __forceinline__ void query_jobs(int nwin, int cnt, int vis2, int* nw, int* nc) {
+  *nw = (nwin + kTile - 1) / kTile + (vis2 + kTile - 1) / kTile;
+  *nc = (cnt + kTile - 1) / kTile;
+}
+
+// Builds the job lists into ws.job_prefix when the host has no lengths.
 __global__ void __launch_bounds__(1024) job_prep_kernel(DevCfg c, DevBatch b, Workspace ws) {
   __shared__ int scan_tmp[33];
-  __shared__ int carry;
+  __shared__ int wcarry, ccarry;
   pdl_wait();
   const int T = b.B * b.S;
-  if (threadIdx.x == 0) carry = 0;
+  int* wp = ws.job_prefix;
+  int* cp = ws.job_prefix + (T + 1);
+  if (threadIdx.x == 0) wcarry = ccarry = 0;
   __syncthreads();
   for (int base = 0; base < T; base += blockDim.x) {
     const int q = base + threadIdx.x;
-    int n = 0;
-    if (q < T) {
+    int nw = 0, nc = 0;
+    if (q < T) {  // no split: every tile of the query in the C list
       const int bi = q / b.S;
       const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
-      n = (p.nwin + kTile - 1) / kTile + (p.cnt + kTile - 1) / kTile + (p.vis2 + kTile - 1) / kTile;
+      query_jobs(p.nwin, p.cnt, p.vis2, &nw, &nc);
+      nc += nw;
+      nw = 0;
     }
-    int total;
-    const int ex = block_exclusive_scan(n, scan_tmp, &total);
-    if (q < T) ws.job_prefix[q] = carry + ex;
+    int wtot, ctot;
+    const int wex = block_exclusive_scan(nw, scan_tmp, &wtot);
+    const int cex = block_exclusive_scan(nc, scan_tmp, &ctot);
+    if (q < T) {
+      wp[q] = wcarry + wex;
+      cp[q] = ccarry + cex;
+    }
     __syncthreads();
-    if (threadIdx.x == 0) carry += total;
+    if (threadIdx.x == 0) {
+      wcarry += wtot;
+      ccarry += ctot;
+    }
     __syncthreads();
   }
-  if (threadIdx.x == 0) ws.job_prefix[T] = carry;
+  if (threadIdx.x == 0) {
+    wp[T] = wcarry;
+    cp[T] = ccarry;
+  }
   pdl_trigger();
 }
 
@@ -861,15 +991,27 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t stride, u
 
 }  // namespace
 
-// Builds the job list on the host when the lengths are known (jobs.host_B =
-// number of queries), else leaves host_B = -1 for the device prep kernel.
-void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, ItemList* jobs) {
-  jobs->host_B = -1;
+// Builds the job lists on the host when the lengths are known (jobs.host_T =
+// number of queries), else leaves host_T = -1 for the device job-list kernel.
+// The W jobs go to the tile CTAs that find a free SM when the grid starts:
+// the grid's CTAs take SMs in index order, and the Top-K blocks that select
+// hold topk_blocks SMs until they finish.
+void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, int num_sms, int topk_blocks,
+               JobLists* jobs) {
+  jobs->host_T = -1;
+  jobs->split = 0;
+  jobs->early = 0;
   if (!lens_host || B * S > kMaxHostReq) return;
-  int acc = 0;
+  // CSA_EARLY_SPLIT=1: the W / C split (see JobLists); by default one list
+  static const bool split = [] {
+    const char* e = getenv("CSA_EARLY_SPLIT");
+    return e && e[0] == '1';
+  }();
+  int wacc = 0, cacc = 0;
   for (int bi = 0; bi < B; ++bi)
     for (int s = 0; s < S; ++s) {
-      jobs->prefix[bi * S + s] = acc;
+      jobs->wprefix[bi * S + s] = wacc;
+      jobs->cprefix[bi * S + s] = cacc;
       const int L = lens_host[bi];
       if (L < S || L > c.max_context) continue;
       const int pos = L - S + s;
@@ -877,10 +1019,23 @@ void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, ItemList
       const int nwin = c.win < pos + 1 ? c.win : pos + 1;
       const int cnt = vis < c.K ? vis : c.K;
       const int vis2 = c.hca_ratio > 0 ? (pos + 1) / c.hca_ratio : 0;
-      acc += (nwin + kTile - 1) / kTile + (cnt + kTile - 1) / kTile + (vis2 + kTile - 1) / kTile;
+      int nw, nc;
+      query_jobs(nwin, cnt, vis2, &nw, &nc);
+      if (!split) {
+        nc += nw;
+        nw = 0;
+      }
+      wacc += nw;
+      cacc += nc;
     }
-  jobs->prefix[B * S] = acc;
-  jobs->host_B = B * S;
+  jobs->wprefix[B * S] = wacc;
+  jobs->cprefix[B * S] = cacc;
+  jobs->host_T = B * S;
+  jobs->split = split ? 1 : 0;
+  // early CTAs: the SMs the selecting Top-K blocks leave free; too few of
+  // them would be swamped with the W jobs, and then all CTAs share them
+  const int early = num_sms - (topk_blocks < num_sms ? topk_blocks : num_sms);
+  jobs->early = (split && topk_blocks > 0 && early >= num_sms / 4) ? early : 0;
 }
 
 // Jobs one query can have at most (sizes the partial-output workspace).
@@ -894,8 +1049,9 @@ int max_jobs_per_query(const DevCfg& c) {
 // Returns launches (>= 1), 0 with nothing to do, -1 on failure, -2 if the
 // batch does not fit this path (the caller then uses the warp-MMA kernel).
 int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
-                         const ItemList& jobs, const int* topk_idx, const int* topk_cnt, void* out,
-                         float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early) {
+                         JobLists& jobs, const int* topk_idx, const int* topk_cnt, void* out,
+                         float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early,
+                         int epoch) {
   const int T = b.B * b.S;
   if (T == 0) return 0;
   if (!ws.part_o || max_jobs_per_query(c) > kMergeMaxJobs || b.raw_rows > 0x7fffffffLL ||
@@ -913,15 +1069,20 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
     return launch_fail("cudaFuncSetAttribute(attn_tile_kernel)", e);
   const bool paged = b.raw_table || b.cmp_table || b.hca_table;
   int n = 0;
-  if (jobs.host_B < 0) {
+  if (jobs.host_T < 0) {
     if (launch_kernel(job_prep_kernel, dim3(1), dim3(1024), 0, st, pdl, c, b, ws) < 0) return -1;
     ++n;
   }
   int grid = num_sms;
-  if (jobs.host_B >= 0 && jobs.prefix[T] < grid) grid = jobs.prefix[T] > 0 ? jobs.prefix[T] : 1;
+  if (jobs.host_T >= 0) {
+    const int total = jobs.wprefix[T] + jobs.cprefix[T];
+    if (total < grid) grid = total > 0 ? total : 1;
+  }
+  // the Top-K ready flags stand in for the grid dependency only when this
+  // kernel follows the step's own Top-K kernel through a programmatic launch
   if (launch_kernel(paged ? attn_tile_kernel<true> : attn_tile_kernel<false>, dim3(grid),
                     dim3(kA5Threads), kA5Dyn, st, pdl, qmap, jobs, c, b, ws, topk_idx, topk_cnt,
-                    (pdl && early) ? 1 : 0) < 0)
+                    (pdl && early) ? 1 : 0, epoch) < 0)
     return -1;
   ++n;
   if (launch_kernel(attn_merge_kernel, dim3(T, kTcV / kMergeDims), dim3(256), 0, st, pdl, jobs, c,

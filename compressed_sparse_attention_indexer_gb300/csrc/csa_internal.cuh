@@ -156,6 +156,24 @@ struct ItemList {
   int prefix[kMaxHostReq + 1];
 };
 
+// The attention job lists of a call, as prefixes over the queries.  With
+// `split`, per query its W jobs (64-row tiles of the window stream, then of
+// the heavy stream: nothing of the Top-K) and its C jobs (tiles of the
+// compressed stream); without, no W jobs and every tile of the query (window,
+// compressed, heavy) in the C list.  Built on the host when it knows the
+// lengths (host_T = number of queries), else by the job-list kernel into the
+// workspace (host_T = -1, no split: W prefix at ws.job_prefix[0 .. T], C
+// prefix at ws.job_prefix[T + 1 .. 2T + 1]).  `early`: tile CTAs that share
+// the W jobs (0: all of them); the others start when the Top-K kernel's
+// blocks leave their SMs.
+struct JobLists {
+  int host_T;
+  int split;
+  int early;
+  int wprefix[kMaxHostReq + 1];
+  int cprefix[kMaxHostReq + 1];
+};
+
 // Device workspace owned by a handle.
 struct Workspace {
   int* status;        // [1]
@@ -163,7 +181,8 @@ struct Workspace {
   float* scores;      // [max_T, max_vis]
   int* topk_idx;      // [max_T, K]
   int* topk_cnt;      // [max_T]
-  int* job_prefix;    // [max_T + 1] attention tiles per query, prefix (device-built)
+  int* job_prefix;    // [2 (max_T + 1)] attention job lists (device-built, see JobLists)
+  int* topk_ready;    // [max_T] per query: the step epoch whose Top-K output is complete
   __nv_bfloat16* part_o;  // [max_T * max_jobs, H, V] per-segment normalised attention output
                           // (bf16: the range of fp32, so any row magnitude survives)
   float* part_lse;    // [max_T * max_jobs, H] per-segment log-sum-exp (log2 units)
@@ -287,18 +306,28 @@ int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, i
                      cudaStream_t st, bool pdl);
 // early: this library's own kernel of the same call runs right before (the
 // lengths are then read before the grid dependency wait)
+// ready / epoch: when ready is not NULL, each query's block stores `epoch`
+// into ready[q] once its outputs are complete (the attention kernel of the
+// same step starts that query's compressed tiles on it)
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st, bool pdl, bool early);
+                cudaStream_t st, bool pdl, bool early, int* ready = nullptr, int epoch = 0);
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
                      cudaStream_t st, bool pdl);
 // early: launched right after this library's Top-K kernel of the same step,
-// so the tile kernel may read the caller's inputs before its grid wait.
+// which signals each query through ws.topk_ready with `epoch`: the tile
+// kernel reads the caller's inputs before its grid wait and starts a query's
+// compressed tiles once that query's Top-K output is complete.
 int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
-                         const ItemList& jobs, const int* topk_idx, const int* topk_cnt, void* out,
-                         float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early);
-void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, ItemList* jobs);
+                         JobLists& jobs, const int* topk_idx, const int* topk_cnt, void* out,
+                         float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early,
+                         int epoch);
+// Builds the job lists on the host when the lengths are known; `topk_blocks`:
+// Top-K blocks of the step that select (their SMs are busy when the tile
+// kernel starts), 0 when no Top-K kernel runs right before.
+void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, int num_sms, int topk_blocks,
+               JobLists* jobs);
 int max_jobs_per_query(const DevCfg& c);
 constexpr int kAttnMma = 0, kAttnTc5 = 1;
 int attention_impl();

@@ -50,6 +50,18 @@ __device__ __forceinline__ uint32_t score_key_fast(float f) {
   return g != g ? 0u : u;
 }
 
+// Publishes a query's Top-K output to the attention kernel of the same step,
+// which may already be running (it waits for the flag with bounded polls):
+// every thread fences its writes, the block meets, and one thread stores the
+// step's epoch with release semantics.  A no-op without a flag array.
+__device__ __forceinline__ void signal_ready(int* ready, int q, int epoch) {
+  if (!ready) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0)
+    asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ready + q), "r"(epoch) : "memory");
+}
+
 // Key i lives at keys[kpad(i)]: one pad word per 16 keys, so the final pass
 // (thread t reads keys 16t .. 16t+15) hits 32 different banks.
 __device__ __forceinline__ int kpad(int i) { return i + (i >> 4); }
@@ -57,7 +69,8 @@ __device__ __forceinline__ int kpad(int i) { return i + (i >> 4); }
 __global__ void __launch_bounds__(kTopkThreads, 1)
     topk_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
                 const int* __restrict__ n_override, int* __restrict__ idx_out,
-                int* __restrict__ cnt_out, int* __restrict__ status, int max_vis) {
+                int* __restrict__ cnt_out, int* __restrict__ status, int max_vis, int* ready,
+                int epoch) {
   extern __shared__ __align__(16) uint32_t keys[];
   __shared__ int hist[kBins];
   __shared__ int scan_tmp[33];
@@ -88,6 +101,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
   if (!do_select) {  // bypass: every visible row
     for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
     if (tid == 0) cnt_out[q] = n < K ? n : K;
+    signal_ready(ready, q, epoch);
     return;
   }
   const float* sc = scores + (int64_t)q * ld;
@@ -193,6 +207,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     if (sel) out[pos++] = i;
   }
   if (tid == 0) cnt_out[q] = K;
+  signal_ready(ready, q, epoch);
 }
 
 // Register-resident variant for rows of at most kJ * 1024 keys (the common
@@ -251,7 +266,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     topk_reg_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
                     const int* __restrict__ n_override, int* __restrict__ idx_out,
                     int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
-                    int early) {
+                    int early, int* ready, int epoch) {
   static_assert(kJ == 2 || kJ % 4 == 0, "keys are loaded as float2 or float4 vectors");
   __shared__ int hist[kBins];
   __shared__ uint32_t cand_key[kCand];
@@ -298,6 +313,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   if (!do_select) {  // bypass: every visible row
     for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
     if (tid == 0) cnt_out[q] = n < K ? n : K;
+    signal_ready(ready, q, epoch);
     return;
   }
   const float* sc = scores + (int64_t)q * ld;
@@ -492,6 +508,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
       ++pos;
     }
   if (tid == 0) cnt_out[q] = K;
+  signal_ready(ready, q, epoch);
 }
 
 }  // namespace
@@ -508,7 +525,7 @@ bool topk_use_reg(int max_vis) {
 
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st, bool pdl, bool early) {
+                cudaStream_t st, bool pdl, bool early, int* ready, int epoch) {
   if (nq == 0) return 0;
   DevBatch none = {};
   none.S = 1;
@@ -516,7 +533,8 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
     return launch_kernel(max_vis <= kShortKeys * kTopkThreads ? topk_reg_kernel<kShortKeys>
                                                               : topk_reg_kernel<kRegKeys>,
                          dim3(nq), dim3(kTopkThreads), 0, st, pdl, c, b ? *b : none, scores, ld,
-                         n_override, idx_out, cnt_out, status, max_vis, (pdl && early) ? 1 : 0);
+                         n_override, idx_out, cnt_out, status, max_vis, (pdl && early) ? 1 : 0,
+                         ready, epoch);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
   if (smem > kTopkSmemMax)  // rows are bounded at create time
     return launch_fail("Top-K: rows longer than the kernel holds", cudaSuccess);
@@ -529,7 +547,7 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
       return launch_fail("cudaFuncSetAttribute(topk_kernel)", e);
   }
   return launch_kernel(topk_kernel, dim3(nq), dim3(kTopkThreads), smem, st, pdl, c, b ? *b : none,
-                       scores, ld, n_override, idx_out, cnt_out, status, max_vis);
+                       scores, ld, n_override, idx_out, cnt_out, status, max_vis, ready, epoch);
 }
 
 }  // namespace csa
