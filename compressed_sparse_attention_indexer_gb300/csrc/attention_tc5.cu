@@ -134,12 +134,17 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 struct JobCursor {
   const int* prefix;
   int q, first, end;
-  __device__ __forceinline__ void init(const int* p, int T, int job) {
+  // q0 >= 0: the query holding `job`, known already; else found by search
+  __device__ __forceinline__ void init(const int* p, int T, int job, int q0) {
     prefix = p;
-    int l = 0, r = T - 1;
-    while (l < r) {
-      const int m = (l + r + 1) >> 1;
-      if (p[m] <= job) l = m; else r = m - 1;
+    int l = q0;
+    if (l < 0) {
+      l = 0;
+      int r = T - 1;
+      while (l < r) {
+        const int m = (l + r + 1) >> 1;
+        if (p[m] <= job) l = m; else r = m - 1;
+      }
     }
     q = l;
     first = p[l];
@@ -162,6 +167,7 @@ struct JobCursor {
 struct Sched {
   const int* wp;
   const int* cp;
+  const uint16_t* cq;  // per-CTA first queries (cta_q of the lists) or null
   int T, NW, NC, G, E;
   __device__ __forceinline__ int wstart(int i) const {
     return i >= E ? NW : (int)((int64_t)i * NW / E);
@@ -187,8 +193,8 @@ struct JobWalk {
     clo = s.cstart(cta);
     nc = s.cstart(cta + 1) - clo;
     NW = s.NW;
-    if (nw > 0) wc.init(s.wp, s.T, wlo);
-    if (nc > 0) cc.init(s.cp, s.T, clo);
+    if (nw > 0) wc.init(s.wp, s.T, wlo, s.cq ? (int)s.cq[cta] : -1);
+    if (nc > 0) cc.init(s.cp, s.T, clo, s.cq ? (int)s.cq[kMaxTileCtas + cta] : -1);
   }
   __device__ __forceinline__ JobRef get(int n) {
     JobRef r;
@@ -226,10 +232,10 @@ struct JobCtx {
 
 // The job's query plan and its stream lengths, from the caller's inputs
 // only; the compressed count (a Top-K output) is filled in by job_topk_cnt.
-__device__ __forceinline__ JobCtx job_ctx(const DevCfg& c, const DevBatch& b, int q) {
+__device__ __forceinline__ JobCtx job_ctx(const DevCfg& c, const DevBatch& b, int q, int len) {
   JobCtx x;
   x.bi = q / b.S;
-  x.p = query_plan(c, b.S, b.ctx_len[x.bi], q - x.bi * b.S, 0);
+  x.p = query_plan(c, b.S, len, q - x.bi * b.S, 0);
   x.n[0] = x.p.nwin;
   x.n[1] = 0;
   x.n[2] = x.p.vis2;
@@ -325,9 +331,10 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   Sched sc;
   sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
   sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
+  sc.cq = jobs.host_T >= 0 && jobs.cta_first ? &jobs.cta_q[0][0] : nullptr;
   sc.T = T;
-  sc.NW = sc.wp[T];
-  sc.NC = sc.cp[T];
+  sc.NW = jobs.host_T >= 0 ? jobs.NW : sc.wp[T];
+  sc.NC = jobs.host_T >= 0 ? jobs.NC : sc.cp[T];
   sc.G = gridDim.x;
   sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < (int)gridDim.x) ? jobs.early : (int)gridDim.x;
   const int J = (sc.wstart(blockIdx.x + 1) - sc.wstart(blockIdx.x)) +
@@ -391,15 +398,24 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     for (int n = g; n < J; n += 2, ++m) {
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
       const JobRef r = walk.get(n);
-      const int q = r.q;
-      JobCtx x = job_ctx(c, b, q);
+      const int q = r.q, bi = q / b.S;
+      const bool split = jobs.host_T >= 0 && jobs.split;
+      // the job's independent loads go out together: the request's length,
+      // its pool offsets and (unless the job is a W job) the first poll of
+      // the query's Top-K flag
+      const int len = b.ctx_len[bi];
+      const int64_t o_raw = (kPaged && b.raw_table) ? -1 : b.raw_off[bi];
+      const int64_t o_cmp = (kPaged && b.cmp_table) ? -1 : b.cmp_off[bi];
+      const int64_t o_hca = (!b.hca || (kPaged && b.hca_table)) ? -1 : b.hca_off[bi];
+      int flag0 = epoch;
+      if (flags && lane == 0 && !(split && r.list == 0)) flag0 = ld_acquire(ws.topk_ready + q);
+      JobCtx x = job_ctx(c, b, q, len);
       int sid, t;
-      job_stream(x, r, jobs.host_T >= 0 && jobs.split, sid, t);
+      job_stream(x, r, split, sid, t);
       const __nv_bfloat16* pool = static_cast<const __nv_bfloat16*>(
           sid == 0 ? b.raw : (sid == 1 ? b.cmp : b.hca));
       const int64_t stride = sid == 0 ? b.raw_stride : (sid == 1 ? b.cmp_stride : b.hca_stride);
-      const int* tbl = kPaged ? (sid == 0 ? b.raw_table : (sid == 1 ? b.cmp_table : b.hca_table)) : nullptr;
-      const int64_t off = tbl ? -1 : (sid == 0 ? b.raw_off[x.bi] : (sid == 1 ? b.cmp_off[x.bi] : b.hca_off[x.bi]));
+      const int64_t off = sid == 0 ? o_raw : (sid == 1 ? o_cmp : o_hca);
       // this lane's rows: their Top-K indices are loaded together with the
       // count they are checked against
       int jr[kQuadsPerWarp];
@@ -410,7 +426,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
           // this query's Top-K output: lane 0 polls its flag (bounded), then
           // every lane acquires it before reading the output
           bool ok = true;
-          if (lane == 0) {
+          if (lane == 0 && flag0 != epoch) {
             uint32_t ns = 32;
             uint32_t i = 0;
             while (ld_acquire(ws.topk_ready + q) != epoch) {
@@ -453,6 +469,18 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           if ((v >> (8 * k)) & 1u) bits |= 1ull << (4 * rq + k);
+      }
+      // while the buffer's previous job is still being consumed, ask L2 for
+      // this job's rows (lane l of a row: its 128-byte line l, and line 8 by
+      // lane 0), so the copies below hit L2
+      if (m >= 1) {
+#pragma unroll
+        for (int i = 0; i < kQuadsPerWarp; ++i)
+          if (src[i]) {
+            const char* row = reinterpret_cast<const char*>(src[i]);
+            prefetch_l2_line(row + ch * 128);
+            if (ch == 0) prefetch_l2_line(row + 8 * 128);
+          }
       }
       bool ok = true;
       if (lane == 0) {
@@ -848,9 +876,10 @@ __global__ void __launch_bounds__(256, 4)
     Sched sc;
     sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
     sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
+    sc.cq = nullptr;
     sc.T = T;
-    sc.NW = sc.wp[T];
-    sc.NC = sc.cp[T];
+    sc.NW = jobs.host_T >= 0 ? jobs.NW : sc.wp[T];
+    sc.NC = jobs.host_T >= 0 ? jobs.NC : sc.cp[T];
     sc.G = G;
     sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < G) ? jobs.early : G;
     int k = list_segments(sc.wp[q], sc.wp[q + 1], sc.NW, sc.E, 0,
@@ -1038,6 +1067,30 @@ void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, int num_
   jobs->early = (split && topk_blocks > 0 && early >= num_sms / 4) ? early : 0;
 }
 
+namespace {
+// The query holding each tile CTA's first job of each list, from the same
+// split of the lists as Sched (wstart / cstart), for host-built lists.
+void host_cta_queries(JobLists& jobs, int grid) {
+  const int T = jobs.host_T;
+  jobs.NW = jobs.wprefix[T];
+  jobs.NC = jobs.cprefix[T];
+  jobs.cta_first = grid <= kMaxTileCtas && T <= 65536 ? 1 : 0;
+  if (!jobs.cta_first) return;
+  const int E = (jobs.early > 0 && jobs.early < grid) ? jobs.early : grid;
+  for (int list = 0; list < 2; ++list) {
+    const int* p = list == 0 ? jobs.wprefix : jobs.cprefix;
+    const int N = list == 0 ? jobs.NW : jobs.NC;
+    int q = 0;
+    for (int i = 0; i < grid; ++i) {
+      const int lo = list == 0 ? (i >= E ? N : (int)((int64_t)i * N / E)) : (int)((int64_t)i * N / grid);
+      // the largest q with p[q] <= lo (lo only grows with i)
+      while (q + 1 < T && p[q + 1] <= lo) ++q;
+      jobs.cta_q[list][i] = (uint16_t)q;
+    }
+  }
+}
+}  // namespace
+
 // Jobs one query can have at most (sizes the partial-output workspace).
 int max_jobs_per_query(const DevCfg& c) {
   const int kmax = c.K < c.max_vis ? c.K : c.max_vis;
@@ -1077,6 +1130,7 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
   if (jobs.host_T >= 0) {
     const int total = jobs.wprefix[T] + jobs.cprefix[T];
     if (total < grid) grid = total > 0 ? total : 1;
+    host_cta_queries(jobs, grid);
   }
   // the Top-K ready flags stand in for the grid dependency only when this
   // kernel follows the step's own Top-K kernel through a programmatic launch

@@ -166,10 +166,18 @@ struct ItemList {
 // prefix at ws.job_prefix[T + 1 .. 2T + 1]).  `early`: tile CTAs that share
 // the W jobs (0: all of them); the others start when the Top-K kernel's
 // blocks leave their SMs.
+// With host-built lists the launcher also fills each tile CTA's first
+// queries (cta_q[0][i]: the query of CTA i's first W job, cta_q[1][i]: of its
+// first C job) and the list totals, so that a CTA finds its jobs without
+// searching the prefixes (cta_first = 0: no per-CTA entries, search).
+constexpr int kMaxTileCtas = 256;
 struct JobLists {
   int host_T;
   int split;
   int early;
+  int NW, NC;  // list totals (host-built lists)
+  int cta_first;
+  uint16_t cta_q[2][kMaxTileCtas];
   int wprefix[kMaxHostReq + 1];
   int cprefix[kMaxHostReq + 1];
 };

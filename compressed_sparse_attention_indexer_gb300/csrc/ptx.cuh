@@ -24,6 +24,11 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, i
                "r"(src_bytes), "l"(policy)
                : "memory");
 }
+// Asks L2 for the 128-byte line holding p, ahead of a later load; nothing is
+// read back.
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
