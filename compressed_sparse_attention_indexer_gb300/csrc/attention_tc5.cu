@@ -40,6 +40,7 @@
 // one softmax over the union of the streams' rows.
 #include <cudaTypedefs.h>
 #include <stddef.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -162,17 +163,25 @@ struct JobCursor {
 // The split of the two job lists over the tile CTAs.  CTA i takes the W jobs
 // [wstart(i), wstart(i+1)), spread over the first E CTAs (the ones that start
 // while the Top-K kernel still runs), then the C jobs [cstart(i),
-// cstart(i+1)), spread over all G.  Job ids: W jobs 0 .. NW-1, C jobs
-// NW .. NW+NC-1; a segment's partial output sits at the id of its first job.
+// cstart(i+1)), spread over all G by weight (c_list_start).  Job ids: W jobs
+// 0 .. NW-1, C jobs NW .. NW+NC-1; a segment's partial output sits at the id
+// of its first job.
 struct Sched {
   const int* wp;
   const int* cp;
   const uint16_t* cq;  // per-CTA first queries (cta_q of the lists) or null
   int T, NW, NC, G, E;
+  int CE, wa, wb;      // C-list weights (see JobLists)
   __device__ __forceinline__ int wstart(int i) const {
     return i >= E ? NW : (int)((int64_t)i * NW / E);
   }
-  __device__ __forceinline__ int cstart(int i) const { return (int)((int64_t)i * NC / G); }
+  __device__ __forceinline__ int cstart(int i) const { return c_list_start(i, NC, G, CE, wa, wb); }
+  __device__ __forceinline__ void weights(const JobLists& jobs) {
+    const bool w = jobs.host_T >= 0 && jobs.cw_early > 0 && jobs.cw_a > 0 && jobs.cw_b > 0;
+    CE = w ? jobs.cw_early : G;
+    wa = w ? jobs.cw_a : 1;
+    wb = w ? jobs.cw_b : 1;
+  }
 };
 
 // A job of a CTA's sequence: its query, list (0 = W, 1 = C), index within
@@ -337,6 +346,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   sc.NC = jobs.host_T >= 0 ? jobs.NC : sc.cp[T];
   sc.G = gridDim.x;
   sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < (int)gridDim.x) ? jobs.early : (int)gridDim.x;
+  sc.weights(jobs);
   const int J = (sc.wstart(blockIdx.x + 1) - sc.wstart(blockIdx.x)) +
                 (sc.cstart(blockIdx.x + 1) - sc.cstart(blockIdx.x));
   pdl_trigger();
@@ -591,7 +601,9 @@ __global__ void __launch_bounds__(kA5Threads, 1)
           const int g = nk & 1, m = nk >> 1;
           if (kseg == qseg && (m == 0 || tc5::mbar_try_wait(smem_u32(&sm.s_empty[g]), (m - 1) & 1)) &&
               tc5::mbar_try_wait(smem_u32(&sm.full[g]), m & 1)) {
-            // S = Q . R^T over 576 dims (M = 64 heads, N = 64 rows)
+            // S = Q . R^T over 576 dims (M = 64 heads, N = 64 rows).  (Issued
+            // whole: issuing it in pieces with a ready PV between them was
+            // measured slower.)
             tc5::fence_after_sync();
             const uint64_t db = dbuf + ((g * kBuf) >> 4);
             const uint32_t ds = tmem + kTmemS + 64 * g;
@@ -843,6 +855,7 @@ __device__ int list_segments(int a, int b, int n, int g, int base, Start start, 
   if (b <= a || n <= 0) return k;
   int i = (int)((int64_t)a * g / n);
   if (i >= g) i = g - 1;
+  while (i > 0 && start(i) > a) --i;  // the guess assumes an even split
   while (i + 1 < g && start(i + 1) <= a) ++i;
   for (; i < g && k < kMergeMaxJobs; ++i) {
     const int lo = start(i), hi = i + 1 < g ? start(i + 1) : n;
@@ -882,6 +895,7 @@ __global__ void __launch_bounds__(256, 4)
     sc.NC = jobs.host_T >= 0 ? jobs.NC : sc.cp[T];
     sc.G = G;
     sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < G) ? jobs.early : G;
+    sc.weights(jobs);
     int k = list_segments(sc.wp[q], sc.wp[q + 1], sc.NW, sc.E, 0,
                           [&](int i) { return sc.wstart(i); }, seg, 0);
     k = list_segments(sc.cp[q], sc.cp[q + 1], sc.NC, sc.G, sc.NW,
@@ -1030,6 +1044,7 @@ void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, int num_
   jobs->host_T = -1;
   jobs->split = 0;
   jobs->early = 0;
+  jobs->cw_early = jobs->cw_a = jobs->cw_b = 0;
   if (!lens_host || B * S > kMaxHostReq) return;
   // CSA_EARLY_SPLIT=1: the W / C split (see JobLists); by default one list
   static const bool split = [] {
@@ -1065,6 +1080,23 @@ void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, int num_
   // them would be swamped with the W jobs, and then all CTAs share them
   const int early = num_sms - (topk_blocks < num_sms ? topk_blocks : num_sms);
   jobs->early = (split && topk_blocks > 0 && early >= num_sms / 4) ? early : 0;
+  // Without the split, the CTAs that start while the Top-K blocks still
+  // hold their SMs take more of the list: weights 5:4 (measured best of
+  // 1:1, 5:4, 4:3, 3:2, 2:1 on a 64-query long-context step; CSA_TILE_WEIGHT=a:b
+  // sets the early and the late CTAs' weights)
+  static const int2 wt = [] {
+    int2 r = make_int2(5, 4);
+    if (const char* e = getenv("CSA_TILE_WEIGHT")) {
+      int a = 0, b2 = 0;
+      if (sscanf(e, "%d:%d", &a, &b2) == 2 && a > 0 && b2 > 0 && a <= 64 && b2 <= 64) r = make_int2(a, b2);
+    }
+    return r;
+  }();
+  if (!split && topk_blocks > 0 && early > 0 && wt.x != wt.y) {
+    jobs->cw_early = early;
+    jobs->cw_a = wt.x;
+    jobs->cw_b = wt.y;
+  }
 }
 
 namespace {
@@ -1077,12 +1109,15 @@ void host_cta_queries(JobLists& jobs, int grid) {
   jobs.cta_first = grid <= kMaxTileCtas && T <= 65536 ? 1 : 0;
   if (!jobs.cta_first) return;
   const int E = (jobs.early > 0 && jobs.early < grid) ? jobs.early : grid;
+  const bool w = jobs.cw_early > 0 && jobs.cw_a > 0 && jobs.cw_b > 0;
+  const int CE = w ? jobs.cw_early : grid, wa = w ? jobs.cw_a : 1, wb = w ? jobs.cw_b : 1;
   for (int list = 0; list < 2; ++list) {
     const int* p = list == 0 ? jobs.wprefix : jobs.cprefix;
     const int N = list == 0 ? jobs.NW : jobs.NC;
     int q = 0;
     for (int i = 0; i < grid; ++i) {
-      const int lo = list == 0 ? (i >= E ? N : (int)((int64_t)i * N / E)) : (int)((int64_t)i * N / grid);
+      const int lo = list == 0 ? (i >= E ? N : (int)((int64_t)i * N / E))
+                               : c_list_start(i, N, grid, CE, wa, wb);
       // the largest q with p[q] <= lo (lo only grows with i)
       while (q + 1 < T && p[q + 1] <= lo) ++q;
       jobs.cta_q[list][i] = (uint16_t)q;

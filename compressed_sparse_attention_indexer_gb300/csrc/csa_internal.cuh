@@ -170,17 +170,33 @@ struct ItemList {
 // queries (cta_q[0][i]: the query of CTA i's first W job, cta_q[1][i]: of its
 // first C job) and the list totals, so that a CTA finds its jobs without
 // searching the prefixes (cta_first = 0: no per-CTA entries, search).
+//
+// The C list is split over the tile CTAs in proportion to weights: the first
+// cw_early CTAs (the ones that find a free SM when the grid starts) weigh
+// cw_a each, the others (which start when the Top-K blocks leave their SMs)
+// cw_b each; see c_list_start.
 constexpr int kMaxTileCtas = 256;
 struct JobLists {
   int host_T;
   int split;
   int early;
+  int cw_early, cw_a, cw_b;
   int NW, NC;  // list totals (host-built lists)
   int cta_first;
   uint16_t cta_q[2][kMaxTileCtas];
   int wprefix[kMaxHostReq + 1];
   int cprefix[kMaxHostReq + 1];
 };
+
+// First C job of tile CTA i of G: the C list's NC jobs split in proportion to
+// the CTAs' weights (the first E weigh wa each, the rest wb).  With equal
+// weights this is i * NC / G.
+__host__ __device__ __forceinline__ int c_list_start(int i, int NC, int G, int E, int wa, int wb) {
+  if (E > G) E = G;
+  const int64_t ci = i <= E ? (int64_t)i * wa : (int64_t)E * wa + (int64_t)(i - E) * wb;
+  const int64_t cg = (int64_t)E * wa + (int64_t)(G - E) * wb;
+  return (int)((int64_t)NC * ci / cg);
+}
 
 // Device workspace owned by a handle.
 struct Workspace {
