@@ -33,6 +33,7 @@ struct csa_handle {
   csa::JobLists jobs;   // host-built attention job lists of the current call
   int max_jobs = 0;     // attention tiles per query, at most
   int epoch = 0;        // decode steps launched (the Top-K ready flags' value)
+  int seg_epoch = 0;    // tile-kernel launches (the segment ready flags' value)
 };
 
 namespace {
@@ -262,8 +263,9 @@ int run_attention(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, co
         for (int s = 0; s < b->S; ++s)
           selecting += (b->ctx_len_host[i] - b->S + s + 1) / h->cfg.ratio > h->cfg.topk ? 1 : 0;
     csa::host_jobs(h->dc, b->B, b->S, b->ctx_len_host, h->num_sms, selecting, &h->jobs);
+    h->seg_epoch = h->seg_epoch == 0x7fffffff ? 1 : h->seg_epoch + 1;
     const int r = csa::launch_attention_tc5(h->dc, db, h->ws, h->jobs, idx, cnt, out, lse,
-                                            h->num_sms, st, pdl, early, h->epoch);
+                                            h->num_sms, st, pdl, early, h->epoch, h->seg_epoch);
     if (r != -2) return r;
   }
   return csa::launch_attention(h->dc, db, h->ws, idx, cnt, out, lse, h->num_sms, st, pdl);
@@ -453,12 +455,14 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   const size_t o_ready = off; off += al(sizeof(int) * maxT);
   const size_t o_part = off; off += tc ? al(sizeof(__nv_bfloat16) * (size_t)maxT * h->max_jobs * d.H * d.V) : 0;
   const size_t o_plse = off; off += tc ? al(sizeof(float) * (size_t)maxT * h->max_jobs * d.H) : 0;
+  const size_t o_sready = off; off += tc ? al(sizeof(int) * (size_t)maxT * h->max_jobs) : 0;
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws_base, off);
   if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaMalloc(workspace)"); }
   char* base = static_cast<char*>(h->ws_base);
   e = cudaMemset(base + o_status, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(base + o_ready, 0, sizeof(int) * maxT);  // epoch 0: never a step's
+  if (e == cudaSuccess && tc) e = cudaMemset(base + o_sready, 0, sizeof(int) * (size_t)maxT * h->max_jobs);
   if (e != cudaSuccess) { cudaFree(h->ws_base); delete h; return cuda_fail(e, "cudaMemset"); }
   csa::Workspace& w = h->ws;
   w.status = reinterpret_cast<int*>(base + o_status);
@@ -470,6 +474,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   w.topk_ready = reinterpret_cast<int*>(base + o_ready);
   w.part_o = tc ? reinterpret_cast<__nv_bfloat16*>(base + o_part) : nullptr;
   w.part_lse = tc ? reinterpret_cast<float*>(base + o_plse) : nullptr;
+  w.seg_ready = tc ? reinterpret_cast<int*>(base + o_sready) : nullptr;
   w.max_T = maxT;
   w.max_batch = cfg->max_batch;
   w.scores_ld = ld;
@@ -665,6 +670,7 @@ int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* 
   w.topk_ready = nullptr;
   w.part_o = nullptr;
   w.part_lse = nullptr;
+  w.seg_ready = nullptr;
   w.max_T = b->B * b->S;
   w.max_batch = b->B;
   w.scores_ld = h.dc.max_vis > 0 ? h.dc.max_vis : 1;

@@ -317,7 +317,7 @@ template <bool kPaged>
 __global__ void __launch_bounds__(kA5Threads, 1)
     attn_tile_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ JobLists jobs,
                      DevCfg c, DevBatch b, Workspace ws, const int* topk_idx, const int* topk_cnt,
-                     int early, int epoch) {
+                     int early, int epoch, int seg_epoch) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   __shared__ A5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -822,6 +822,14 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         }
         tc5::fence_before_sync();
         tc5::mbar_arrive(smem_u32(&sm.o_empty));
+        // publish the segment to the merge kernel: every softmax thread
+        // fences its partial stores, the four warps meet, one thread stores
+        // this launch's epoch into the segment's flag with release semantics
+        __threadfence();
+        named_barrier_sync(2, 128);
+        if (tid == 0 && !bad)
+          asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ws.seg_ready + slot), "r"(seg_epoch)
+                       : "memory");
         ++seg;
       }
     }
@@ -865,9 +873,14 @@ __device__ int list_segments(int a, int b, int n, int g, int base, Start start, 
   return k;
 }
 
+// flags != 0: launched right after the tile kernel of the same call, which
+// publishes each segment through ws.seg_ready with seg_epoch: a block starts
+// as soon as its query's segments are written, and waits for the tile grid
+// only at its end.
 __global__ void __launch_bounds__(256, 4)
     attn_merge_kernel(const __grid_constant__ JobLists jobs, DevCfg c, DevBatch b, Workspace ws,
-                      int G, __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
+                      int G, __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out,
+                      int flags, int seg_epoch) {
   __shared__ int seg[kMergeMaxJobs + 1];
   __shared__ int nseg_s;
   __shared__ float2 rope[kRopeTable];  // cos, sin of the block's rotary pairs
@@ -903,8 +916,32 @@ __global__ void __launch_bounds__(256, 4)
     nseg_s = k;
   }
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
+  if (flags) {
+    // thread k < nseg polls segment k's flag (bounded); a wait that gives up
+    // reports a timeout and the query is written as zeros
+    pdl_trigger();
+    const int ns = min(nseg_s, kMergeMaxJobs);
+    if (t < ns) {
+      const uint32_t limit = c.wait_polls < 0 ? (1u << 23) : (uint32_t)c.wait_polls;
+      const int* f = ws.seg_ready + seg[t];
+      uint32_t i = 0, nsl = 32;
+      while (ld_acquire(f) != seg_epoch) {
+        if (++i >= limit) {
+          set_status(ws.status, kStatusTimeout);
+          nseg_s = 0;
+          break;
+        }
+        if (i >= 8) {
+          __nanosleep(nsl);
+          nsl = nsl * 2 > 256 ? 256 : nsl * 2;
+        }
+      }
+    }
+    __syncthreads();
+  } else {
+    pdl_wait();
+    pdl_trigger();
+  }
   const int nseg = min(nseg_s, kMergeMaxJobs);
   const int h = t >> 2;
   const int v0 = dg * kMergeDims + 16 * (t & 3);
@@ -921,10 +958,11 @@ __global__ void __launch_bounds__(256, 4)
     for (int kk = 0; kk < kMergeUnroll; ++kk) {
       if (k0 + kk < nseg) {
         const int64_t sb = (int64_t)seg[k0 + kk] * kTcH + h;
+        // L2-coherent loads: with flags the tile kernel may still be running
         const uint4* src = reinterpret_cast<const uint4*>(ws.part_o + sb * kTcV + v0);
-        u[kk][0] = src[0];
-        u[kk][1] = src[1];
-        lk[kk] = ws.part_lse[sb];
+        u[kk][0] = __ldcg(src);
+        u[kk][1] = __ldcg(src + 1);
+        lk[kk] = __ldcg(ws.part_lse + sb);
       } else {
         u[kk][0] = u[kk][1] = make_uint4(0u, 0u, 0u, 0u);
         lk[kk] = -INFINITY;
@@ -971,6 +1009,9 @@ __global__ void __launch_bounds__(256, 4)
   dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
   if (lse_out && dg == 0 && (t & 3) == 0)
     lse_out[(int64_t)q * kTcH + h] = M == -INFINITY ? -INFINITY : (M + log2f(tot)) * 0.6931471805599453f;
+  // with flags nothing above waited for the tile grid: this grid completes
+  // only after it, so that every later kernel of the stream follows it
+  if (flags) pdl_wait();
 }
 
 // W and C job counts of a query (see JobLists), from the bound min(vis, K).
@@ -1139,7 +1180,7 @@ int max_jobs_per_query(const DevCfg& c) {
 int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                          JobLists& jobs, const int* topk_idx, const int* topk_cnt, void* out,
                          float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early,
-                         int epoch) {
+                         int epoch, int seg_epoch) {
   const int T = b.B * b.S;
   if (T == 0) return 0;
   if (!ws.part_o || max_jobs_per_query(c) > kMergeMaxJobs || b.raw_rows > 0x7fffffffLL ||
@@ -1171,11 +1212,13 @@ int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws
   // kernel follows the step's own Top-K kernel through a programmatic launch
   if (launch_kernel(paged ? attn_tile_kernel<true> : attn_tile_kernel<false>, dim3(grid),
                     dim3(kA5Threads), kA5Dyn, st, pdl, qmap, jobs, c, b, ws, topk_idx, topk_cnt,
-                    (pdl && early) ? 1 : 0, epoch) < 0)
+                    (pdl && early) ? 1 : 0, epoch, seg_epoch) < 0)
     return -1;
   ++n;
+  // the segment flags stand in for the tile grid's completion when the merge
+  // follows it through a programmatic launch
   if (launch_kernel(attn_merge_kernel, dim3(T, kTcV / kMergeDims), dim3(256), 0, st, pdl, jobs, c,
-                    b, ws, grid, static_cast<__nv_bfloat16*>(out), lse_out) < 0)
+                    b, ws, grid, static_cast<__nv_bfloat16*>(out), lse_out, pdl ? 1 : 0, seg_epoch) < 0)
     return -1;
   return n + 1;
 }

@@ -207,6 +207,7 @@ struct Workspace {
   int* topk_cnt;      // [max_T]
   int* job_prefix;    // [2 (max_T + 1)] attention job lists (device-built, see JobLists)
   int* topk_ready;    // [max_T] per query: the step epoch whose Top-K output is complete
+  int* seg_ready;     // [max_T * max_jobs] per segment slot: the launch epoch whose partial is complete
   __nv_bfloat16* part_o;  // [max_T * max_jobs, H, V] per-segment normalised attention output
                           // (bf16: the range of fp32, so any row magnitude survives)
   float* part_lse;    // [max_T * max_jobs, H] per-segment log-sum-exp (log2 units)
@@ -343,10 +344,13 @@ int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, co
 // which signals each query through ws.topk_ready with `epoch`: the tile
 // kernel reads the caller's inputs before its grid wait and starts a query's
 // compressed tiles once that query's Top-K output is complete.
+// seg_epoch: this launch's value of the per-segment ready flags (never 0 and
+// never the previous launch's), through which the merge kernel starts a
+// query once every partial of it is written.
 int launch_attention_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                          JobLists& jobs, const int* topk_idx, const int* topk_cnt, void* out,
                          float* lse_out, int num_sms, cudaStream_t st, bool pdl, bool early,
-                         int epoch);
+                         int epoch, int seg_epoch);
 // Builds the job lists on the host when the lengths are known; `topk_blocks`:
 // Top-K blocks of the step that select (their SMs are busy when the tile
 // kernel starts), 0 when no Top-K kernel runs right before.
