@@ -822,14 +822,16 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         }
         tc5::fence_before_sync();
         tc5::mbar_arrive(smem_u32(&sm.o_empty));
-        // publish the segment to the merge kernel: every softmax thread
-        // fences its partial stores, the four warps meet, one thread stores
-        // this launch's epoch into the segment's flag with release semantics
-        __threadfence();
+        // publish the segment to the merge kernel: the four warps meet (the
+        // barrier orders their partial stores before thread 0's gpu-scope
+        // fence), and one thread stores this launch's epoch into the
+        // segment's flag with release semantics
         named_barrier_sync(2, 128);
-        if (tid == 0 && !bad)
+        if (tid == 0 && !bad) {
+          __threadfence();
           asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ws.seg_ready + slot), "r"(seg_epoch)
                        : "memory");
+        }
         ++seg;
       }
     }

@@ -52,14 +52,16 @@ __device__ __forceinline__ uint32_t score_key_fast(float f) {
 
 // Publishes a query's Top-K output to the attention kernel of the same step,
 // which may already be running (it waits for the flag with bounded polls):
-// every thread fences its writes, the block meets, and one thread stores the
-// step's epoch with release semantics.  A no-op without a flag array.
+// the block meets (the barrier orders every thread's output stores before
+// thread 0's gpu-scope fence), and one thread stores the step's epoch with
+// release semantics.  A no-op without a flag array.
 __device__ __forceinline__ void signal_ready(int* ready, int q, int epoch) {
   if (!ready) return;
-  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0)
+  if (threadIdx.x == 0) {
+    __threadfence();
     asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ready + q), "r"(epoch) : "memory");
+  }
 }
 
 // Key i lives at keys[kpad(i)]: one pad word per 16 keys, so the final pass
