@@ -29,6 +29,12 @@ __device__ __forceinline__ void cp_async16_hint(uint32_t dst, const void* src, i
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p) : "memory");
 }
+// Asks L2 for [p, p + bytes) through the bulk-copy (TMA) unit, ahead of a
+// later load; nothing is read back.  p 16-byte aligned, bytes a multiple of
+// 16, the range inside one allocation.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }

@@ -64,6 +64,33 @@ __device__ __forceinline__ void signal_ready(int* ready, int q, int epoch) {
   }
 }
 
+// Block-wide exclusive scan of one int per thread with a single barrier: each
+// warp scans the per-warp sums itself.  `warp_tmp` (>= 32 ints) is written
+// before the barrier and read after it, so consecutive calls alternate two
+// buffers (a call's barrier then separates the reads of one use of a buffer
+// from the writes of its next use).  *total receives the block sum.
+__device__ __forceinline__ int block_exclusive_scan1(int v, int* warp_tmp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tmp[warp] = x;
+  __syncthreads();
+  int t = lane < nwarps ? warp_tmp[lane] : 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, t, o);
+    if (lane >= o) t += y;
+  }
+  const int base = __shfl_sync(0xffffffffu, t, (warp + 31) & 31);  // inclusive sum of warps < warp
+  *total = __shfl_sync(0xffffffffu, t, 31);
+  return (warp > 0 ? base : 0) + x - v;
+}
+
 // Key i lives at keys[kpad(i)]: one pad word per 16 keys, so the final pass
 // (thread t reads keys 16t .. 16t+15) hits 32 different banks.
 __device__ __forceinline__ int kpad(int i) { return i + (i >> 4); }
@@ -273,7 +300,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   __shared__ int hist[kBins];
   __shared__ uint32_t cand_key[kCand];
   __shared__ int cand_idx[kCand];
-  __shared__ int scan_tmp[33];
+  __shared__ int scan_tmp[2][32];  // alternating buffers of block_exclusive_scan1
   __shared__ uint32_t warp_or[32], warp_and[32];
   __shared__ uint32_t s_tkey;
   __shared__ int s_bin, s_above, s_ncand, s_tidx;
@@ -366,6 +393,9 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     warp_or[warp] = aor;
     warp_and[warp] = aand;
   }
+  // the first radix pass's histogram is cleared under the same barrier
+  hist[tid] = 0;
+  hist[tid + kTopkThreads] = 0;
   __syncthreads();
   aor = warp_or[lane];
   aand = warp_and[lane];
@@ -382,13 +412,16 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   uint32_t tkey = 0u;
   int tidx = 0;
   int mode = 0;  // 1: threshold known, 2: rank the candidates, 0: equal keys
+  int sb = 0;    // scan buffer of the last block_exclusive_scan1
   for (bool first_pass = true; start > 0; first_pass = false) {
     const int wbits = start < 11 ? start : 11;
     const int sh = start - wbits;
     const uint32_t mask = (1u << wbits) - 1u;
-    hist[tid] = 0;
-    hist[tid + kTopkThreads] = 0;
-    __syncthreads();
+    if (!first_pass) {
+      hist[tid] = 0;
+      hist[tid + kTopkThreads] = 0;
+      __syncthreads();
+    }
     if (first_pass) {  // every key shares the common prefix
 #pragma unroll
       for (int j = 0; j < kJ; ++j)
@@ -399,26 +432,53 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
         if (((vmask >> j) & 1u) && (k[j] >> start) == prefix) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
     }
     __syncthreads();
-    {  // the digit holding the need-th largest key (counts of higher bins)
-      const int b0 = 2 * tid, b1 = 2 * tid + 1;
-      const int h0 = hist[b0], h1 = hist[b1];
-      const int rv = h0 + h1;
-      int tot;
-      const int ex = block_exclusive_scan(rv, scan_tmp, &tot);
-      const int above_t = tot - ex - rv;  // keys in bins above this thread's pair
-      if (above_t < need && above_t + rv >= need) {
-        if (above_t + h1 >= need) {
-          s_bin = b1;
-          s_above = above_t;
-        } else {
-          s_bin = b0;
-          s_above = above_t + h1;
-        }
+    // the digit holding the need-th largest key, found by every warp alike
+    // after one barrier: warp w's lanes hold bins 64 w .. 64 w + 63 (two
+    // each); the warps' totals go through shared memory, then each warp
+    // finds the warp w* whose bins hold the key (keys in higher warps' bins
+    // fewer than need, with w*'s at least need), and within w* the lane and
+    // the bin, from suffix sums
+    int bin, above;
+    {
+      int wt = hist[2 * tid] + hist[2 * tid + 1];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) wt += __shfl_xor_sync(0xffffffffu, wt, o);
+      int* wsum = scan_tmp[sb ^= 1];
+      if (lane == 0) wsum[warp] = wt;
+      __syncthreads();
+      const int ws = wsum[lane];  // kTopkThreads / 32 == 32 warps
+      int suf = ws;               // keys in the bins of warps >= lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += y;
+      }
+      const int wabove = suf - ws;
+      const uint32_t wb = __ballot_sync(0xffffffffu, wabove < need && suf >= need);
+      const int wstar = wb ? __ffs(wb) - 1 : 0;  // (never 0: need <= the keys left)
+      const int above_w = __shfl_sync(0xffffffffu, wabove, wstar);
+      const int g0 = hist[64 * wstar + 2 * lane], g1 = hist[64 * wstar + 2 * lane + 1];
+      const int r = g0 + g1;
+      int sr = r;  // keys in the pairs of lanes >= lane of warp w*
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, sr, o);
+        if (lane + o < 32) sr += y;
+      }
+      const int above_l = above_w + sr - r;
+      const uint32_t lb = __ballot_sync(0xffffffffu, above_l < need && above_l + r >= need);
+      const int ls = lb ? __ffs(lb) - 1 : 0;
+      const int al = __shfl_sync(0xffffffffu, above_l, ls);
+      const int h1s = __shfl_sync(0xffffffffu, g1, ls);
+      if (al + h1s >= need) {
+        bin = 64 * wstar + 2 * ls + 1;
+        above = al;
+      } else {
+        bin = 64 * wstar + 2 * ls;
+        above = al + h1s;
       }
     }
-    __syncthreads();
-    const int bin = s_bin;
-    need -= s_above;
+    need -= above;
     prefix = (start >= 32 ? 0u : (prefix << wbits)) | (uint32_t)bin;
     start = sh;
     in_bin = hist[bin];
@@ -480,7 +540,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
 #pragma unroll
     for (int j = 0; j < kJ; ++j) eq += (((vmask >> j) & 1u) && k[j] == prefix) ? 1 : 0;
     int tot;
-    const int ex = block_exclusive_scan(eq, scan_tmp, &tot);
+    const int ex = block_exclusive_scan1(eq, scan_tmp[sb ^= 1], &tot);
     if (ex < need && ex + eq >= need) {
       int r = ex;
 #pragma unroll
@@ -502,7 +562,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     smask |= (uint32_t)sel << j;
   }
   int tot;
-  int pos = block_exclusive_scan(__popc(smask), scan_tmp, &tot);
+  int pos = block_exclusive_scan1(__popc(smask), scan_tmp[sb ^= 1], &tot);
 #pragma unroll
   for (int j = 0; j < kJ; ++j)
     if ((smask >> j) & 1u) {
