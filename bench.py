@@ -262,9 +262,9 @@ def src_sha(files):
 # is dropped once any of them changes)
 _C = "compressed_sparse_attention_indexer_gb300/csrc/"
 KERNEL_SOURCES = {
-    "indexer": [_C + "indexer_tc5.cu", _C + "tc5.cuh", _C + "csa_internal.cuh"],
-    "attention": [_C + "attention_tc5.cu", _C + "tc5.cuh", _C + "csa_internal.cuh"],
-    "topk": [_C + "topk.cu", _C + "csa_internal.cuh"],
+    "indexer": [_C + "indexer_tc5.cu", _C + "tc5.cuh", _C + "ptx.cuh", _C + "csa_internal.cuh"],
+    "attention": [_C + "attention_tc5.cu", _C + "tc5.cuh", _C + "ptx.cuh", _C + "csa_internal.cuh"],
+    "topk": [_C + "topk.cu", _C + "ptx.cuh", _C + "csa_internal.cuh"],
     "plan": [_C + "plan.cu", _C + "csa_internal.cuh"],
 }
 
