@@ -11,14 +11,18 @@
 //
 // attn_tile_kernel: persistent, one CTA per SM, warp-specialised.  A job is
 // one 64-row tile of one stream (window, compressed, heavy) of one query; a
-// CTA takes a contiguous range of the job list, and the jobs of one query
-// inside that range form a segment whose output accumulates in TMEM.
+// CTA takes a contiguous range of the job list (the CTAs that start beside
+// the Top-K blocks take more), and the jobs of one query inside that range
+// form a segment whose output accumulates in TMEM.
 //   warps 5-10, two groups of three: group g gathers every other job into
 //            job buffer g with coalesced 16-byte cp.async, rows scattered
 //            over the pools, into nine 128-byte-swizzled 64-dim sub-tiles
 //            (72 KB); each thread fences its copies for the async proxy and
 //            arrives on the buffer's barrier.  Two buffers: one job's rows
-//            land while the previous job is computed;
+//            land while the previous job is computed, and the next job's
+//            rows are asked of L2 while its buffer is still busy.  In a
+//            decode step a query's compressed tiles start once its Top-K
+//            block has published its output (a per-query flag);
 //   warp 4   loads the query's 64 heads x 576 (72 KB, TMA) when the query
 //            changes and issues the tcgen05 MMAs as their inputs become
 //            ready: S[64 heads x 64 rows] = Q . R^T over 576 dims (M = 64,
@@ -26,18 +30,22 @@
 //            O^T[512 dims x 64 heads] += V^T . P^T (M = 128 per 128-dim
 //            chunk, N = 64; V read in place as an MN-major operand, P^T
 //            from the rope sub-tile that QK no longer needs) into TMEM;
-//   warps 0-3 softmax, one thread per head (lanes 0-15: the M = 64 layout
-//            puts head 16w + i in lane 32w + i): scale and mask the job's 64
-//            scores, keep a per-head reference max that moves only when a
-//            tile max exceeds it by 2^8 (then O^T is rescaled in TMEM by all
-//            128 threads), write the head's row of P^T as bf16 and sum the
+//   warps 0-3 softmax, two threads per head (lanes i and i + 16 of warp w:
+//            head 16w + i, which the M = 64 layout puts in TMEM lane
+//            32w + i; rows 0-31 and 32-63): scale and mask the job's scores,
+//            keep a per-head reference max that moves only when a tile max
+//            exceeds it by 2^8 (then O^T is rescaled in TMEM by all 128
+//            threads), write the head's row of P^T as bf16 and sum the
 //            rounded weights.  At a segment's end all four warps read O^T
-//            (thread = dim) and write the normalised partial output (bf16,
-//            heads x dims) and the heads' log-sum-exp to the workspace.
+//            (thread = dim), write the normalised partial output (bf16,
+//            heads x dims) and the heads' log-sum-exp to the workspace, and
+//            publish the segment (a per-segment flag).
 // attn_merge_kernel: per query and 64 output dims, the log-sum-exp merge of
 // the query's segments in job order, inverse RoPE on the last R dims, the
-// bf16 store.  Because the merge is exact, segment softmax + merge equals
-// one softmax over the union of the streams' rows.
+// bf16 store; after a tile kernel launched just before it, a block starts as
+// soon as its query's segments are published.  Because the merge is exact,
+// segment softmax + merge equals one softmax over the union of the streams'
+// rows.
 #include <cudaTypedefs.h>
 #include <stddef.h>
 #include <stdio.h>
