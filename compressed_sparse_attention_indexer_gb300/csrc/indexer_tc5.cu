@@ -283,6 +283,11 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int kc = 0, qc = 0, job = 0;
+      // ring positions and phase parities as wrapping counters: this single
+      // thread's loop bounds the item rate, and a division per ring per item
+      // (runtime ring sizes) measurably slowed it (~1 us per step)
+      int st_i = 0, cb_i = 0, tb_i = 0, q_i = 0;
+      uint32_t st_ph = 0, cb_ph = 0, tb_ph = 0;
       ReqCursor cur;
       cur.init(prefix, b.B, lo);
       for (int it = lo; it < hi && !*abort; ++it) {
@@ -295,23 +300,23 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
           if (qc > 0) tc5::mma_commit(smem_u32(&sm.qempty[(qc - 1) % NQB]));
           const int qb = qc % NQB;
           if (!tc5::mbar_wait(smem_u32(&sm.qfull[qb]), (qc / NQB) & 1, abort)) break;
+          q_i = qb;
           ++qc;
         }
-        const int st = kc % NST;
-        const int cb = kc % NCB;
+        const int st = st_i, cb = cb_i;
         if (kFp8) {
-          if (!tc5::mbar_wait(smem_u32(&sm.cfull[cb]), (kc / NCB) & 1, abort)) break;
+          if (!tc5::mbar_wait(smem_u32(&sm.cfull[cb]), cb_ph, abort)) break;
         } else {
-          if (!tc5::mbar_wait(smem_u32(&sm.full[st]), (kc / NST) & 1, abort)) break;
+          if (!tc5::mbar_wait(smem_u32(&sm.full[st]), st_ph, abort)) break;
         }
         tc5::fence_after_sync();
         const uint32_t ka = kFp8 ? cbuf + cb * kStageBytes : kbuf + st * kStageBytes;
-        const uint32_t qa = qbuf + ((qc - 1) % NQB) * qbytes;
+        const uint32_t qa = qbuf + q_i * qbytes;
         bool ok = true;
         for (int g = 0; g < u.ngroups; ++g) {
           const int gn = min(G, u.su - g * G);
-          const int tb = job % NB;
-          if (job >= NB && !tc5::mbar_wait(smem_u32(&sm.tempty[tb]), ((job / NB) - 1) & 1, abort)) {
+          const int tb = tb_i;
+          if (job >= NB && !tc5::mbar_wait(smem_u32(&sm.tempty[tb]), tb_ph ^ 1u, abort)) {
             ok = false;
             break;
           }
@@ -327,10 +332,13 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
           }
           tc5::mma_commit(smem_u32(&sm.tfull[tb]));
           ++job;
+          if (++tb_i == NB) { tb_i = 0; tb_ph ^= 1u; }
         }
         if (!ok) break;
         tc5::mma_commit(smem_u32(kFp8 ? &sm.cempty[cb] : &sm.empty[st]));
         ++kc;
+        if (++st_i == NST) { st_i = 0; st_ph ^= 1u; }
+        if (kFp8 && ++cb_i == NCB) { cb_i = 0; cb_ph ^= 1u; }
       }
       // every MMA issued above has finished before TMEM is freed
       tc5::mma_commit(smem_u32(&sm.done));
