@@ -446,7 +446,8 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
       int* wsum = scan_tmp[sb ^= 1];
       if (lane == 0) wsum[warp] = wt;
       __syncthreads();
-      const int ws = wsum[lane];  // kTopkThreads / 32 == 32 warps
+      static_assert(kTopkThreads == 32 * 32, "one warp total per lane: 32 warps of 64 bins");
+      const int ws = wsum[lane];
       int suf = ws;               // keys in the bins of warps >= lane
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
