@@ -859,26 +859,48 @@ __global__ void __launch_bounds__(kA5Threads, 1)
 // Per (query, 64 output dims): LSE merge of the query's segment partials,
 // inverse RoPE on the last R dims, bf16 store.  The segments are the query's
 // W jobs cut at the tile CTAs' W ranges, then its C jobs cut at their C
-// ranges (see Sched); one thread lists them.  Thread t owns head t >> 2 and
-// 16 consecutive dims (t & 3) of the block's 64: it loads its head's LSE and
-// a 32-byte piece of the partials, two segments per batch, derives the
-// weights itself (running max across batches), and stores 32 bytes.
+// ranges (see Sched); the block lists them, thread i testing CTA i.  Thread
+// t owns head t >> 2 and 16 consecutive dims (t & 3) of the block's 64: it
+// loads its head's LSE and a 32-byte piece of the partials, two segments per
+// batch, derives the weights itself (running max across batches), and stores
+// 32 bytes.  (Four per batch need 80 registers, so three blocks per SM, and
+// the last blocks then start only after the tile grid: measured slower.)
 constexpr int kMergeUnroll = 2;  // partials whose loads are in flight together
 
 // Appends to seg[] the partial slots of the CTA ranges that intersect the
 // jobs [a, b) of one list of n jobs split at start(i), i < g (id offset
-// `base`); returns the new count.
+// `base`), in CTA order; returns the new count.  Every thread of the block
+// calls it: thread t tests CTAs t, t + blockDim.x, ..., and a ballot per warp
+// plus the warps' counts place the pieces in order (a serial walk by one
+// thread costs microseconds of dependent divisions at the end of the step).
+// `wcnt` holds one int per warp.
 template <typename Start>
-__device__ int list_segments(int a, int b, int n, int g, int base, Start start, int* seg, int k) {
+__device__ int list_segments(int a, int b, int n, int g, int base, Start start, int* seg, int k,
+                             int* wcnt) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
   if (b <= a || n <= 0) return k;
-  int i = (int)((int64_t)a * g / n);
-  if (i >= g) i = g - 1;
-  while (i > 0 && start(i) > a) --i;  // the guess assumes an even split
-  while (i + 1 < g && start(i + 1) <= a) ++i;
-  for (; i < g && k < kMergeMaxJobs; ++i) {
-    const int lo = start(i), hi = i + 1 < g ? start(i + 1) : n;
-    if (lo >= b) break;
-    if (hi > lo && hi > a) seg[k++] = base + (lo > a ? lo : a);
+  for (int i0 = 0; i0 < g; i0 += blockDim.x) {
+    const int i = i0 + t;
+    bool in = false;
+    int slot = 0;
+    if (i < g) {
+      const int lo = start(i), hi = i + 1 < g ? start(i + 1) : n;
+      in = hi > lo && hi > a && lo < b;
+      slot = base + (lo > a ? lo : a);
+    }
+    const uint32_t bal = __ballot_sync(0xffffffffu, in);
+    if (lane == 0) wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int cw = wcnt[w];
+      before += w < warp ? cw : 0;
+      tot += cw;
+    }
+    const int pos = k + before + __popc(bal & ((1u << lane) - 1u));
+    if (in && pos < kMergeMaxJobs) seg[pos] = slot;
+    k += tot;
+    __syncthreads();  // wcnt is rewritten by the next chunk
   }
   return k;
 }
@@ -893,13 +915,16 @@ __global__ void __launch_bounds__(256, 4)
                       int flags, int seg_epoch) {
   __shared__ int seg[kMergeMaxJobs + 1];
   __shared__ int nseg_s;
+  __shared__ int wcnt[256 / 32];  // per-warp piece counts of list_segments (256 threads)
   __shared__ float2 rope[kRopeTable];  // cos, sin of the block's rotary pairs
   // The segment list and the rotary table need only the job lists and the
   // lengths, which are complete before the tile kernel lets this grid
   // launch (the tile kernel waits for the job-list kernel before it
   // triggers, and for the caller's inputs before it or its predecessor
   // does); only the partials wait for the tile grid.
-  const int q = blockIdx.x, dg = blockIdx.y, t = threadIdx.x;
+  // the blocks of the last dims (the rotary ones, whose table takes longest
+  // to set up) are dispatched first
+  const int q = blockIdx.x, dg = gridDim.y - 1 - blockIdx.y, t = threadIdx.x;
   const int T = b.B * b.S;
   const int rope0 = kTcV - c.R;  // first rotary dim
   if (dg * kMergeDims + kMergeDims > rope0 && t >= 64 && t < 64 + c.R / 2 && t - 64 < kRopeTable) {
@@ -908,7 +933,7 @@ __global__ void __launch_bounds__(256, 4)
     const int i = t - 64;
     rope[i] = (p.flags & kPlanBad) ? make_float2(1.f, 0.f) : rope_cos_sin((double)p.pos, c.rope_theta[i]);
   }
-  if (t == 0) {
+  {
     Sched sc;
     sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
     sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
@@ -919,11 +944,11 @@ __global__ void __launch_bounds__(256, 4)
     sc.G = G;
     sc.E = (jobs.host_T >= 0 && jobs.early > 0 && jobs.early < G) ? jobs.early : G;
     sc.weights(jobs);
-    int k = list_segments(sc.wp[q], sc.wp[q + 1], sc.NW, sc.E, 0,
-                          [&](int i) { return sc.wstart(i); }, seg, 0);
-    k = list_segments(sc.cp[q], sc.cp[q + 1], sc.NC, sc.G, sc.NW,
-                      [&](int i) { return sc.cstart(i); }, seg, k);
-    nseg_s = k;
+    // the query's job ranges, loaded together before the first barrier
+    const int wa = sc.wp[q], wb = sc.wp[q + 1], ca = sc.cp[q], cb = sc.cp[q + 1];
+    int k = list_segments(wa, wb, sc.NW, sc.E, 0, [&](int i) { return sc.wstart(i); }, seg, 0, wcnt);
+    k = list_segments(ca, cb, sc.NC, sc.G, sc.NW, [&](int i) { return sc.cstart(i); }, seg, k, wcnt);
+    if (t == 0) nseg_s = k;
   }
   __syncthreads();
   if (flags) {
