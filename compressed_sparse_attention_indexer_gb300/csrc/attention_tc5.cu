@@ -143,8 +143,9 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 struct JobCursor {
   const int* prefix;
   int q, first, end;
-  // q0 >= 0: the query holding `job`, known already; else found by search
-  __device__ __forceinline__ void init(const int* p, int T, int job, int q0) {
+  // q0 >= 0: the query holding `job`, known already (span: its job range
+  // [p[q0], p[q0 + 1]), if known too); else found by search
+  __device__ __forceinline__ void init(const int* p, int T, int job, int q0, const int* span) {
     prefix = p;
     int l = q0;
     if (l < 0) {
@@ -156,8 +157,8 @@ struct JobCursor {
       }
     }
     q = l;
-    first = p[l];
-    end = p[l + 1];
+    first = span ? span[0] : p[l];
+    end = span ? span[1] : p[l + 1];
   }
   __device__ __forceinline__ void advance(int job) {
     while (job >= end) {
@@ -178,6 +179,7 @@ struct Sched {
   const int* wp;
   const int* cp;
   const uint16_t* cq;  // per-CTA first queries (cta_q of the lists) or null
+  const int* cspan;    // their job ranges (cta_span of the lists), with cq
   int T, NW, NC, G, E;
   int CE, wa, wb;      // C-list weights (see JobLists)
   __device__ __forceinline__ int wstart(int i) const {
@@ -210,8 +212,11 @@ struct JobWalk {
     clo = s.cstart(cta);
     nc = s.cstart(cta + 1) - clo;
     NW = s.NW;
-    if (nw > 0) wc.init(s.wp, s.T, wlo, s.cq ? (int)s.cq[cta] : -1);
-    if (nc > 0) cc.init(s.cp, s.T, clo, s.cq ? (int)s.cq[kMaxTileCtas + cta] : -1);
+    if (nw > 0)
+      wc.init(s.wp, s.T, wlo, s.cq ? (int)s.cq[cta] : -1, s.cq ? s.cspan + 2 * cta : nullptr);
+    if (nc > 0)
+      cc.init(s.cp, s.T, clo, s.cq ? (int)s.cq[kMaxTileCtas + cta] : -1,
+              s.cq ? s.cspan + 2 * (kMaxTileCtas + cta) : nullptr);
   }
   __device__ __forceinline__ JobRef get(int n) {
     JobRef r;
@@ -349,6 +354,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
   sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
   sc.cq = jobs.host_T >= 0 && jobs.cta_first ? &jobs.cta_q[0][0] : nullptr;
+  sc.cspan = &jobs.cta_span[0][0][0];
   sc.T = T;
   sc.NW = jobs.host_T >= 0 ? jobs.NW : sc.wp[T];
   sc.NC = jobs.host_T >= 0 ? jobs.NC : sc.cp[T];
@@ -365,6 +371,12 @@ __global__ void __launch_bounds__(kA5Threads, 1)
   volatile int* abort = &sm.abort;
   // polls before a consumer wait gives up (the default: about a second)
   const uint32_t wpolls = c.wait_polls < 0 ? tc5::kBackoffPolls : (uint32_t)c.wait_polls;
+
+  // every role walks the CTA's jobs from the same start; its first query and
+  // job range (host lists: kernel parameters of this CTA) load alongside the
+  // set-up below
+  JobWalk walk0;
+  walk0.init(sc, blockIdx.x);
 
   if (warp == 4) {
     tc5::tmem_alloc(smem_u32(&sm.tmem_base), 512);
@@ -409,8 +421,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     const __nv_bfloat16* null_src = static_cast<const __nv_bfloat16*>(b.q);
     const int ch = lane & 7;
     const uint64_t rpol = tc5::policy_evict_first();  // rows are read once per step
-    JobWalk walk;
-    walk.init(sc, blockIdx.x);
+    JobWalk walk = walk0;
     int m = 0;
     bool waited = !flags;
     for (int n = g; n < J; n += 2, ++m) {
@@ -546,9 +557,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       const uint64_t dq = tc5::sdesc_k_sw128(qres);
       const uint64_t dbuf = tc5::sdesc_k_sw128(bufs);
       const uint64_t dv = sdesc_mn_sw128(bufs, kSub);
-      JobWalk qw, pw;  // the next QK job and the next PV job
-      qw.init(sc, blockIdx.x);
-      pw.init(sc, blockIdx.x);
+      JobWalk qw = walk0, pw = walk0;  // the next QK job and the next PV job
       int nk = 0, np = 0;  // CTA-local index of the next job to QK / to PV
       int nq = 0, nqd = 0, seg = 0;
       int qseg = -1;       // first job of the segment whose Q is resident (or loading)
@@ -657,8 +666,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
     const uint32_t lanes = (uint32_t)(warp * 32) << 16;
     const float sc2 = c.scale * kLog2e;
     float mref = -INFINITY, lrun = 0.f;
-    JobWalk walk;
-    walk.init(sc, blockIdx.x);
+    JobWalk walk = walk0;
     int seg = 0, slot = 0;
     bool bad = false;  // a wait of this thread gave up
     for (int n = 0; n < J; ++n) {
@@ -938,6 +946,7 @@ __global__ void __launch_bounds__(256, 4)
     sc.wp = jobs.host_T >= 0 ? jobs.wprefix : ws.job_prefix;
     sc.cp = jobs.host_T >= 0 ? jobs.cprefix : ws.job_prefix + (T + 1);
     sc.cq = nullptr;
+    sc.cspan = nullptr;
     sc.T = T;
     sc.NW = jobs.host_T >= 0 ? jobs.NW : sc.wp[T];
     sc.NC = jobs.host_T >= 0 ? jobs.NC : sc.cp[T];
@@ -1197,6 +1206,8 @@ void host_cta_queries(JobLists& jobs, int grid) {
       // the largest q with p[q] <= lo (lo only grows with i)
       while (q + 1 < T && p[q + 1] <= lo) ++q;
       jobs.cta_q[list][i] = (uint16_t)q;
+      jobs.cta_span[list][i][0] = p[q];
+      jobs.cta_span[list][i][1] = p[q + 1];
     }
   }
 }

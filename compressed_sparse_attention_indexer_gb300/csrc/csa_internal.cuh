@@ -184,6 +184,7 @@ struct JobLists {
   int NW, NC;  // list totals (host-built lists)
   int cta_first;
   uint16_t cta_q[2][kMaxTileCtas];
+  int cta_span[2][kMaxTileCtas][2];  // the job range [first, end) of query cta_q[list][i]
   int wprefix[kMaxHostReq + 1];
   int cprefix[kMaxHostReq + 1];
 };
