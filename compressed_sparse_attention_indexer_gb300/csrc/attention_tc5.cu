@@ -452,8 +452,9 @@ __global__ void __launch_bounds__(kA5Threads, 1)
       for (int i = 0; i < kQuadsPerWarp; ++i) jr[i] = -1;
       if (sid == 1) {
         if (flags) {
-          // this query's Top-K output: lane 0 polls its flag (bounded), then
-          // every lane acquires it before reading the output
+          // this query's Top-K output: lane 0 acquires its flag (the first
+          // poll above, then bounded polls), and the warp barrier below
+          // orders that before every lane's reads of the output
           bool ok = true;
           if (lane == 0 && flag0 != epoch) {
             uint32_t ns = 32;
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(kA5Threads, 1)
             }
           }
           if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-          (void)ld_acquire(ws.topk_ready + q);
+          __syncwarp();
         } else if (!waited) {
           pdl_wait();
           waited = true;
@@ -839,12 +840,12 @@ __global__ void __launch_bounds__(kA5Threads, 1)
         tc5::fence_before_sync();
         tc5::mbar_arrive(smem_u32(&sm.o_empty));
         // publish the segment to the merge kernel: the four warps meet (the
-        // barrier orders their partial stores before thread 0's gpu-scope
-        // fence), and one thread stores this launch's epoch into the
-        // segment's flag with release semantics
+        // barrier orders their partial stores before thread 0's release, which
+        // is cumulative over what the barrier ordered before it), and one
+        // thread stores this launch's epoch into the segment's flag with
+        // release semantics
         named_barrier_sync(2, 128);
         if (tid == 0 && !bad) {
-          __threadfence();
           asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ws.seg_ready + slot), "r"(seg_epoch)
                        : "memory");
         }

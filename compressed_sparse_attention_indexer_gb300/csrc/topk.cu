@@ -53,13 +53,13 @@ __device__ __forceinline__ uint32_t score_key_fast(float f) {
 // Publishes a query's Top-K output to the attention kernel of the same step,
 // which may already be running (it waits for the flag with bounded polls):
 // the block meets (the barrier orders every thread's output stores before
-// thread 0's gpu-scope fence), and one thread stores the step's epoch with
-// release semantics.  A no-op without a flag array.
+// thread 0's release, which is cumulative over what the barrier ordered
+// before it), and one thread stores the step's epoch with release semantics.
+// A no-op without a flag array.
 __device__ __forceinline__ void signal_ready(int* ready, int q, int epoch) {
   if (!ready) return;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
     asm volatile("st.release.gpu.global.b32 [%0], %1;\n" ::"l"(ready + q), "r"(epoch) : "memory");
   }
 }
