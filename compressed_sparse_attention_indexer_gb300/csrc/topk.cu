@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   __shared__ int scan_tmp[2][32];  // alternating buffers of block_exclusive_scan1
   __shared__ uint32_t warp_or[32], warp_and[32];
   __shared__ uint32_t s_tkey;
-  __shared__ int s_bin, s_above, s_ncand, s_tidx;
+  __shared__ int s_ncand, s_tidx;
 
   const int K = c.K;
   const int q = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
       mode = 2;
       break;
     }
-    __syncthreads();  // hist and s_bin are rewritten by the next pass
+    __syncthreads();  // hist is cleared and rewritten by the next pass
   }
   if (mode == 0 && in_bin <= kCand) mode = 2;
 
