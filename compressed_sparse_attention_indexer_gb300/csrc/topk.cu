@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
                     int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
                     int early, int* ready, int epoch) {
   static_assert(kJ == 2 || kJ % 4 == 0, "keys are loaded as float2 or float4 vectors");
+  constexpr uint32_t kFull = (1u << kJ) - 1u;  // every key of the thread exists
   __shared__ int hist[kBins];
   __shared__ uint32_t cand_key[kCand];
   __shared__ int cand_idx[kCand];
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   {
     float v[kJ];
     const bool vec = ((reinterpret_cast<uintptr_t>(sc) & (kJ == 2 ? 7u : 15u)) == 0) && i0 + kJ <= n;
-    if (vec) {
+    if (vec) {  // every key of this thread exists: no per-key checks
       if (kJ == 2) {
         const float2 x = ld_once2(sc + i0);
         v[0] = x.x;
@@ -370,17 +371,24 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
           v[j + 3] = x.w;
         }
       }
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        k[j] = score_key_fast(v[j]);
+        aor |= k[j];
+        aand &= k[j];
+      }
+      vmask = kFull;
     } else {
 #pragma unroll
       for (int j = 0; j < kJ; ++j) v[j] = i0 + j < n ? ld_once(sc + i0 + j) : 0.f;
-    }
 #pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      k[j] = score_key_fast(v[j]);
-      if (i0 + j < n) {
-        vmask |= 1u << j;
-        aor |= k[j];
-        aand &= k[j];
+      for (int j = 0; j < kJ; ++j) {
+        k[j] = score_key_fast(v[j]);
+        if (i0 + j < n) {
+          vmask |= 1u << j;
+          aor |= k[j];
+          aand &= k[j];
+        }
       }
     }
   }
@@ -423,9 +431,14 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
       __syncthreads();
     }
     if (first_pass) {  // every key shares the common prefix
+      if (vmask == kFull) {
 #pragma unroll
-      for (int j = 0; j < kJ; ++j)
-        if ((vmask >> j) & 1u) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+        for (int j = 0; j < kJ; ++j) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+      } else if (vmask) {
+#pragma unroll
+        for (int j = 0; j < kJ; ++j)
+          if ((vmask >> j) & 1u) atomicAdd(&hist[(k[j] >> sh) & mask], 1);
+      }
     } else {  // start < 32 after a pass
 #pragma unroll
       for (int j = 0; j < kJ; ++j)
@@ -502,19 +515,22 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     // slots), then rank each among them
     uint32_t m = 0u;
 #pragma unroll
-    for (int j = 0; j < kJ; ++j)
-      if (((vmask >> j) & 1u) && (k[j] >> start) == prefix) m |= 1u << j;  // start < 32 here
+    for (int j = 0; j < kJ; ++j) m |= (uint32_t)((k[j] >> start) == prefix) << j;  // start < 32 here
+    m &= vmask;
     if (m) {
       int slot = atomicAdd(&s_ncand, __popc(m));
+      // the set bits only (a thread has few candidates); k[] stays in
+      // registers: the key is picked by a fixed-index select
+      for (uint32_t mm = m; mm; mm &= mm - 1u, ++slot) {
+        const int j = __ffs(mm) - 1;
+        uint32_t kj = 0u;
 #pragma unroll
-      for (int j = 0; j < kJ; ++j)
-        if ((m >> j) & 1u) {
-          if (slot < kCand) {
-            cand_key[slot] = k[j];
-            cand_idx[slot] = i0 + j;
-          }
-          ++slot;
+        for (int jj = 0; jj < kJ; ++jj) kj = jj == j ? k[jj] : kj;
+        if (slot < kCand) {
+          cand_key[slot] = kj;
+          cand_idx[slot] = i0 + j;
         }
+      }
     }
     __syncthreads();
     if (tid < in_bin) {
@@ -558,18 +574,14 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   uint32_t smask = 0u;
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
-    const int i = i0 + j;
-    const bool sel = ((vmask >> j) & 1u) && (k[j] > tkey || (k[j] == tkey && i <= tidx));
+    const bool sel = k[j] > tkey || (k[j] == tkey && i0 + j <= tidx);
     smask |= (uint32_t)sel << j;
   }
+  smask &= vmask;  // keys past the row are never kept
   int tot;
   int pos = block_exclusive_scan1(__popc(smask), scan_tmp[sb ^= 1], &tot);
-#pragma unroll
-  for (int j = 0; j < kJ; ++j)
-    if ((smask >> j) & 1u) {
-      if (pos < K) out[pos] = i0 + j;
-      ++pos;
-    }
+  for (uint32_t mm = smask; mm; mm &= mm - 1u, ++pos)  // the set bits only
+    if (pos < K) out[pos] = i0 + __ffs(mm) - 1;
   if (tid == 0) cnt_out[q] = K;
   signal_ready(ready, q, epoch);
 }
