@@ -187,7 +187,7 @@ struct Sched {
   }
   __device__ __forceinline__ int cstart(int i) const { return c_list_start(i, NC, G, CE, wa, wb); }
   __device__ __forceinline__ void weights(const JobLists& jobs) {
-    const bool w = jobs.host_T >= 0 && jobs.cw_early > 0 && jobs.cw_a > 0 && jobs.cw_b > 0;
+    const bool w = jobs.host_T >= 0 && jobs.cw_early > 0 && (jobs.cw_a == 0 || (jobs.cw_a > 0 && jobs.cw_b > 0));
     CE = w ? jobs.cw_early : G;
     wa = w ? jobs.cw_a : 1;
     wb = w ? jobs.cw_b : 1;
@@ -1167,18 +1167,21 @@ void host_jobs(const DevCfg& c, int B, int S, const int32_t* lens_host, int num_
   const int early = num_sms - (topk_blocks < num_sms ? topk_blocks : num_sms);
   jobs->early = (split && topk_blocks > 0 && early >= num_sms / 4) ? early : 0;
   // Without the split, the CTAs that start while the Top-K blocks still
-  // hold their SMs take more of the list: weights 5:4 (measured best of
-  // 1:1, 5:4, 4:3, 3:2, 2:1 on a 64-query long-context step; CSA_TILE_WEIGHT=a:b
-  // sets the early and the late CTAs' weights)
+  // hold their SMs take more of the list: an even split whose left-over jobs
+  // go to them first (cw_a = 0).  A late CTA's start (its SM freed, the
+  // CTA's set-up, the first rows) costs about a job's time, so it gets no
+  // more than the average; measured on a 64-query long-context step against
+  // weight ratios from 2:1 to 1:1 (5:4 was 1 us slower, 12:11, which gives
+  // the same split there, as fast).  CSA_TILE_WEIGHT=a:b sets weights instead.
   static const int2 wt = [] {
-    int2 r = make_int2(5, 4);
+    int2 r = make_int2(0, 0);
     if (const char* e = getenv("CSA_TILE_WEIGHT")) {
       int a = 0, b2 = 0;
       if (sscanf(e, "%d:%d", &a, &b2) == 2 && a > 0 && b2 > 0 && a <= 64 && b2 <= 64) r = make_int2(a, b2);
     }
     return r;
   }();
-  if (!split && topk_blocks > 0 && early > 0 && wt.x != wt.y) {
+  if (!split && topk_blocks > 0 && early > 0 && (wt.x == 0 || wt.x != wt.y)) {
     jobs->cw_early = early;
     jobs->cw_a = wt.x;
     jobs->cw_b = wt.y;
@@ -1195,7 +1198,7 @@ void host_cta_queries(JobLists& jobs, int grid) {
   jobs.cta_first = grid <= kMaxTileCtas && T <= 65536 ? 1 : 0;
   if (!jobs.cta_first) return;
   const int E = (jobs.early > 0 && jobs.early < grid) ? jobs.early : grid;
-  const bool w = jobs.cw_early > 0 && jobs.cw_a > 0 && jobs.cw_b > 0;
+  const bool w = jobs.cw_early > 0 && (jobs.cw_a == 0 || (jobs.cw_a > 0 && jobs.cw_b > 0));
   const int CE = w ? jobs.cw_early : grid, wa = w ? jobs.cw_a : 1, wb = w ? jobs.cw_b : 1;
   for (int list = 0; list < 2; ++list) {
     const int* p = list == 0 ? jobs.wprefix : jobs.cprefix;

@@ -171,10 +171,12 @@ struct ItemList {
 // first C job) and the list totals, so that a CTA finds its jobs without
 // searching the prefixes (cta_first = 0: no per-CTA entries, search).
 //
-// The C list is split over the tile CTAs in proportion to weights: the first
-// cw_early CTAs (the ones that find a free SM when the grid starts) weigh
-// cw_a each, the others (which start when the Top-K blocks leave their SMs)
-// cw_b each; see c_list_start.
+// The C list is split over the tile CTAs unevenly when the first cw_early
+// CTAs (the ones that find a free SM when the grid starts) start well before
+// the others (which start when the Top-K blocks leave their SMs): with
+// cw_a = 0 the jobs an even split leaves over go to the early CTAs first;
+// with cw_a > 0 the split is in proportion to weights, cw_a for each early
+// and cw_b for each late CTA; see c_list_start.
 constexpr int kMaxTileCtas = 256;
 struct JobLists {
   int host_T;
@@ -189,11 +191,20 @@ struct JobLists {
   int cprefix[kMaxHostReq + 1];
 };
 
-// First C job of tile CTA i of G: the C list's NC jobs split in proportion to
-// the CTAs' weights (the first E weigh wa each, the rest wb).  With equal
-// weights this is i * NC / G.
+// First C job of tile CTA i of G.  wa > 0: the C list's NC jobs split in
+// proportion to the CTAs' weights (the first E weigh wa each, the rest wb);
+// with equal weights this is i * NC / G.  wa == 0: every CTA takes NC / G
+// jobs, and the NC % G left over go one each to the first E CTAs, then to
+// the CTAs after them.
 __host__ __device__ __forceinline__ int c_list_start(int i, int NC, int G, int E, int wa, int wb) {
   if (E > G) E = G;
+  if (wa == 0) {
+    const int per = NC / G, r = NC - per * G;
+    const int r1 = r < E ? r : E;  // the early CTAs' extra jobs
+    if (i <= E) return i * per + (i < r1 ? i : r1);
+    const int r2 = r - r1, j = i - E;
+    return i * per + r1 + (j < r2 ? j : r2);
+  }
   const int64_t ci = i <= E ? (int64_t)i * wa : (int64_t)E * wa + (int64_t)(i - E) * wb;
   const int64_t cg = (int64_t)E * wa + (int64_t)(G - E) * wb;
   return (int)((int64_t)NC * ci / cg);
