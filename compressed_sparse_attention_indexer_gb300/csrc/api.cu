@@ -34,6 +34,7 @@ struct csa_handle {
   int max_jobs = 0;     // attention tiles per query, at most
   int epoch = 0;        // decode steps launched (the Top-K ready flags' value)
   int seg_epoch = 0;    // tile-kernel launches (the segment ready flags' value)
+  int done_set = 0;     // the indexer completion-counter set (ws.idx_done) the next publishing launch uses
 };
 
 namespace {
@@ -293,9 +294,12 @@ int finish(csa_handle* h, const Launches& L) {
   return CSA_OK;
 }
 
-// plan (if needed) + indexer into `scores`
+// plan (if needed) + indexer into `scores`.  done (not NULL): the tcgen05
+// indexer publishes each request's scored items to the handle's current
+// counter set and zeroes the other one; *done then points at the set it used
+// (NULL if no kernel published), and the next publishing launch uses the other.
 void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int score_all,
-                 float* scores, int64_t ld, cudaStream_t st, Launches& L) {
+                 float* scores, int64_t ld, cudaStream_t st, Launches& L, int** done = nullptr) {
   csa::ItemList& items = h->items;
   host_items(h, b, score_all, &items);
   const bool pdl = use_pdl();
@@ -305,9 +309,19 @@ void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int
                    return csa::launch_prep(h->dc, db, h->ws, score_all,
                                            csa::indexer_qsplit(h->dc, b->S), st, pdl);
                  }));
+  int* cur = nullptr;
+  int* other = nullptr;
+  if (done && h->ws.idx_done) {
+    cur = h->ws.idx_done + (size_t)h->done_set * h->ws.max_batch;
+    other = h->ws.idx_done + (size_t)(h->done_set ^ 1) * h->ws.max_batch;
+  }
+  bool published = false;
   L.add(staged(h, kStageIndexer, st, [&] {
-    return csa::launch_indexer(h->dc, db, h->ws, items, score_all, scores, ld, h->num_sms, st, pdl);
+    return csa::launch_indexer(h->dc, db, h->ws, items, score_all, scores, ld, h->num_sms, st, pdl,
+                               cur, other, &published);
   }));
+  if (done) *done = published ? cur : nullptr;
+  if (published) h->done_set ^= 1;
 }
 
 // ---- allocation-free variant of indexer + Top-K ----------------------------
@@ -456,6 +470,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   const size_t o_part = off; off += tc ? al(sizeof(__nv_bfloat16) * (size_t)maxT * h->max_jobs * d.H * d.V) : 0;
   const size_t o_plse = off; off += tc ? al(sizeof(float) * (size_t)maxT * h->max_jobs * d.H) : 0;
   const size_t o_sready = off; off += tc ? al(sizeof(int) * (size_t)maxT * h->max_jobs) : 0;
+  const size_t o_done = off; off += al(sizeof(int) * 2 * (size_t)cfg->max_batch);
   h->ws_bytes = off;
   e = cudaMalloc(&h->ws_base, off);
   if (e != cudaSuccess) { delete h; return cuda_fail(e, "cudaMalloc(workspace)"); }
@@ -463,6 +478,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   e = cudaMemset(base + o_status, 0, sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(base + o_ready, 0, sizeof(int) * maxT);  // epoch 0: never a step's
   if (e == cudaSuccess && tc) e = cudaMemset(base + o_sready, 0, sizeof(int) * (size_t)maxT * h->max_jobs);
+  if (e == cudaSuccess) e = cudaMemset(base + o_done, 0, sizeof(int) * 2 * (size_t)cfg->max_batch);
   if (e != cudaSuccess) { cudaFree(h->ws_base); delete h; return cuda_fail(e, "cudaMemset"); }
   csa::Workspace& w = h->ws;
   w.status = reinterpret_cast<int*>(base + o_status);
@@ -475,6 +491,7 @@ int csa_decode_create(const csa_config* cfg, csa_handle** out) {
   w.part_o = tc ? reinterpret_cast<__nv_bfloat16*>(base + o_part) : nullptr;
   w.part_lse = tc ? reinterpret_cast<float*>(base + o_plse) : nullptr;
   w.seg_ready = tc ? reinterpret_cast<int*>(base + o_sready) : nullptr;
+  w.idx_done = reinterpret_cast<int*>(base + o_done);
   w.max_T = maxT;
   w.max_batch = cfg->max_batch;
   w.scores_ld = ld;
@@ -544,12 +561,13 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
   // the flags start with)
   h->epoch = h->epoch == 0x7fffffff ? 1 : h->epoch + 1;
   Launches L;
-  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
+  int* done = nullptr;
+  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L, &done);
   const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr, idx,
                             cnt, h->ws.status, h->dc.max_vis, st, pdl, early, h->ws.topk_ready,
-                            h->epoch);
+                            h->epoch, done, csa::indexer_qsplit(h->dc, b->S));
   }));
   L.add(staged(h, kStageAttention, st, [&] {
     return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl, true);
@@ -671,6 +689,7 @@ int csa_indexer_topk_static(const csa_config* cfg, const csa_batch* b, int32_t* 
   w.part_o = nullptr;
   w.part_lse = nullptr;
   w.seg_ready = nullptr;
+  w.idx_done = nullptr;
   w.max_T = b->B * b->S;
   w.max_batch = b->B;
   w.scores_ld = h.dc.max_vis > 0 ? h.dc.max_vis : 1;

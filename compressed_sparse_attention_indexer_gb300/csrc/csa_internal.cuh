@@ -146,6 +146,14 @@ __device__ __forceinline__ int request_rows(const DevCfg& c, int S, int L, int s
   return rows;
 }
 
+// Indexer items of a request (the work list's prefix[b + 1] - prefix[b]):
+// its 128-row key chunks, times its query groups when split by qsplit.
+__device__ __forceinline__ int request_items(const DevCfg& c, int S, int L, int score_all, int qsplit) {
+  int n = (request_rows(c, S, L, score_all) + kIdxChunk - 1) / kIdxChunk;
+  if (qsplit) n *= (S + qsplit - 1) / qsplit;
+  return n;
+}
+
 // Indexer work list: prefix[b] = first item (128-row chunk) of request b,
 // prefix[B] = number of items.  Passed by value when the host knows the
 // lengths and B <= kMaxHostReq, else computed on the device by the prep
@@ -220,6 +228,7 @@ struct Workspace {
   int* job_prefix;    // [2 (max_T + 1)] attention job lists (device-built, see JobLists)
   int* topk_ready;    // [max_T] per query: the step epoch whose Top-K output is complete
   int* seg_ready;     // [max_T * max_jobs] per segment slot: the launch epoch whose partial is complete
+  int* idx_done;      // [2, max_batch] per request: indexer items scored (two sets, see launch_indexer)
   __nv_bfloat16* part_o;  // [max_T * max_jobs, H, V] per-segment normalised attention output
                           // (bf16: the range of fp32, so any row magnitude survives)
   float* part_lse;    // [max_T * max_jobs, H] per-segment log-sum-exp (log2 units)
@@ -323,9 +332,14 @@ void* tensor_map_encoder();
 // `pdl`: launch as a programmatic dependent of the previous kernel.
 int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int score_all, int qsplit,
                 cudaStream_t st, bool pdl);
+// done / done_clear (may be NULL): with the tcgen05 kernel, each CTA adds
+// (release) to done[b] the number of request b's items it has scored once
+// their scores are stored, and the kernel zeroes done_clear[0, B) (the set
+// the next such launch uses); *published says whether it did.
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
                    int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
-                   bool pdl);
+                   bool pdl, int* done = nullptr, int* done_clear = nullptr,
+                   bool* published = nullptr);
 bool indexer_tc5_fits(const DevCfg& c, int S);
 // queries per group when a request's work is split by query group (see
 // indexer_qsplit): the warp-MMA indexer's q_idx group, and the tcgen05
@@ -335,7 +349,8 @@ constexpr int kT5Group = 4;
 int indexer_qsplit(const DevCfg& c, int S);
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
-                       int num_sms, int qsplit, cudaStream_t st, bool pdl);
+                       int num_sms, int qsplit, cudaStream_t st, bool pdl, int* done = nullptr,
+                       int* done_clear = nullptr);
 // The cache update before a step: pool[slot[t]] = src[t] (row_bytes each) for
 // t < n; strides in bytes; status may be NULL.
 int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, int n, void* pool,
@@ -346,9 +361,14 @@ int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, i
 // ready / epoch: when ready is not NULL, each query's block stores `epoch`
 // into ready[q] once its outputs are complete (the attention kernel of the
 // same step starts that query's compressed tiles on it)
+// done (with early and b): the indexer of the same call publishes each
+// request's scored items there (see launch_indexer); a block then waits for
+// its request's items instead of the indexer grid, and for the grid only at
+// its end.  qsplit: the indexer's queries per item group (indexer_qsplit).
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st, bool pdl, bool early, int* ready = nullptr, int epoch = 0);
+                cudaStream_t st, bool pdl, bool early, int* ready = nullptr, int epoch = 0,
+                const int* done = nullptr, int qsplit = 0);
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
                      cudaStream_t st, bool pdl);

@@ -77,6 +77,12 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4 in, uint32_t out[8])
   }
 }
 
+// Adds v to *p with release semantics at GPU scope (a reader that acquires
+// the sum sees every store that happened before the add).
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
+
 // Walks the work list in item order: the request owning the current item and
 // its item range, re-read only when the request changes (the single-thread
 // roles would otherwise pay a dependent global load per item).
@@ -148,7 +154,8 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
                        const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
                        int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
-                       int acc_cols, int NB, int NCB, int qsplit_arg) {
+                       int acc_cols, int NB, int NCB, int qsplit_arg, int* __restrict__ done,
+                       int* __restrict__ done_clear) {
   const int qsplit = kSplit ? qsplit_arg : 0;
   // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
   // MMAs run up to NB jobs ahead of the epilogue
@@ -378,15 +385,22 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;  // TMEM lane = key row within the item
+    // the set of completion counters the next launch uses starts at zero
+    if (done_clear && blockIdx.x == 0)
+      for (int i = row; i < b.B; i += 128) done_clear[i] = 0;
     int job = 0;
     ReqCursor cur;
     cur.init(prefix, b.B, lo);
     int L = 0;
     int64_t off = 0;
     uint32_t ephase = 0;
+    // this CTA's items of request pub_bi scored so far: published (a release
+    // add to done[pub_bi]) once every epilogue thread has stored them
+    int pub_bi = -1, pub_n = 0;
     for (int it = lo; it < hi && !*abort; ++it) {
-      bool new_unit = cur.advance(it) || it == lo;
-      if (new_unit) {
+      const bool new_req = cur.advance(it) || it == lo;
+      bool new_unit = new_req;
+      if (new_req) {
         L = b.ctx_len[cur.bi];
         off = b.idx_table ? 0 : b.idx_off[cur.bi];
         u.start(it - cur.first, chunks_of(cur.bi));
@@ -396,8 +410,14 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       if (new_unit) {
         // the unit's w (su x 64) into shared memory, shared by its items
         // (bounded barriers: a warp that gave up a wait must not strand the
-        // others)
+        // others).  The first barrier also orders every thread's score
+        // stores of the previous request before its publication.
         if (!tc5::bar_bounded(smem_u32(&sm.ebar), ephase, abort)) break;
+        if (new_req) {
+          if (done && row == 0 && pub_n > 0) red_release_add(done + pub_bi, pub_n);
+          pub_bi = cur.bi;
+          pub_n = 0;
+        }
         const float* wsrc = b.w + ((int64_t)cur.bi * S + u.g0) * kTcHi;
         for (int v = row; v < u.su * kTcHi; v += 128) w_sm[v] = __ldg(wsrc + v);
         if (!tc5::bar_bounded(smem_u32(&sm.ebar), ephase, abort)) break;
@@ -464,7 +484,11 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
         ++job;
       }
       if (!ok) break;
+      ++pub_n;
     }
+    // the last request's items, once every epilogue thread has stored them
+    if (done && !*abort && tc5::bar_bounded(smem_u32(&sm.ebar), ephase, abort) && row == 0 && pub_n > 0)
+      red_release_add(done + pub_bi, pub_n);
   }
 
   if (tid == 0 && *abort) set_status(ws.status, kStatusTimeout);
@@ -554,7 +578,8 @@ bool indexer_tc5_fits(const DevCfg& c, int S) {
 // the work list's queries per item (0: all of a request's).
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
-                       int num_sms, int qsplit, cudaStream_t st, bool pdl) {
+                       int num_sms, int qsplit, cudaStream_t st, bool pdl, int* done,
+                       int* done_clear) {
   const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;
   if (known == 0) return 0;
   if (b.idx_rows <= 0 || b.idx_rows > 0x7fffffffLL) return -2;
@@ -584,7 +609,8 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   const dim3 block(fp8 ? kT5ThreadsFp8 : kT5Threads);
   auto go = [&](auto kernel) {
     return launch_kernel(kernel, dim3(grid), block, smem, st, pdl, kmap, qmap, items, c, b, ws,
-                         score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB, p.NCB, qsplit);
+                         score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB, p.NCB, qsplit, done,
+                         done_clear);
   };
   if (fp8) return qsplit ? go(indexer_tc5_kernel<true, true>) : go(indexer_tc5_kernel<true, false>);
   return qsplit ? go(indexer_tc5_kernel<false, true>) : go(indexer_tc5_kernel<false, false>);

@@ -22,8 +22,7 @@ __global__ void __launch_bounds__(1024) prep_kernel(DevCfg c, DevBatch b, Worksp
     int items = 0;
     if (bi < b.B) {
       const int L = b.ctx_len[bi];
-      items = (request_rows(c, b.S, L, score_all) + kIdxChunk - 1) / kIdxChunk;
-      if (qsplit) items *= (b.S + qsplit - 1) / qsplit;  // (query group, key chunk) items
+      items = request_items(c, b.S, L, score_all, qsplit);  // (query group, key chunk) items
     }
     int total;
     const int ex = block_exclusive_scan(items, scan_tmp, &total);

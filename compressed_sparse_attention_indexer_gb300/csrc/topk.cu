@@ -64,6 +64,32 @@ __device__ __forceinline__ void signal_ready(int* ready, int q, int epoch) {
   }
 }
 
+// Waits until the indexer of the same call has published `target` scored
+// items of request bi in done[bi] (thread 0 polls with acquire loads,
+// bounded: a wait that gives up records CSA_ERR_TIMEOUT and the block goes
+// on), then the block meets, so that every thread's score loads follow it.
+__device__ __forceinline__ void wait_request_scored(const int* done, int bi, int target, int* status,
+                                                    int polls) {
+  if (threadIdx.x == 0) {
+    const uint32_t limit = polls < 0 ? (1u << 23) : (uint32_t)polls;
+    uint32_t i = 0, ns = 32;
+    while (true) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(done + bi) : "memory");
+      if (v >= target) break;
+      if (++i >= limit) {
+        set_status(status, kStatusTimeout);
+        break;
+      }
+      if (i >= 8) {
+        __nanosleep(ns);
+        ns = ns * 2 > 256 ? 256 : ns * 2;
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // Block-wide exclusive scan of one int per thread with a single barrier: each
 // warp scans the per-warp sums itself.  `warp_tmp` (>= 32 ints) is written
 // before the barrier and read after it, so consecutive calls alternate two
@@ -295,7 +321,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     topk_reg_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
                     const int* __restrict__ n_override, int* __restrict__ idx_out,
                     int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
-                    int early, int* ready, int epoch) {
+                    int early, int* ready, int epoch, const int* __restrict__ done, int qsplit) {
   static_assert(kJ == 2 || kJ % 4 == 0, "keys are loaded as float2 or float4 vectors");
   constexpr uint32_t kFull = (1u << kJ) - 1u;  // every key of the thread exists
   __shared__ int hist[kBins];
@@ -312,16 +338,21 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
   // kernel of the same call (early != 0), which waits for its predecessor
   // before it lets this grid launch, the lengths (the caller's inputs) are
   // complete already, so only the scores wait.
-  int n = 0;
+  int n = 0, len = 0;
   bool bad = false;
   auto plan_len = [&] {
     const int bi = q / b.S;
-    const QueryPlan p = query_plan(c, b.S, b.ctx_len[bi], q - bi * b.S, 0);
+    len = b.ctx_len[bi];
+    const QueryPlan p = query_plan(c, b.S, len, q - bi * b.S, 0);
     bad = p.flags & kPlanBad;
     n = p.vis;
   };
+  // With the indexer's per-request counters (done), a block waits for its
+  // request's scores only, and for the indexer grid at its end (so that this
+  // grid still completes after it)
+  const bool by_request = done && early && !n_override;
   if (!n_override && early) plan_len();
-  pdl_wait();
+  if (!by_request) pdl_wait();
   pdl_trigger();
   bool do_select;
   if (n_override) {
@@ -344,8 +375,10 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
     if (tid == 0) cnt_out[q] = n < K ? n : K;
     signal_ready(ready, q, epoch);
+    if (by_request) pdl_wait();
     return;
   }
+  if (by_request) wait_request_scored(done, q / b.S, request_items(c, b.S, len, 0, qsplit), status, c.wait_polls);
   const float* sc = scores + (int64_t)q * ld;
   if (tid == 0) s_ncand = 0;
   // this thread's keys (all loads in flight at once), and the OR / AND over
@@ -584,6 +617,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     if (pos < K) out[pos] = i0 + __ffs(mm) - 1;
   if (tid == 0) cnt_out[q] = K;
   signal_ready(ready, q, epoch);
+  if (by_request) pdl_wait();
 }
 
 }  // namespace
@@ -600,7 +634,8 @@ bool topk_use_reg(int max_vis) {
 
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
-                cudaStream_t st, bool pdl, bool early, int* ready, int epoch) {
+                cudaStream_t st, bool pdl, bool early, int* ready, int epoch, const int* done,
+                int qsplit) {
   if (nq == 0) return 0;
   DevBatch none = {};
   none.S = 1;
@@ -609,7 +644,7 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
                                                               : topk_reg_kernel<kRegKeys>,
                          dim3(nq), dim3(kTopkThreads), 0, st, pdl, c, b ? *b : none, scores, ld,
                          n_override, idx_out, cnt_out, status, max_vis, (pdl && early) ? 1 : 0,
-                         ready, epoch);
+                         ready, epoch, (pdl && early && b) ? done : nullptr, qsplit);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
   if (smem > kTopkSmemMax)  // rows are bounded at create time
     return launch_fail("Top-K: rows longer than the kernel holds", cudaSuccess);
