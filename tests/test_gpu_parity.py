@@ -415,6 +415,44 @@ def test_many_consecutive_steps_keep_a_clean_status():
     assert torch.equal(out, first)
 
 
+def test_steps_without_indexer_work_between_selecting_steps():
+    # The indexer publishes each request's scored items to one of two
+    # counter sets and zeroes the other for its next launch; a step whose
+    # queries all bypass scoring launches no indexer.  Alternating such steps
+    # (with and without host lengths) with selecting ones, with the indexer +
+    # Top-K entry (which publishes nothing) in between, every selecting step
+    # must reproduce the first one bit for bit with a clean status: a counter
+    # set left stale would let Top-K read scores early.
+    wl = WORKLOADS["topk_b16_l8192"]
+    cfg = wl.cfg
+    sel = make_batch(wl, lens=[8192, 5000, 2100, 4097])
+    byp = make_batch(wl, lens=[2048, 700, 129, 1])
+    ds, db_ = to_device(sel, DEV), to_device(byp, DEV)
+    dec = csa.Decoder(cfg, 4, 1, 8192)
+    ls, lb = sel["ctx_len"].clone(), byp["ctx_len"].clone()
+    structs = [csa.make_batch_struct(ds, ls), csa.make_batch_struct(ds)]
+    bstructs = [csa.make_batch_struct(db_, lb), csa.make_batch_struct(db_)]
+    out = torch.empty(4, 1, cfg.H, cfg.V, dtype=cfg.torch_dtype, device=DEV)
+    idx = torch.empty(4, 1, cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(4, 1, dtype=torch.int32, device=DEV)
+    dec.decode_step(structs[0], out, None, idx, cnt)
+    torch.cuda.synchronize()
+    assert dec.status() == csa.CSA_OK, csa.last_error()
+    first, first_idx = out.clone(), idx.clone()
+    for i in range(12):
+        for _ in range(i % 3):
+            dec.decode_step(bstructs[i % 2], out, None, idx, cnt)
+        if i % 4 == 1:
+            dec.indexer_topk(structs[i % 2], idx, cnt)
+        out.fill_(float("nan"))
+        dec.decode_step(structs[(i // 2) % 2], out, None, idx, cnt)
+        torch.cuda.synchronize()
+        assert dec.status() == csa.CSA_OK, csa.last_error()
+        assert torch.equal(idx, first_idx)
+        assert torch.equal(out, first)
+    dec.close()
+
+
 def test_empty_batch_is_a_noop():
     wl = WORKLOADS["bypass_b16_l256"]
     hb = make_batch(wl, lens=[256])
