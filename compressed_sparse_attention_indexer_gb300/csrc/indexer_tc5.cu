@@ -5,7 +5,8 @@
 // unpack" (the indexer) and "Fix: port the DeepSeek-V4 MoE, hc_pre and
 // prefill fixes to DSpark" (fixed, ascending reduction order; no atomics).
 //
-// Persistent kernel, one CTA per SM, warp-specialised:
+// Persistent kernel, two CTAs per SM (one when a work unit's q_idx leaves no
+// room), warp-specialised:
 //   warp 4  TMA producer: per work item (128 key rows of one request) two
 //           128x64 bf16 boxes, 128-byte swizzled, into a ring of stages;
 //           the work unit's q_idx (its queries x 64 heads x 128) when the
@@ -19,6 +20,8 @@
 //           of NB TMEM accumulators (8 of 64 columns when S = 1, so the MMAs
 //           run up to 8 items ahead of the epilogue), then commits to
 //           mbarriers;
+//   warps 6-9 (FP8 keys) converters: one thread per key row turns the
+//           item's E4M3 codes into the bf16 tile the MMA reads;
 //   warps 0-3 epilogue: thread t owns TMEM lane t = key row t of the item;
 //           it reads that row's 64 head dot products of a query and sums
 //           w_h * ReLU(.) as four 16-head partials (h ascending within each),
@@ -39,7 +42,9 @@ namespace csa {
 namespace {
 
 constexpr int kT5Threads = 192;
-constexpr int kConvThreads = 256;               // FP8: eight converter warps, two per key row
+constexpr int kConvWarps = 4;                   // FP8: converter warps, one thread per key row
+constexpr int kConvThreads = 32 * kConvWarps;
+constexpr int kFp8CtasPerSm = 2;                // FP8: CTAs per SM (register budget of the launch)
 constexpr int kT5ThreadsFp8 = kT5Threads + kConvThreads;
 constexpr int kSubBytes = kIdxChunk * 64 * 2;   // 128 rows x 64 dims bf16 = 16 KB
 constexpr int kStageBytes = 2 * kSubBytes;      // 32 KB: one item of keys
@@ -149,7 +154,7 @@ struct UnitCursor {
 // kSplit: the work list splits requests by query group (qsplit queries per
 // unit); without it the unit bookkeeping folds away.
 template <bool kFp8, bool kSplit>
-__global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
+__global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8CtasPerSm : 1)
     indexer_tc5_kernel(const __grid_constant__ CUtensorMap kmap,
                        const __grid_constant__ CUtensorMap qmap,
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
@@ -353,12 +358,12 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
     }
   } else if (kFp8 && warp >= 6) {
     // ------------------------------------------------------------ converters (FP8 keys)
-    // two threads per key row r of each item: half hf converts dims
-    // 64 hf .. 64 hf + 63, four 16-byte FP8 chunks of the TMA tile (128-byte
-    // swizzle: chunk c at (c ^ (r & 7))), into bf16 sub-tile hf of a
-    // converted buffer (the same swizzle); then each thread frees the stage
-    // and publishes the buffer to the MMA issuer
-    const int r = ((warp - 6) & 3) * 32 + lane, hf = (warp - 6) >> 2;
+    // one thread per key row r of each item: the row's eight 16-byte FP8
+    // chunks of the TMA tile (128-byte swizzle: chunk c at (c ^ (r & 7)))
+    // into the two bf16 sub-tiles of a converted buffer (the same swizzle);
+    // then each thread frees the stage and publishes the buffer to the MMA
+    // issuer
+    const int r = (warp - 6) * 32 + lane;
     int kc = 0;
     for (int it = lo; it < hi && !*abort; ++it, ++kc) {
       const int st = kc % NST, cb = kc % NCB;
@@ -368,7 +373,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
       const uint8_t* src = smem_raw + (kbuf + st * kStage8Bytes - smem_u32(smem_raw)) + r * 128;
       uint8_t* dst = smem_raw + (cbuf + cb * kStageBytes - smem_u32(smem_raw)) + r * 128;
 #pragma unroll
-      for (int c = 4 * hf; c < 4 * hf + 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
         uint32_t o[8];
         e4m3x16_to_bf16(v, o);
@@ -445,14 +450,16 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, 1)
           const QueryPlan p = query_plan(c, S, L, s, score_all);
           if (!(p.flags & kPlanScore) || p.vis <= c0) continue;  // warp-uniform
           const uint32_t ta = tmem + ((uint32_t)(warp * 32) << 16) + tb * acc_cols + sl * kTcHi;
-          float v[64];
-          tc5::tmem_ld32x2(ta, v, v + 32);
           // four disjoint 16-head partials, each summed in ascending h, then
-          // added in ascending order
+          // added in ascending order; the heads come out of TMEM 32 at a time
+          // (FP8 keys: two CTAs per SM leave fewer registers per thread)
           const float4* w4 = reinterpret_cast<const float4*>(w_sm + (g * G + sl) * kTcHi);
           float part[4];
+          float v[64];
+          if (!kFp8) tc5::tmem_ld32x2(ta, v, v + 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
+            if (kFp8 && (k & 1) == 0) tc5::tmem_ld32(ta + 16 * k, v + 16 * k);
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -524,6 +531,39 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 struct T5Plan {
   int ctas_per_sm, acc_cols, NB, NCB, NST, NQB, stage_bytes, conv_bytes, qbytes;
 };
+// The plan for a given number of CTAs per SM; false if two key stages do
+// not fit.
+static bool plan_t5_with(const DevCfg& c, int S, int ctas, int max_stages, T5Plan* p) {
+  const bool fp8 = c.idx_fp8 != 0;
+  p->ctas_per_sm = ctas;
+  const int G = S < 4 ? S : 4;
+  p->acc_cols = 32;
+  while (p->acc_cols < 64 * G) p->acc_cols <<= 1;  // power of two >= 32
+  p->NB = 512 / p->ctas_per_sm / p->acc_cols;       // accumulators that fit in TMEM
+  if (p->NB > 8) p->NB = 8;
+  if (p->NB < 2) return false;
+  p->qbytes = S * 2 * kQSubBytes;
+  const int per_cta = 228 * 1024 / p->ctas_per_sm - 1024;  // per-SM shared memory / CTAs
+  p->stage_bytes = fp8 ? kStage8Bytes : kStageBytes;
+  const int fixed = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
+  // FP8: two converted items when two key stages still fit beside them,
+  // else one (measured: a third adds nothing)
+  p->NCB = fp8 ? kConvBufs : 0;
+  if (fp8 && fixed - p->NCB * kStageBytes - p->qbytes < 2 * p->stage_bytes) p->NCB = 1;
+  p->conv_bytes = p->NCB * kStageBytes;
+  // key stages first: a CTA spans few requests, so a second q_idx buffer
+  // (prefetching the next request's queries) is kept only when it costs no
+  // key stage
+  const int budget = fixed - p->conv_bytes;
+  auto stages = [&](int nqb) {
+    const int n = (budget - nqb * p->qbytes) / p->stage_bytes;
+    return n > max_stages ? max_stages : n;
+  };
+  p->NQB = stages(2) >= stages(1) ? 2 : 1;
+  p->NST = stages(p->NQB);
+  return p->NST >= 2;
+}
+
 static bool plan_t5(const DevCfg& c, int S, T5Plan* p) {
   static const int max_stages = [] {
     const char* e = getenv("CSA_T5_STAGES");
@@ -538,33 +578,13 @@ static bool plan_t5(const DevCfg& c, int S, T5Plan* p) {
   // CTAs per SM: two independent pipelines per SM stream measurably faster
   // than one deeper ring (the ring depth beyond three stages does not
   // matter), so two whenever a request's q_idx leaves room for two stages
-  // each.  FP8 keys: one CTA per SM (the converted buffers leave no room for
-  // a second CTA's ring).
-  const bool fp8 = c.idx_fp8 != 0;
-  p->ctas_per_sm = forced_ctas ? forced_ctas : ((S <= 2 && !fp8) ? 2 : 1);
-  const int G = S < 4 ? S : 4;
-  p->acc_cols = 32;
-  while (p->acc_cols < 64 * G) p->acc_cols <<= 1;  // power of two >= 32
-  p->NB = 512 / p->ctas_per_sm / p->acc_cols;       // accumulators that fit in TMEM
-  if (p->NB > 8) p->NB = 8;
-  if (p->NB < 2) return false;
-  p->qbytes = S * 2 * kQSubBytes;
-  const int per_cta = 228 * 1024 / p->ctas_per_sm - 1024;  // per-SM shared memory / CTAs
-  p->stage_bytes = fp8 ? kStage8Bytes : kStageBytes;
-  // FP8: two converted items (measured: a third adds nothing)
-  p->NCB = fp8 ? kConvBufs : 0;
-  p->conv_bytes = p->NCB * kStageBytes;
-  // key stages first: a CTA spans few requests, so a second q_idx buffer
-  // (prefetching the next request's queries) is kept only when it costs no
-  // key stage
-  const int budget = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4 - p->conv_bytes;
-  auto stages = [&](int nqb) {
-    const int n = (budget - nqb * p->qbytes) / p->stage_bytes;
-    return n > max_stages ? max_stages : n;
-  };
-  p->NQB = stages(2) >= stages(1) ? 2 : 1;
-  p->NST = stages(p->NQB);
-  return p->NST >= 2;
+  // each; FP8 keys likewise, each CTA with one converted buffer when two do
+  // not fit (the FP8 kernel is compiled for two CTAs' registers).
+  if (forced_ctas) return plan_t5_with(c, S, forced_ctas, max_stages, p);
+  const int first = c.idx_fp8 ? kFp8CtasPerSm : (S <= 2 ? 2 : 1);
+  for (int ctas = first; ctas >= 1; --ctas)
+    if (plan_t5_with(c, S, ctas, max_stages, p)) return true;
+  return false;
 }
 
 bool indexer_tc5_fits(const DevCfg& c, int S) {
