@@ -160,11 +160,16 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
                        int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
                        int acc_cols, int NB, int NCB, int qsplit_arg, int* __restrict__ done,
-                       int* __restrict__ done_clear) {
+                       int* __restrict__ done_clear, int a_tmem) {
   const int qsplit = kSplit ? qsplit_arg : 0;
   // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
   // MMAs run up to NB jobs ahead of the epilogue
-  const uint32_t tmem_cols = (uint32_t)(NB * acc_cols);
+  // FP8 keys with a_tmem: the NCB converted items (128 rows x 64 columns of
+  // bf16 pairs each) sit in TMEM after the accumulators, as the MMAs' A
+  // operand, instead of in shared memory
+  const bool ta = kFp8 && a_tmem;
+  const uint32_t tmem_cols = (uint32_t)(NB * acc_cols + (ta ? NCB * 64 : 0));
+  const uint32_t acol = (uint32_t)(NB * acc_cols);  // the first converted item's column
   extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 below
   __shared__ T5Smem sm;
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -177,7 +182,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
   const int S = b.S;
   const int SU = qsplit ? qsplit : S;                          // queries per unit
   const uint32_t qbytes = (uint32_t)SU * 2u * kQSubBytes;      // one unit's q_idx
-  const uint32_t qbuf = cbuf + (kFp8 ? (uint32_t)NCB * kStageBytes : 0u);  // NQB x qbytes
+  const uint32_t qbuf = cbuf + ((kFp8 && !a_tmem) ? (uint32_t)NCB * kStageBytes : 0u);  // NQB x qbytes
   float* w_sm = reinterpret_cast<float*>(smem_raw + (qbuf + (uint32_t)NQB * qbytes - smem_u32(smem_raw)));
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -334,13 +339,24 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
           }
           tc5::fence_after_sync();
           const uint32_t idesc = tc5::idesc_bf16_f32(128, 64 * gn);
+          if (ta) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (uint32_t)(k & 3) * 32u;
-            const uint64_t ad = tc5::sdesc_k_sw128(ka + (k >> 2) * kSubBytes + off);
-            const uint64_t bd =
-                tc5::sdesc_k_sw128(qa + (k >> 2) * (SU * kQSubBytes) + g * G * kQSubBytes + off);
-            tc5::mma_bf16(tmem + tb * acc_cols, ad, bd, idesc, k > 0 ? 1u : 0u);
+            for (int k = 0; k < 8; ++k) {  // K = 16: eight columns of bf16 pairs per step
+              const uint32_t off = (uint32_t)(k & 3) * 32u;
+              const uint64_t bd =
+                  tc5::sdesc_k_sw128(qa + (k >> 2) * (SU * kQSubBytes) + g * G * kQSubBytes + off);
+              tc5::mma_bf16_ta(tmem + tb * acc_cols, tmem + acol + cb * 64 + 8 * k, bd, idesc,
+                               k > 0 ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t off = (uint32_t)(k & 3) * 32u;
+              const uint64_t ad = tc5::sdesc_k_sw128(ka + (k >> 2) * kSubBytes + off);
+              const uint64_t bd =
+                  tc5::sdesc_k_sw128(qa + (k >> 2) * (SU * kQSubBytes) + g * G * kQSubBytes + off);
+              tc5::mma_bf16(tmem + tb * acc_cols, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
           }
           tc5::mma_commit(smem_u32(&sm.tfull[tb]));
           ++job;
@@ -363,7 +379,9 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
     // into the two bf16 sub-tiles of a converted buffer (the same swizzle);
     // then each thread frees the stage and publishes the buffer to the MMA
     // issuer
-    const int r = (warp - 6) * 32 + lane;
+    // (a_tmem: into the row's TMEM lane, which this warp's lane quarter holds,
+    // column 8c + i holding dims 16c + 2i and 16c + 2i + 1)
+    const int r = 32 * (warp & 3) + lane;
     int kc = 0;
     for (int it = lo; it < hi && !*abort; ++it, ++kc) {
       const int st = kc % NST, cb = kc % NCB;
@@ -371,6 +389,26 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
       if (kc >= NCB && !tc5::mbar_wait(smem_u32(&sm.cempty[cb]), ((kc / NCB) - 1) & 1, abort))
         break;
       const uint8_t* src = smem_raw + (kbuf + st * kStage8Bytes - smem_u32(smem_raw)) + r * 128;
+      if (ta) {
+        tc5::fence_after_sync();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t o[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c = 4 * h + c4;
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((c ^ (r & 7)) << 4));
+            e4m3x16_to_bf16(v, o + 8 * c4);
+          }
+          tc5::tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + acol + cb * 64 + 32 * h,
+                         reinterpret_cast<const float*>(o));
+        }
+        tc5::tmem_wait_st();
+        tc5::fence_before_sync();
+        tc5::mbar_arrive(smem_u32(&sm.empty[st]));
+        tc5::mbar_arrive(smem_u32(&sm.cfull[cb]));
+        continue;
+      }
       uint8_t* dst = smem_raw + (cbuf + cb * kStageBytes - smem_u32(smem_raw)) + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -529,28 +567,34 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 // the warp-MMA kernel).  Tuning knobs, read once: CSA_T5_STAGES caps the ring
 // depth, CSA_T5_CTAS forces the CTAs per SM (1..4).
 struct T5Plan {
-  int ctas_per_sm, acc_cols, NB, NCB, NST, NQB, stage_bytes, conv_bytes, qbytes;
+  int ctas_per_sm, acc_cols, NB, NCB, NST, NQB, stage_bytes, conv_bytes, qbytes, a_tmem;
 };
-// The plan for a given number of CTAs per SM; false if two key stages do
+// The plan for a given number of CTAs per SM (FP8 keys: converted items in
+// TMEM or in shared memory); false if two key stages or two accumulators do
 // not fit.
-static bool plan_t5_with(const DevCfg& c, int S, int ctas, int max_stages, T5Plan* p) {
+static bool plan_t5_with(const DevCfg& c, int S, int ctas, bool a_tmem, int max_stages, T5Plan* p) {
   const bool fp8 = c.idx_fp8 != 0;
   p->ctas_per_sm = ctas;
+  p->a_tmem = fp8 && a_tmem ? 1 : 0;
   const int G = S < 4 ? S : 4;
   p->acc_cols = 32;
   while (p->acc_cols < 64 * G) p->acc_cols <<= 1;  // power of two >= 32
-  p->NB = 512 / p->ctas_per_sm / p->acc_cols;       // accumulators that fit in TMEM
+  // accumulators that fit in TMEM beside the converted items (two of 64
+  // columns with a_tmem); an allocation is a power of two columns
+  const int areserve = p->a_tmem ? 2 * 64 : 0;
+  p->NB = (512 / p->ctas_per_sm - areserve) / p->acc_cols;
   if (p->NB > 8) p->NB = 8;
+  while (p->NB >= 2 && ((p->NB * p->acc_cols + areserve) & (p->NB * p->acc_cols + areserve - 1))) --p->NB;
   if (p->NB < 2) return false;
   p->qbytes = S * 2 * kQSubBytes;
   const int per_cta = 228 * 1024 / p->ctas_per_sm - 1024;  // per-SM shared memory / CTAs
   p->stage_bytes = fp8 ? kStage8Bytes : kStageBytes;
   const int fixed = per_cta - 1024 - (int)sizeof(T5Smem) - 64 - S * kTcHi * 4;
-  // FP8: two converted items when two key stages still fit beside them,
-  // else one (measured: a third adds nothing)
+  // FP8 converted items: two in TMEM, or in shared memory two when two key
+  // stages still fit beside them, else one (measured: a third adds nothing)
   p->NCB = fp8 ? kConvBufs : 0;
-  if (fp8 && fixed - p->NCB * kStageBytes - p->qbytes < 2 * p->stage_bytes) p->NCB = 1;
-  p->conv_bytes = p->NCB * kStageBytes;
+  if (fp8 && !p->a_tmem && fixed - p->NCB * kStageBytes - p->qbytes < 2 * p->stage_bytes) p->NCB = 1;
+  p->conv_bytes = (fp8 && !p->a_tmem) ? p->NCB * kStageBytes : 0;
   // key stages first: a CTA spans few requests, so a second q_idx buffer
   // (prefetching the next request's queries) is kept only when it costs no
   // key stage
@@ -575,15 +619,24 @@ static bool plan_t5(const DevCfg& c, int S, T5Plan* p) {
     const int v = f ? atoi(f) : 0;
     return (v < 0 || v > 4) ? 0 : v;
   }();
+  // FP8 converted items in TMEM unless CSA_T5_ATMEM=0
+  static const bool atmem = [] {
+    const char* e = getenv("CSA_T5_ATMEM");
+    return !(e && e[0] == '0');
+  }();
   // CTAs per SM: two independent pipelines per SM stream measurably faster
   // than one deeper ring (the ring depth beyond three stages does not
   // matter), so two whenever a request's q_idx leaves room for two stages
-  // each; FP8 keys likewise, each CTA with one converted buffer when two do
-  // not fit (the FP8 kernel is compiled for two CTAs' registers).
-  if (forced_ctas) return plan_t5_with(c, S, forced_ctas, max_stages, p);
-  const int first = c.idx_fp8 ? kFp8CtasPerSm : (S <= 2 ? 2 : 1);
-  for (int ctas = first; ctas >= 1; --ctas)
-    if (plan_t5_with(c, S, ctas, max_stages, p)) return true;
+  // each; FP8 keys likewise (the FP8 kernel is compiled for two CTAs'
+  // registers), with the converted items in TMEM when they fit beside the
+  // accumulators, else in shared memory.
+  const bool fp8 = c.idx_fp8 != 0;
+  const int first = forced_ctas ? forced_ctas : (fp8 ? kFp8CtasPerSm : (S <= 2 ? 2 : 1));
+  const int last = forced_ctas ? forced_ctas : 1;
+  for (int ctas = first; ctas >= last; --ctas) {
+    if (fp8 && atmem && plan_t5_with(c, S, ctas, true, max_stages, p)) return true;
+    if (plan_t5_with(c, S, ctas, false, max_stages, p)) return true;
+  }
   return false;
 }
 
@@ -630,7 +683,7 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   auto go = [&](auto kernel) {
     return launch_kernel(kernel, dim3(grid), block, smem, st, pdl, kmap, qmap, items, c, b, ws,
                          score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB, p.NCB, qsplit, done,
-                         done_clear);
+                         done_clear, p.a_tmem);
   };
   if (fp8) return qsplit ? go(indexer_tc5_kernel<true, true>) : go(indexer_tc5_kernel<true, false>);
   return qsplit ? go(indexer_tc5_kernel<false, true>) : go(indexer_tc5_kernel<false, false>);
