@@ -167,8 +167,8 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
   // FP8 keys with a_tmem: the NCB converted items (128 rows x 64 columns of
   // bf16 pairs each) sit in TMEM after the accumulators, as the MMAs' A
   // operand, instead of in shared memory
-  const bool ta = kFp8 && a_tmem;
-  const uint32_t tmem_cols = (uint32_t)(NB * acc_cols + (ta ? NCB * 64 : 0));
+  const bool a_in_tmem = kFp8 && a_tmem;
+  const uint32_t tmem_cols = (uint32_t)(NB * acc_cols + (a_in_tmem ? NCB * 64 : 0));
   const uint32_t acol = (uint32_t)(NB * acc_cols);  // the first converted item's column
   extern __shared__ __align__(16) uint8_t smem_raw[];  // aligned to 1024 below
   __shared__ T5Smem sm;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
           }
           tc5::fence_after_sync();
           const uint32_t idesc = tc5::idesc_bf16_f32(128, 64 * gn);
-          if (ta) {
+          if (a_in_tmem) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) {  // K = 16: eight columns of bf16 pairs per step
               const uint32_t off = (uint32_t)(k & 3) * 32u;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
       if (kc >= NCB && !tc5::mbar_wait(smem_u32(&sm.cempty[cb]), ((kc / NCB) - 1) & 1, abort))
         break;
       const uint8_t* src = smem_raw + (kbuf + st * kStage8Bytes - smem_u32(smem_raw)) + r * 128;
-      if (ta) {
+      if (a_in_tmem) {
         tc5::fence_after_sync();
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -491,9 +491,13 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
           // four disjoint 16-head partials, each summed in ascending h, then
           // added in ascending order; the heads come out of TMEM 32 at a time
           // (FP8 keys: two CTAs per SM leave fewer registers per thread)
+          // FP8 keys: with a positive row scale, ReLU(ks x) = ks ReLU(x), so
+          // the scale multiplies the row's sum once (any other scale: each
+          // dot product, as defined)
           const float4* w4 = reinterpret_cast<const float4*>(w_sm + (g * G + sl) * kTcHi);
           float part[4];
           float v[64];
+          const bool per_head = kFp8 && !(ks > 0.f);
           if (!kFp8) tc5::tmem_ld32x2(ta, v, v + 32);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
             for (int i = 0; i < 4; ++i) {
               const float4 wv = w4[k * 4 + i];
               const int h = k * 16 + i * 4;
-              if (kFp8) {
+              if (per_head) {
                 acc = fmaf(wv.x, fmaxf(v[h] * ks, 0.f), acc);
                 acc = fmaf(wv.y, fmaxf(v[h + 1] * ks, 0.f), acc);
                 acc = fmaf(wv.z, fmaxf(v[h + 2] * ks, 0.f), acc);
@@ -517,7 +521,8 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
             }
             part[k] = acc;
           }
-          const float sum = ((part[0] + part[1]) + part[2]) + part[3];
+          float sum = ((part[0] + part[1]) + part[2]) + part[3];
+          if (kFp8 && !per_head) sum *= ks;
           const int j = c0 + row;
           if (j < p.vis) {
             if (!in_pool) set_status(ws.status, kStatusBadIndex);
