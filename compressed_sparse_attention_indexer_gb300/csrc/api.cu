@@ -38,6 +38,9 @@ struct csa_handle {
 };
 
 namespace {
+// queries per request up to which a decode step's Top-K blocks wait on the
+// indexer's per-request counters (see csa_decode_step)
+constexpr int kCounterMaxS = 1;
 enum Stage { kStagePlan = 0, kStageIndexer = 1, kStageTopk = 2, kStageAttention = 3, kStages = 4 };
 
 cudaEvent_t take_event(csa_handle* h) {
@@ -561,8 +564,13 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
   // the flags start with)
   h->epoch = h->epoch == 0x7fffffff ? 1 : h->epoch + 1;
   Launches L;
+  // Top-K blocks start per request (indexer completion counters) in
+  // single-token decode; with more queries per request it measured slower
+  // than waiting for the indexer grid (S = 8: 105.2 against 102.4 us per
+  // step; a 512-token prefill chunk, hundreds of blocks polling one
+  // request's counter: 782 against 437 us)
   int* done = nullptr;
-  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L, &done);
+  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L, b->S <= kCounterMaxS ? &done : nullptr);
   const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr, idx,
