@@ -59,6 +59,26 @@ def test_variant_parity(env):
     assert r.returncode == 0 and "variant ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
 
 
+# FP8 keys under the indexer's other launch shapes: converted items in
+# shared memory (CSA_T5_ATMEM=0, two CTAs per SM with one converted item
+# each), one CTA per SM (CSA_T5_CTAS=1, converted items in TMEM beside six
+# accumulators), and both
+CHILD_FP8 = CHILD.replace(
+    "cfg = BF16_CFG", "from dataclasses import replace\ncfg = replace(BF16_CFG, idx_dtype=\"fp8\")")
+
+
+@pytest.mark.parametrize("env", [{"CSA_T5_ATMEM": "0"}, {"CSA_T5_CTAS": "1"},
+                                 {"CSA_T5_ATMEM": "0", "CSA_T5_CTAS": "1"}])
+def test_fp8_indexer_launch_shapes(env):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    code = "ROOT = %r\n" % ROOT + CHILD_FP8
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), cwd=ROOT,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "variant ok" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
+
+
 CHILD_SPLIT = r'''
 import sys, numpy as np, torch
 sys.path.insert(0, ROOT)
