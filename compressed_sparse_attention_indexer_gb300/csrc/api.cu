@@ -302,7 +302,8 @@ int finish(csa_handle* h, const Launches& L) {
 // counter set and zeroes the other one; *done then points at the set it used
 // (NULL if no kernel published), and the next publishing launch uses the other.
 void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int score_all,
-                 float* scores, int64_t ld, cudaStream_t st, Launches& L, int** done = nullptr) {
+                 float* scores, int64_t ld, cudaStream_t st, Launches& L, int** done = nullptr,
+                 bool keys = false, bool* keyed = nullptr) {
   csa::ItemList& items = h->items;
   host_items(h, b, score_all, &items);
   const bool pdl = use_pdl();
@@ -318,11 +319,12 @@ void run_indexer(csa_handle* h, const csa_batch* b, const csa::DevBatch& db, int
     cur = h->ws.idx_done + (size_t)h->done_set * h->ws.max_batch;
     other = h->ws.idx_done + (size_t)(h->done_set ^ 1) * h->ws.max_batch;
   }
-  bool published = false;
+  bool published = false, wrote_keys = false;
   L.add(staged(h, kStageIndexer, st, [&] {
     return csa::launch_indexer(h->dc, db, h->ws, items, score_all, scores, ld, h->num_sms, st, pdl,
-                               cur, other, &published);
+                               cur, other, &published, keys, &wrote_keys);
   }));
+  if (keyed) *keyed = wrote_keys;
   if (done) *done = published ? cur : nullptr;
   if (published) h->done_set ^= 1;
 }
@@ -522,11 +524,16 @@ int csa_indexer_topk(csa_handle* h, const csa_batch* b, int32_t* topk_idx, int32
   const csa::DevBatch db = dev_batch(b);
   const bool pdl = use_pdl();
   Launches L;
-  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L);
+  // the internal scores go to Top-K as order-preserving keys when the
+  // register kernel selects (it then skips the conversion)
+  bool keyed = false;
+  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L, nullptr,
+              csa::topk_use_reg(h->dc.max_vis), &keyed);
   const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr,
-                            topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st, pdl, early);
+                            topk_idx, topk_cnt, h->ws.status, h->dc.max_vis, st, pdl, early,
+                            nullptr, 0, nullptr, 0, keyed);
   }));
   return finish(h, L);
 }
@@ -570,12 +577,16 @@ int csa_decode_step(csa_handle* h, const csa_batch* b, void* out, float* lse_out
   // step; a 512-token prefill chunk, hundreds of blocks polling one
   // request's counter: 782 against 437 us)
   int* done = nullptr;
-  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L, b->S <= kCounterMaxS ? &done : nullptr);
+  // the internal scores go to Top-K as order-preserving keys when the
+  // register kernel selects (it then skips the conversion)
+  bool keyed = false;
+  run_indexer(h, b, db, 0, h->ws.scores, h->ws.scores_ld, st, L, b->S <= kCounterMaxS ? &done : nullptr,
+              csa::topk_use_reg(h->dc.max_vis), &keyed);
   const bool early = L.n > 0;  // the plan or indexer kernel runs right before
   L.add(staged(h, kStageTopk, st, [&] {
     return csa::launch_topk(h->dc, &db, b->B * b->S, h->ws.scores, h->ws.scores_ld, nullptr, idx,
                             cnt, h->ws.status, h->dc.max_vis, st, pdl, early, h->ws.topk_ready,
-                            h->epoch, done, csa::indexer_qsplit(h->dc, b->S));
+                            h->epoch, done, csa::indexer_qsplit(h->dc, b->S), keyed);
   }));
   L.add(staged(h, kStageAttention, st, [&] {
     return run_attention(h, b, db, idx, cnt, out, lse_out, st, pdl, true);

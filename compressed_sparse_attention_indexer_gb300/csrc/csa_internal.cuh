@@ -146,6 +146,18 @@ __device__ __forceinline__ int request_rows(const DevCfg& c, int S, int L, int s
   return rows;
 }
 
+// A score as an order-preserving 32-bit key (a larger score, a larger key):
+// adding +0.0 turns -0.0 into +0.0 (IEEE round to nearest), then negative
+// values have every bit flipped and the others only the sign bit; NaN is 0,
+// below every number.  The indexer can store its scores in this form for the
+// Top-K kernel of the same call.
+__device__ __forceinline__ uint32_t score_order_key(float f) {
+  const float g = f + 0.f;
+  uint32_t u = __float_as_uint(g);
+  u ^= (uint32_t)((int32_t)u >> 31) | 0x80000000u;
+  return g != g ? 0u : u;
+}
+
 // Indexer items of a request (the work list's prefix[b + 1] - prefix[b]):
 // its 128-row key chunks, times its query groups when split by qsplit.
 __device__ __forceinline__ int request_items(const DevCfg& c, int S, int L, int score_all, int qsplit) {
@@ -336,10 +348,12 @@ int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int sco
 // (release) to done[b] the number of request b's items it has scored once
 // their scores are stored, and the kernel zeroes done_clear[0, B) (the set
 // the next such launch uses); *published says whether it did.
+// keys (tcgen05 kernel only): the scores are stored as score_order_key bits;
+// *keyed says whether they were.
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
                    int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
                    bool pdl, int* done = nullptr, int* done_clear = nullptr,
-                   bool* published = nullptr);
+                   bool* published = nullptr, bool keys = false, bool* keyed = nullptr);
 bool indexer_tc5_fits(const DevCfg& c, int S);
 // queries per group when a request's work is split by query group (see
 // indexer_qsplit): the warp-MMA indexer's q_idx group, and the tcgen05
@@ -350,7 +364,7 @@ int indexer_qsplit(const DevCfg& c, int S);
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
                        int num_sms, int qsplit, cudaStream_t st, bool pdl, int* done = nullptr,
-                       int* done_clear = nullptr);
+                       int* done_clear = nullptr, bool keys = false);
 // The cache update before a step: pool[slot[t]] = src[t] (row_bytes each) for
 // t < n; strides in bytes; status may be NULL.
 int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, int n, void* pool,
@@ -365,10 +379,13 @@ int launch_writeback(const void* src, int64_t src_stride, const int64_t* slot, i
 // request's scored items there (see launch_indexer); a block then waits for
 // its request's items instead of the indexer grid, and for the grid only at
 // its end.  qsplit: the indexer's queries per item group (indexer_qsplit).
+// keys: the scores are score_order_key bits (only with the register kernel,
+// topk_use_reg).
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
                 cudaStream_t st, bool pdl, bool early, int* ready = nullptr, int epoch = 0,
-                const int* done = nullptr, int qsplit = 0);
+                const int* done = nullptr, int qsplit = 0, bool keys = false);
+bool topk_use_reg(int max_vis);
 int launch_attention(const DevCfg& c, const DevBatch& b, const Workspace& ws, const int* topk_idx,
                      const int* topk_cnt, void* out, float* lse_out, int num_sms,
                      cudaStream_t st, bool pdl);

@@ -287,21 +287,24 @@ int indexer_qsplit(const DevCfg& c, int S) {
 
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,
                    int score_all, float* scores, int64_t ld, int num_sms, cudaStream_t st,
-                   bool pdl, int* done, int* done_clear, bool* published) {
+                   bool pdl, int* done, int* done_clear, bool* published, bool keys, bool* keyed) {
   if (published) *published = false;
+  if (keyed) *keyed = false;
   const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;  // items, if known
   if (known == 0) return 0;
   const int qsplit = indexer_qsplit(c, b.S);
   if (c.idx_fp8) {  // FP8 keys: the tcgen05 kernel only (its shape is checked at create)
     const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, qsplit, st,
-                                     pdl, done, done_clear);
+                                     pdl, done, done_clear, keys);
     if (r > 0 && published) *published = done != nullptr;
+    if (r > 0 && keyed) *keyed = keys;
     return r == -2 ? -1 : r;
   }
   if (tensor_core_shape(c) && indexer_impl() == kIndexerTc5) {
     const int r = launch_indexer_tc5(c, b, ws, items, score_all, scores, ld, num_sms, qsplit, st,
-                                     pdl, done, done_clear);
+                                     pdl, done, done_clear, keys);
     if (r > 0 && published) *published = done != nullptr;
+    if (r > 0 && keyed) *keyed = keys;
     if (r != -2) return r;  // -2: shape outside the tcgen05 kernel, use warp MMA
   }
   if (tensor_core_shape(c)) {

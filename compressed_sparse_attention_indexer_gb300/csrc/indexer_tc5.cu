@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
                        const __grid_constant__ ItemList items, DevCfg c, DevBatch b, Workspace ws,
                        int score_all, float* __restrict__ scores, int64_t ld, int NST, int NQB,
                        int acc_cols, int NB, int NCB, int qsplit_arg, int* __restrict__ done,
-                       int* __restrict__ done_clear, int a_tmem) {
+                       int* __restrict__ done_clear, int a_tmem, int keys) {
   const int qsplit = kSplit ? qsplit_arg : 0;
   // NB TMEM accumulators of acc_cols columns (>= 64 * queries per group): the
   // MMAs run up to NB jobs ahead of the epilogue
@@ -526,7 +526,10 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
           const int j = c0 + row;
           if (j < p.vis) {
             if (!in_pool) set_status(ws.status, kStatusBadIndex);
-            scores[(int64_t)qid * ld + j] = sum;
+            if (keys)
+              reinterpret_cast<uint32_t*>(scores)[(int64_t)qid * ld + j] = score_order_key(sum);
+            else
+              scores[(int64_t)qid * ld + j] = sum;
           }
         }
         tc5::fence_before_sync();
@@ -657,7 +660,7 @@ bool indexer_tc5_fits(const DevCfg& c, int S) {
 int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
                        const ItemList& items, int score_all, float* scores, int64_t ld,
                        int num_sms, int qsplit, cudaStream_t st, bool pdl, int* done,
-                       int* done_clear) {
+                       int* done_clear, bool keys) {
   const int known = items.host_B >= 0 ? items.prefix[items.host_B] : -1;
   if (known == 0) return 0;
   if (b.idx_rows <= 0 || b.idx_rows > 0x7fffffffLL) return -2;
@@ -688,7 +691,7 @@ int launch_indexer_tc5(const DevCfg& c, const DevBatch& b, const Workspace& ws,
   auto go = [&](auto kernel) {
     return launch_kernel(kernel, dim3(grid), block, smem, st, pdl, kmap, qmap, items, c, b, ws,
                          score_all, scores, ld, p.NST, p.NQB, p.acc_cols, p.NB, p.NCB, qsplit, done,
-                         done_clear, p.a_tmem);
+                         done_clear, p.a_tmem, keys ? 1 : 0);
   };
   if (fp8) return qsplit ? go(indexer_tc5_kernel<true, true>) : go(indexer_tc5_kernel<true, false>);
   return qsplit ? go(indexer_tc5_kernel<false, true>) : go(indexer_tc5_kernel<false, false>);

@@ -40,15 +40,6 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The same order-preserving key in fewer instructions: adding +0.0 turns
-// -0.0 into +0.0 (IEEE round to nearest), then negative values have every
-// bit flipped and the others only the sign bit; NaN is 0.
-__device__ __forceinline__ uint32_t score_key_fast(float f) {
-  const float g = f + 0.f;
-  uint32_t u = __float_as_uint(g);
-  u ^= (uint32_t)((int32_t)u >> 31) | 0x80000000u;
-  return g != g ? 0u : u;
-}
 
 // Publishes a query's Top-K output to the attention kernel of the same step,
 // which may already be running (it waits for the flag with bounded polls):
@@ -321,7 +312,8 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
     topk_reg_kernel(DevCfg c, DevBatch b, const float* __restrict__ scores, int64_t ld,
                     const int* __restrict__ n_override, int* __restrict__ idx_out,
                     int* __restrict__ cnt_out, int* __restrict__ status, int max_vis,
-                    int early, int* ready, int epoch, const int* __restrict__ done, int qsplit) {
+                    int early, int* ready, int epoch, const int* __restrict__ done, int qsplit,
+                    int keys) {
   static_assert(kJ == 2 || kJ % 4 == 0, "keys are loaded as float2 or float4 vectors");
   constexpr uint32_t kFull = (1u << kJ) - 1u;  // every key of the thread exists
   __shared__ int hist[kBins];
@@ -406,7 +398,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
       }
 #pragma unroll
       for (int j = 0; j < kJ; ++j) {
-        k[j] = score_key_fast(v[j]);
+        k[j] = keys ? __float_as_uint(v[j]) : score_order_key(v[j]);
         aor |= k[j];
         aand &= k[j];
       }
@@ -416,7 +408,7 @@ __global__ void __launch_bounds__(kTopkThreads, kJ <= kShortKeys ? 2 : 1)
       for (int j = 0; j < kJ; ++j) v[j] = i0 + j < n ? ld_once(sc + i0 + j) : 0.f;
 #pragma unroll
       for (int j = 0; j < kJ; ++j) {
-        k[j] = score_key_fast(v[j]);
+        k[j] = keys ? __float_as_uint(v[j]) : score_order_key(v[j]);
         if (i0 + j < n) {
           vmask |= 1u << j;
           aor |= k[j];
@@ -635,7 +627,7 @@ bool topk_use_reg(int max_vis) {
 int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores, int64_t ld,
                 const int* n_override, int* idx_out, int* cnt_out, int* status, int max_vis,
                 cudaStream_t st, bool pdl, bool early, int* ready, int epoch, const int* done,
-                int qsplit) {
+                int qsplit, bool keys) {
   if (nq == 0) return 0;
   DevBatch none = {};
   none.S = 1;
@@ -644,7 +636,8 @@ int launch_topk(const DevCfg& c, const DevBatch* b, int nq, const float* scores,
                                                               : topk_reg_kernel<kRegKeys>,
                          dim3(nq), dim3(kTopkThreads), 0, st, pdl, c, b ? *b : none, scores, ld,
                          n_override, idx_out, cnt_out, status, max_vis, (pdl && early) ? 1 : 0,
-                         ready, epoch, (pdl && early && b) ? done : nullptr, qsplit);
+                         ready, epoch, (pdl && early && b) ? done : nullptr, qsplit, keys ? 1 : 0);
+  if (keys) return launch_fail("Top-K: score keys need the register kernel", cudaSuccess);
   const int smem = (max_vis + max_vis / 16 + 1) * 4;
   if (smem > kTopkSmemMax)  // rows are bounded at create time
     return launch_fail("Top-K: rows longer than the kernel holds", cudaSuccess);
