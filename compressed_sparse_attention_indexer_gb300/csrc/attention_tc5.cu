@@ -172,7 +172,8 @@ struct JobCursor {
 // The split of the two job lists over the tile CTAs.  CTA i takes the W jobs
 // [wstart(i), wstart(i+1)), spread over the first E CTAs (the ones that start
 // while the Top-K kernel still runs), then the C jobs [cstart(i),
-// cstart(i+1)), spread over all G by weight (c_list_start).  Job ids: W jobs
+// cstart(i+1)), spread over all G (c_list_start: evenly with the left-over
+// jobs on the first E CTAs, or by weights).  Job ids: W jobs
 // 0 .. NW-1, C jobs NW .. NW+NC-1; a segment's partial output sits at the id
 // of its first job.
 struct Sched {
