@@ -346,8 +346,9 @@ int launch_prep(const DevCfg& c, const DevBatch& b, const Workspace& ws, int sco
                 cudaStream_t st, bool pdl);
 // done / done_clear (may be NULL): with the tcgen05 kernel, each CTA adds
 // (release) to done[b] the number of request b's items it has scored once
-// their scores are stored, and the kernel zeroes done_clear[0, B) (the set
-// the next such launch uses); *published says whether it did.
+// their scores are stored, and the kernel's CTA 0 zeroes the whole set
+// done_clear[0, ws.max_batch) (the set the next such launch uses, whatever
+// its batch size); *published says whether it did.
 // keys (tcgen05 kernel only): the scores are stored as score_order_key bits;
 // *keyed says whether they were.
 int launch_indexer(const DevCfg& c, const DevBatch& b, const Workspace& ws, const ItemList& items,

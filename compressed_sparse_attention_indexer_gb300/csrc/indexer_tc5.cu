@@ -215,6 +215,12 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
     tc5::prefetch_tmap(&qmap);
   }
   pdl_wait();
+  // the set of completion counters the next publishing launch uses starts at
+  // zero: all of it (the next batch may be larger than this one, and an entry
+  // past this batch may hold an earlier launch's count), cleared by CTA 0
+  // whether or not it has items (a small batch leaves it none)
+  if (done_clear && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < ws.max_batch; i += blockDim.x) done_clear[i] = 0;
   const int* __restrict__ prefix = items.host_B >= 0 ? items.prefix : ws.item_prefix;
   const int N = prefix[b.B];
   const int lo = (int)((int64_t)blockIdx.x * N / gridDim.x);
@@ -428,9 +434,6 @@ __global__ void __launch_bounds__(kFp8 ? kT5ThreadsFp8 : kT5Threads, kFp8 ? kFp8
   } else if (warp < 4) {
     // ------------------------------------------------------------ epilogue
     const int row = warp * 32 + lane;  // TMEM lane = key row within the item
-    // the set of completion counters the next launch uses starts at zero
-    if (done_clear && blockIdx.x == 0)
-      for (int i = row; i < b.B; i += 128) done_clear[i] = 0;
     int job = 0;
     ReqCursor cur;
     cur.init(prefix, b.B, lo);

@@ -453,6 +453,52 @@ def test_steps_without_indexer_work_between_selecting_steps():
     dec.close()
 
 
+def test_counter_sets_after_a_smaller_batch():
+    # A publishing launch zeroes the other counter set for the next one.  When
+    # a smaller batch comes between two larger ones, the entries past the
+    # small batch must be cleared as well: otherwise the third step's Top-K
+    # blocks of those requests find the first step's counts already at their
+    # target and select from the scores as they stand (the first step's).
+    # The third step must equal the same batch run on a fresh handle.
+    wl = WORKLOADS["topk_b16_l8192"]
+    cfg = wl.cfg
+    lens = [8192, 6000, 4097, 8192, 3000, 7000, 2500, 8000]
+    big1 = to_device(make_batch(wl, lens=lens, seed=601), DEV)
+    small = to_device(make_batch(wl, lens=[8192, 5000], seed=602), DEV)
+    big2 = to_device(make_batch(wl, lens=lens, seed=603), DEV)
+    lt = torch.tensor(lens, dtype=torch.int32)
+    B = len(lens)
+
+    def outputs(bs):
+        return (torch.empty(bs, 1, cfg.H, cfg.V, dtype=cfg.torch_dtype, device=DEV),
+                torch.empty(bs, 1, cfg.topk, dtype=torch.int32, device=DEV),
+                torch.empty(bs, 1, dtype=torch.int32, device=DEV))
+
+    fresh = csa.Decoder(cfg, B, 1, 8192)
+    o_ref, i_ref, c_ref = outputs(B)
+    fresh.decode_step(csa.make_batch_struct(big2, lt), o_ref, None, i_ref, c_ref)
+    torch.cuda.synchronize()
+    assert fresh.status() == csa.CSA_OK, csa.last_error()
+    fresh.close()
+
+    ls = torch.tensor([8192, 5000], dtype=torch.int32)  # host lengths, alive while used
+    dec = csa.Decoder(cfg, B, 1, 8192)
+    for rep in range(3):
+        o, i, c = outputs(B)
+        dec.decode_step(csa.make_batch_struct(big1, lt), o, None, i, c)
+        o2, i2, c2 = outputs(2)
+        dec.decode_step(csa.make_batch_struct(small, ls), o2, None, i2, c2)
+        o, i, c = outputs(B)
+        o.fill_(float("nan"))
+        dec.decode_step(csa.make_batch_struct(big2, lt), o, None, i, c)
+        torch.cuda.synchronize()
+        assert dec.status() == csa.CSA_OK, csa.last_error()
+        assert torch.equal(i, i_ref), f"repetition {rep}"
+        assert torch.equal(c, c_ref)
+        assert torch.equal(o, o_ref)
+    dec.close()
+
+
 def test_empty_batch_is_a_noop():
     wl = WORKLOADS["bypass_b16_l256"]
     hb = make_batch(wl, lens=[256])
