@@ -499,6 +499,62 @@ def test_counter_sets_after_a_smaller_batch():
     dec.close()
 
 
+@pytest.mark.parametrize("name,maxB,max_len", [("topk_b16_l8192", 8, 8192),
+                                               ("multitoken_hca_b16_s8", 4, 16384)])
+def test_random_batch_sequence_matches_fresh_handles(name, maxB, max_len):
+    # Every piece of state that outlives a step (counter sets, ready flags and
+    # their epochs, work lists, scores, partials) must not leak into the next
+    # one: one handle runs a seeded random sequence of batches of different
+    # sizes, lengths and data (one all-bypass), with and without host
+    # lengths, and each step must equal that batch run alone on a fresh
+    # handle in the same launch form, bit for bit.  (The two forms may differ
+    # in the last bits: with host lengths the tile CTAs' job split favours
+    # the CTAs that start while Top-K runs, which moves segment boundaries
+    # and so the merge's rounding.)  Single-token steps start Top-K per
+    # request on the indexer's counters; multi-token steps wait for the
+    # indexer grid and add the heavy-compression stream.
+    wl = WORKLOADS[name]
+    cfg = wl.cfg
+    S = wl.S
+    rng = np.random.default_rng(77)
+    bypass_len = cfg.topk * cfg.ratio - S  # every query's vis <= K
+    batches = []
+    for i in range(6):
+        B = int(rng.integers(1, maxB + 1))
+        hi = bypass_len if i == 2 else max_len  # batch 2: every query bypasses scoring
+        lens = [int(x) for x in rng.integers(S, hi + 1, size=B)]
+        batches.append((to_device(make_batch(wl, lens=lens, seed=700 + i), DEV),
+                        torch.tensor(lens, dtype=torch.int32)))
+
+    def run(dec, db, lh):
+        B = int(db["B"])
+        o = torch.full((B, S, cfg.H, cfg.V), float("nan"), dtype=cfg.torch_dtype, device=DEV)
+        i = torch.full((B, S, cfg.topk), -7, dtype=torch.int32, device=DEV)
+        c = torch.full((B, S), -7, dtype=torch.int32, device=DEV)
+        dec.decode_step(csa.make_batch_struct(db, lh), o, None, i, c)
+        torch.cuda.synchronize()
+        assert dec.status() == csa.CSA_OK, csa.last_error()
+        return o, i, c
+
+    ref = {}
+    for k, (db, lh) in enumerate(batches):
+        for host in (True, False):
+            fresh = csa.Decoder(cfg, maxB, S, max_len)
+            ref[k, host] = run(fresh, db, lh if host else None)
+            fresh.close()
+    dec = csa.Decoder(cfg, maxB, S, max_len)
+    for step in range(24):
+        k = int(rng.integers(0, len(batches)))
+        db, lh = batches[k]
+        host = step % 3 != 0
+        o, i, c = run(dec, db, lh if host else None)
+        r = ref[k, host]
+        assert torch.equal(i, r[1]), f"step {step}, batch {k}, host lengths {host}"
+        assert torch.equal(c, r[2]), f"step {step}, batch {k}, host lengths {host}"
+        assert torch.equal(o, r[0]), f"step {step}, batch {k}, host lengths {host}"
+    dec.close()
+
+
 def test_empty_batch_is_a_noop():
     wl = WORKLOADS["bypass_b16_l256"]
     hb = make_batch(wl, lens=[256])
