@@ -5,6 +5,8 @@ for elements whose oracle score is within 1e-6 (relative) of the K-th
 oracle score; attention outputs within 2e-2 max-abs / 1e-2 mean-abs of the
 fp64 oracle for bf16 inputs and 1e-5 for the fp32 workload.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -500,6 +502,7 @@ def test_counter_sets_after_a_smaller_batch():
 
 
 @pytest.mark.parametrize("name,maxB,max_len", [("topk_b16_l8192", 8, 8192),
+                                               ("topk_b16_l8192 fp8", 8, 8192),
                                                ("multitoken_hca_b16_s8", 4, 16384)])
 def test_random_batch_sequence_matches_fresh_handles(name, maxB, max_len):
     # Every piece of state that outlives a step (counter sets, ready flags and
@@ -512,8 +515,11 @@ def test_random_batch_sequence_matches_fresh_handles(name, maxB, max_len):
     # the CTAs that start while Top-K runs, which moves segment boundaries
     # and so the merge's rounding.)  Single-token steps start Top-K per
     # request on the indexer's counters; multi-token steps wait for the
-    # indexer grid and add the heavy-compression stream.
-    wl = WORKLOADS[name]
+    # indexer grid and add the heavy-compression stream.  "fp8": the same
+    # with E4M3 indexer keys and per-row scales.
+    wl = WORKLOADS[name.split()[0]]
+    if name.endswith("fp8"):
+        wl = dataclasses.replace(wl, cfg=dataclasses.replace(wl.cfg, idx_dtype="fp8"))
     cfg = wl.cfg
     S = wl.S
     rng = np.random.default_rng(77)
