@@ -300,12 +300,14 @@ def run_e2e(args, csa, dec, hb, copies, lens_host, out, idx, cnt, stream, dev, T
     for k in keys:
         o, nb = offs[k]
         host_buf[o:o + nb].copy_(hb[k].contiguous().view(-1).view(torch.uint8))
-    # Steps go in groups of G: a group's uploads are issued while the previous
-    # group runs, and the compute stream meets the copy streams only between
-    # groups (one wait before a group, one event after it), so the kernels of
-    # a group's consecutive steps stay chained by programmatic dependent
-    # launch.  Every step still uploads its own inputs and reads back its own
-    # output.
+    # Steps go in groups of up to G: a group's uploads are issued while the
+    # previous group runs, and the compute stream meets the copy streams only
+    # between groups (one wait before a group, one event after it), so the
+    # kernels of a group's consecutive steps stay chained by programmatic
+    # dependent launch.  The first and the last group hold one step, so that
+    # only one step's upload precedes the first kernels and only one step's
+    # read-back follows the last.  Every step still uploads its own inputs and
+    # reads back its own output.
     G = 4
     nbuf = 2 * G
     dev_bufs = [torch.empty(tot, dtype=torch.uint8, device=dev) for _ in range(nbuf)]
@@ -328,47 +330,58 @@ def run_e2e(args, csa, dec, hb, copies, lens_host, out, idx, cnt, stream, dev, T
     x_done = [torch.cuda.Event() for _ in range(2)]
     d2h_done = [torch.cuda.Event() for _ in range(2)]
 
-    def upload(g):  # group g's inputs into buffers (g % 2) * G ...
+    def upload(g, size):  # group g's inputs into buffers (g % 2) * G ...
         p = g % 2
         if g >= 2:
             up.wait_event(x_done[p])          # group g - 2 has run on these buffers
         with torch.cuda.stream(up):
-            for t in range(G):
+            for t in range(size):
                 dev_bufs[p * G + t].copy_(host_buf, non_blocking=True)
         h2d_done[p].record(up)
 
-    def run_group(g):
+    def run_group(g, size):
         p = g % 2
         stream.wait_event(h2d_done[p])
         if g >= 2:
             stream.wait_event(d2h_done[p])    # group g - 2's outputs have been read back
-        for t in range(G):
+        for t in range(size):
             dec.decode_step(structs[p * G + t], outs[p * G + t], None, idx, cnt, stream)
         x_done[p].record(stream)
         down.wait_event(x_done[p])
         with torch.cuda.stream(down):
-            for t in range(G):
+            for t in range(size):
                 out_host[p * G + t].copy_(outs[p * G + t], non_blocking=True)
         d2h_done[p].record(down)
+        return out_host[p * G + size - 1]
 
-    def run_groups(n):
-        upload(0)
-        for g in range(n):
-            if g + 1 < n:
-                upload(g + 1)
-            run_group(g)
+    def group_sizes(n):  # n steps: 1, G, G, ..., the rest, 1
+        if n <= 2:
+            return [1] * n
+        mid, sizes = n - 2, [1]
+        sizes += [G] * (mid // G) + ([mid % G] if mid % G else [])
+        return sizes + [1]
 
-    run_groups(max((args.warmup + G - 1) // G, 2))
+    def run_steps(n):
+        sizes = group_sizes(n)
+        upload(0, sizes[0])
+        last = None
+        for g, size in enumerate(sizes):
+            if g + 1 < len(sizes):
+                upload(g + 1, sizes[g + 1])
+            last = run_group(g, size)
+        return last
+
+    run_steps(max(args.warmup, 2 * G))
     torch.cuda.synchronize()
-    ngroups = max((args.steps + G - 1) // G, 1)
+    nsteps = max(args.steps, 1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(up)
-    run_groups(ngroups)
+    last = run_steps(nsteps)
     e1.record(down)
     torch.cuda.synchronize()
-    ems = reduce_max(e0.elapsed_time(e1) / (ngroups * G), dist, dev)
+    ems = reduce_max(e0.elapsed_time(e1) / nsteps, dist, dev)
     # the pipelined step computes what the device-resident step computes
-    if not torch.equal(out_host[((ngroups - 1) % 2) * G + G - 1], out.cpu()):
+    if not torch.equal(last, out.cpu()):
         raise RuntimeError("end-to-end output differs from the device-resident step")
     return {"value": job_throughput(T, ws, ems), "unit": "queries/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ems,
@@ -408,8 +421,9 @@ def measure(args, name, steps, warmup, dev, ws, rank, dist, with_e2e, with_cpu):
     def step(i):
         dec.decode_step(structs[i % len(structs)], out, None, idx, cnt, stream)
 
-    for i in range(max(warmup, 3)):
-        step(i)
+    # a first step gives the status, the launch count and the selection the
+    # algorithmic bytes are counted from
+    step(0)
     torch.cuda.synchronize()
     st = dec.status()
     if st != csa.CSA_OK:
@@ -418,12 +432,16 @@ def measure(args, name, steps, warmup, dev, ws, rank, dist, with_e2e, with_cpu):
     sel = idx.cpu().numpy().reshape(T, cfg.topk)
     bytes_ = step_bytes(cfg, lens, S, sel)
 
-    # ---- timed region: K steps
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    # ---- W warm-up steps right before the timed region (the clock sampler is
+    # started first: its start-up, and the host work above, leave the GPU idle,
+    # which a timed region that follows directly would pay for), then K steps
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(dev.index) as clk:
+        for i in range(max(warmup, 3)):
+            step(i)
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         ev0.record(stream)
         for i in range(steps):
             step(i)
