@@ -255,6 +255,53 @@ def test_topk_select_bit_exact_rows_past_16384():
         assert gi[i].tolist() == ref.tolist(), f"{name} n={s.size}"
 
 
+def _nonfinite_row(rng, n, f_nan, f_ninf=0.0, n_pinf=0):
+    s = rng.standard_normal(n).astype(np.float32)
+    pos = rng.permutation(n)
+    a, b = int(f_nan * n), int((f_nan + f_ninf) * n)
+    s[pos[:a]] = np.nan
+    s[pos[a:b]] = -np.inf
+    s[pos[b:b + n_pinf]] = np.inf
+    return s
+
+
+@pytest.mark.parametrize("max_context,ld,sizes", [(8192, 2048, (2000, 600, 1500, 2048)),
+                                                  (65536, 16384, (16384, 700, 5000, 3000)),
+                                                  (131072, 32768, (20000, 17000, 18000, 16500))])
+def test_topk_select_nonfinite_scores(max_context, ld, sizes):
+    # NaN scores rank below every other score (-inf included), +inf above;
+    # equal keys (every NaN is one key) go to the lower index.  The oracle
+    # takes no NaN, so its input maps -inf and NaN to two values below every
+    # finite float, in that order.  Each of the three Top-K kernels (two and
+    # sixteen keys per thread in registers, rows in shared memory) on rows
+    # with scattered NaN, fewer finite scores than K, only NaN, and -inf / +inf
+    # mixed in.
+    rng = np.random.default_rng(max_context)
+    cfg = BF16_CFG
+    n1, n2, n3, n4 = sizes
+    cases = [("nan_10pct", _nonfinite_row(rng, n1, 0.10, n_pinf=3)),
+             ("finite_below_k", _nonfinite_row(rng, n2, 1.0 - 300.0 / n2)),
+             ("all_nan", np.full(n3, np.nan, np.float32)),
+             ("nan_and_ninf", _nonfinite_row(rng, n4, 0.45, f_ninf=0.45, n_pinf=5))]
+    dec = csa.Decoder(cfg, len(cases), 1, max_context)
+    sc = np.full((len(cases), ld), np.nan, np.float32)
+    n = np.zeros(len(cases), np.int32)
+    for i, (_, s) in enumerate(cases):
+        sc[i, :s.size] = s
+        n[i] = s.size
+    idx = torch.empty(len(cases), cfg.topk, dtype=torch.int32, device=DEV)
+    cnt = torch.empty(len(cases), dtype=torch.int32, device=DEV)
+    dec.topk_select(torch.from_numpy(sc).to(DEV), torch.from_numpy(n).to(DEV), idx, cnt)
+    assert dec.status() == csa.CSA_OK
+    gi, gc = idx.cpu().numpy(), cnt.cpu().numpy()
+    for i, (name, s) in enumerate(cases):
+        d = s.astype(np.float64)
+        d = np.where(np.isnan(d), -1e301, np.where(np.isneginf(d), -1e300, d))
+        ref = oracle.topk(d, cfg.topk)
+        assert gc[i] == ref.size, name
+        assert gi[i, :ref.size].tolist() == ref.tolist(), f"{name} n={s.size}"
+
+
 # ---------------------------------------------------------------------------
 # edge cases: tiny and ragged lengths, bypass boundary, maximum length, poison
 
