@@ -185,9 +185,10 @@ CSA_API int csa_indexer_topk(csa_handle *h, const csa_batch *b, int32_t *topk_id
  * log-sum-exp of the merged streams, may be NULL.  Accuracy of lse_out on the
  * bf16 tensor-core path: the softmax weights are rounded to bf16 (the tensor
  * cores' operand type) before they are summed, so ln(sum) may differ from the
- * exact value by up to u/(1-u) ~ 1.96e-3 with u = 2^-9; this bound comes from
- * that operand choice, not from the method, and is the tolerance the parity
- * tests apply to lse_out (the fp32 path: 1e-5). */
+ * exact value by up to -ln(1-u) ~ 3.91e-3 with u = 2^-8 (bf16's unit
+ * roundoff); this bound comes from that operand choice, not from the method,
+ * and (with fp32 noise, 4e-3) is the tolerance the parity tests apply to
+ * lse_out (the fp32 path: 1e-5). */
 CSA_API int csa_sparse_attn(csa_handle *h, const csa_batch *b, const int32_t *topk_idx,
                     const int32_t *topk_cnt, void *out, float *lse_out, void *stream);
 

@@ -23,7 +23,7 @@ from compressed_sparse_attention_indexer_gb300 import build as csa_build
 from compressed_sparse_attention_indexer_gb300 import csa
 from compressed_sparse_attention_indexer_gb300.workloads import (
     BF16_CFG, WORKLOADS, Workload, make_batch, to_device)
-from helpers import TOL_BF16, assert_close, assert_topk_sets
+from helpers import TOL_BF16, TOL_LSE_BF16, assert_close, assert_topk_sets
 
 FP8_CFG = replace(BF16_CFG, idx_dtype="fp8")
 DEV = "cuda:0"
@@ -132,7 +132,7 @@ def _check(wl, hb, g, ref=None, what=""):
     assert_topk_sets(g["idx"], g["cnt"], ref, lambda q: oracle.query_scores(cfg, hb, q // S, q % S),
                      cfg.topk, what)
     assert_close(g["out"], ref["out"], TOL_BF16, what + " out")
-    assert_close(g["lse"], ref["lse"], (2.5e-3, 5e-4), what + " lse")
+    assert_close(g["lse"], ref["lse"], TOL_LSE_BF16, what + " lse")
     return ref
 
 
