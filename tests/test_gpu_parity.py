@@ -500,21 +500,28 @@ def test_steps_without_indexer_work_between_selecting_steps():
     dec.close()
 
 
-@pytest.mark.parametrize("name,lens", [("topk_b16_l8192", [8192, 5000, 2100, 300]),
-                                       ("multitoken_hca_b16_s8", [32768, 9000])])
-def test_peaked_softmax_against_oracle(name, lens):
-    # Query heads drawn with standard deviation 16 instead of 1: scores of
-    # standard deviation ~16 (raw rows) and ~8 (compressed rows), so a job's
-    # maximum often exceeds a segment's reference maximum by more than 8 in
-    # log2 units and the accumulated output is rescaled in TMEM, and the
-    # softmax is dominated by a few rows.  Both launch forms, against the
-    # oracle.
+@pytest.mark.parametrize("name,lens,dists,what", [
+    ("topk_b16_l8192", [8192, 5000, 2100, 300], Dists(q=16.0), "peaked"),
+    ("multitoken_hca_b16_s8", [32768, 9000], Dists(q=16.0), "peaked"),
+    ("topk_b16_l8192", [8192, 5000, 2100, 300], Dists(q=0.0), "flat"),
+    ("topk_b16_l8192", [8192, 5000, 2100, 300], Dists(w_hi=0.0), "zero_scores")])
+def test_softmax_and_score_extremes_against_oracle(name, lens, dists, what):
+    # peaked: query heads drawn with standard deviation 16 instead of 1:
+    # scores of standard deviation ~16 (raw rows) and ~8 (compressed rows), so
+    # a job's maximum often exceeds a segment's reference maximum by more than
+    # 8 in log2 units and the accumulated output is rescaled in TMEM, and the
+    # softmax is dominated by a few rows.  flat: q = 0, every attention score
+    # 0, the output the mean of the rows and lse = ln(rows).  zero_scores:
+    # w = 0, every indexer score 0, so the selection is the first K rows
+    # (ties to the lower index), checked exactly.  Both launch forms.
     wl = WORKLOADS[name]
-    hb = make_batch(wl, lens=lens, dists=Dists(q=16.0))
+    hb = make_batch(wl, lens=lens, dists=dists)
     ref = None
     for host in (False, True):
         g = run_step(wl, hb, host_lens=host)
-        ref = check_against_oracle(wl, hb, g, ref=ref, what=f"{name} peaked host={host}")
+        ref = check_against_oracle(wl, hb, g, ref=ref, what=f"{name} {what} host={host}")
+        if what == "zero_scores":
+            np.testing.assert_array_equal(g["idx"], ref["topk_idx"].reshape(g["idx"].shape))
 
 
 def test_counter_sets_after_a_smaller_batch():
