@@ -137,10 +137,20 @@ def _check(wl, hb, g, ref=None, what=""):
 
 
 @pytest.mark.gpu
-def test_fp8_indexer_scores_against_oracle():
+@pytest.mark.parametrize("signs", [False, True])
+def test_fp8_indexer_scores_against_oracle(signs):
+    # signs: every third row's scale negated and every seventh row's zero, so
+    # that the kernel's per-dot-product scaling (a scale that is not
+    # positive cannot be moved out of the ReLU) is checked beside the
+    # factored one
     _gpu()
     wl = Workload("fp8-scores", FP8_CFG, B=4, S=1, L=1, seed=33)
     hb = make_batch(wl, lens=[8192, 300, 1029, 4097], gap_rows=2)
+    if signs:
+        sc_ = hb["idx_scale"].clone()
+        sc_[::3] = -sc_[::3]
+        sc_[::7] = 0.0
+        hb["idx_scale"] = sc_
     db = to_device(hb, DEV)
     dec = csa.Decoder(FP8_CFG, 4, 1, 8192)
     ld = 8192 // 4
