@@ -524,6 +524,24 @@ def test_softmax_and_score_extremes_against_oracle(name, lens, dists, what):
             np.testing.assert_array_equal(g["idx"], ref["topk_idx"].reshape(g["idx"].shape))
 
 
+def test_large_k_takes_the_warp_mma_attention():
+    # K = 4096 gives a query up to 2 + 64 jobs of 64 rows, more than the
+    # tcgen05 merge takes (64): the step's attention then runs on the
+    # warp-MMA kernel by itself, with the tcgen05 indexer and the register
+    # Top-K (selection of 4096 of up to 10000 rows) before it.  Requests past,
+    # below and at the bypass boundary, both launch forms, against the oracle.
+    cfg = dataclasses.replace(BF16_CFG, topk=4096)
+    wl = Workload("k4096", cfg, B=3, S=1, L=1, seed=4096)
+    hb = make_batch(wl, lens=[40000, 16384, 9000])
+    ref = None
+    for host in (False, True):
+        g = run_step(wl, hb, max_context=40960, host_lens=host)
+        ref = check_against_oracle(wl, hb, g, ref=ref, what=f"K=4096 host={host}")
+        if host:  # indexer, Top-K and one attention launch (not tile + merge)
+            assert g["dec"].last_launch_count() == 3
+    assert (ref["cnt"] == [4096, 4096, 2250]).all()
+
+
 def test_counter_sets_after_a_smaller_batch():
     # A publishing launch zeroes the other counter set for the next one.  When
     # a smaller batch comes between two larger ones, the entries past the
