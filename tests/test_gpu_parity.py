@@ -542,6 +542,21 @@ def test_large_k_takes_the_warp_mma_attention():
     assert (ref["cnt"] == [4096, 4096, 2250]).all()
 
 
+def test_long_context_takes_the_shared_memory_topk():
+    # max_context 131072: rows of up to 32768 compressed scores, past what the
+    # register Top-K holds, so the step selects with the shared-memory kernel
+    # (float scores from the indexer, the Top-K blocks still started per
+    # request and publishing ready flags to the attention).  Both launch
+    # forms, against the oracle.
+    wl = WORKLOADS["topk_b16_l8192"]
+    hb = make_batch(wl, lens=[131072, 100001, 70000, 5000], seed=131)
+    ref = None
+    for host in (False, True):
+        g = run_step(wl, hb, max_context=131072, host_lens=host)
+        ref = check_against_oracle(wl, hb, g, ref=ref, what=f"long context host={host}")
+    assert (ref["vis"] == [32768, 25000, 17500, 1250]).all()
+
+
 def test_counter_sets_after_a_smaller_batch():
     # A publishing launch zeroes the other counter set for the next one.  When
     # a smaller batch comes between two larger ones, the entries past the
