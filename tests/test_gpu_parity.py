@@ -368,6 +368,21 @@ def test_multi_token_small():
     check_against_oracle(wl, hb, g, what="multi-token")
 
 
+@pytest.mark.parametrize("S", [2, 3, 7])
+def test_multi_token_query_groups(S):
+    # S queries per request on the tensor-core shape: the tcgen05 indexer
+    # scores up to four queries of a request per MMA group (N = 64 per
+    # query), so S = 2, 3, 7 give groups of 2, 3 and 4 + 3; requests that
+    # bypass scoring, that cross the bypass boundary inside the chunk and
+    # that select, both launch forms, against the oracle.
+    wl = Workload("mt-groups", BF16_CFG, B=4, S=S, L=1, seed=200 + S)
+    hb = make_batch(wl, lens=[2048 + S - 2, 9000, 700, 30001], gap_rows=1)
+    ref = None
+    for host in (False, True):
+        g = run_step(wl, hb, max_context=30001, host_lens=host)
+        ref = check_against_oracle(wl, hb, g, ref=ref, what=f"S={S} host={host}")
+
+
 def test_generic_shapes_simt_path():
     # shapes outside the tensor-core set (bf16 and fp32) run on the SIMT kernels
     for dt in ("bf16", "f32"):
