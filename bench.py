@@ -281,6 +281,16 @@ def load_traffic(kernel: str, workload: str):
     return d.get("dram_bytes_per_launch")
 
 
+def e2e_group_sizes(n: int, G: int) -> list:
+    """The end-to-end loop's groups for n steps: one step, then groups of G,
+    the rest, and one step (exactly n steps; no group empty or above G)."""
+    if n <= 2:
+        return [1] * n
+    mid, sizes = n - 2, [1]
+    sizes += [G] * (mid // G) + ([mid % G] if mid % G else [])
+    return sizes + [1]
+
+
 def run_e2e(args, csa, dec, hb, copies, lens_host, out, idx, cnt, stream, dev, T, ws, dist):
     """The same step through the public API with host buffers, as a serving
     loop runs it: every step copies its activations (q, q_idx, w, lengths,
@@ -354,15 +364,8 @@ def run_e2e(args, csa, dec, hb, copies, lens_host, out, idx, cnt, stream, dev, T
         d2h_done[p].record(down)
         return out_host[p * G + size - 1]
 
-    def group_sizes(n):  # n steps: 1, G, G, ..., the rest, 1
-        if n <= 2:
-            return [1] * n
-        mid, sizes = n - 2, [1]
-        sizes += [G] * (mid // G) + ([mid % G] if mid % G else [])
-        return sizes + [1]
-
     def run_steps(n):
-        sizes = group_sizes(n)
+        sizes = e2e_group_sizes(n, G)
         upload(0, sizes[0])
         last = None
         for g, size in enumerate(sizes):

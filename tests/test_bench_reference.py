@@ -42,3 +42,17 @@ def test_reference_arm_other_ranks_exit_quietly():
     assert _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}) == []
     lines = _run({"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"})
     assert len(lines) == 1 and lines[0]["n_gpus"] == 2
+
+
+def test_e2e_groups_cover_every_step_once():
+    # the end-to-end loop's group plan: exactly n steps, no group empty or
+    # above G, one step first and last (so one upload precedes the first
+    # kernels and one read-back follows the last)
+    sys.path.insert(0, ROOT)
+    import bench
+    for G in (1, 4, 8):
+        for n in range(0, 41):
+            g = bench.e2e_group_sizes(n, G)
+            assert sum(g) == n and all(1 <= x <= G for x in g), (n, G, g)
+            if n >= 2:
+                assert g[0] == 1 and g[-1] == 1
